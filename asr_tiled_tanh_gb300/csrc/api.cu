@@ -1,0 +1,466 @@
+// api.cu -- the C ABI of librnnt_gb300 (declared in include/rnnt.h).
+//
+// Host side only: argument checks, the layout of the caller's `saved` and
+// `ws` buffers, and the order of kernel launches on the caller's stream.
+// Every arithmetic step runs in this library's CUDA kernels.
+//
+// Forward (Flash RNN-T blog, "Compute it, use it, make room"; sample-wise
+// transducer paper §2):
+//   1. validate lengths/labels, per-sample tile counts and offsets;
+//   2. joint projections pA = hA W^A^T + b^Z, pL = hL W^L^T (the matrix
+//      products of Eq. 3 hoisted out of the lattice: they depend on t or u
+//      only);
+//   3. per tile: z = tanh(pA[t] + pL[u]), scores h = W^O z + b^O, and from
+//      the scores only ln P_D and the blank/label log-probabilities (Eq. 7);
+//   4. alpha/beta and the loss (Eq. 8-9).
+// Backward (Flash RNN-T: recompute each tile, overwrite its scores with their
+// gradients; sample-wise paper §4: accumulate the parameter gradients):
+//   per tile: recompute z and h, dh in place (Eq. 10), dz = dh W^O,
+//   da = dz (1 - z^2) summed over u into dA[b,t] and over t into dLr[b,u],
+//   dW^O += dh^T z, db^O += sum dh; then dh^A = dA W^A, dW^A = dA^T hA,
+//   dh^L = dLr W^L, dW^L = dLr^T hL, db^Z = sum dA.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "kernels.h"
+#include "profile.h"
+#include "tc.h"
+
+using namespace rnnt;
+
+namespace {
+
+constexpr long long kMaxI32 = 2147483647LL;
+
+bool make_plan(const rnnt_dims* d, Plan* p) {
+  if (!d) return false;
+  if (d->B < 0 || d->T < 1 || d->U1 < 1 || d->HA < 1 || d->HL < 1 || d->H < 1 || d->V < 1)
+    return false;
+  if (d->blank < 0 || d->blank >= d->V) return false;
+  if (d->dtype != RNNT_F32 && d->dtype != RNNT_BF16) return false;
+  if (d->mode != RNNT_TILED && d->mode != RNNT_UNTILED) return false;
+  if (d->tile_cells < 0) return false;
+  std::memset(p, 0, sizeof(*p));
+  p->B = d->B; p->T = d->T; p->U1 = d->U1; p->HA = d->HA; p->HL = d->HL; p->H = d->H;
+  p->V = d->V; p->blank = d->blank; p->dtype = d->dtype; p->mode = d->mode;
+  p->tc = (d->dtype == RNNT_BF16) && tc_path_enabled();
+  p->max_tiles = (long long)d->B * cdiv(d->T, TT) * cdiv(d->U1, TU);
+  if (p->max_tiles > kMaxI32 / TILE) return false;
+  if ((long long)d->B * d->T * d->U1 > kMaxI32 * 8LL) return false;
+  p->zelem = p->tc ? 2 : 4;
+  p->helem = p->tc ? 2 : 4;
+  const size_t B = d->B, T = d->T, U1 = d->U1, H = d->H, V = d->V, HA = d->HA, HL = d->HL;
+  if (d->mode == RNNT_UNTILED) {
+    p->chunk_tiles = p->max_tiles;
+  } else {
+    long long ct;
+    if (d->tile_cells > 0) {
+      ct = cdiv(d->tile_cells, TILE);
+    } else {
+      // default: about 64 MiB of tile buffers, at least one tile per SM
+      const long long per_tile = (long long)TILE * (H * p->zelem + V * p->helem);
+      ct = (64LL << 20) / per_tile;
+      ct = ct / 152 * 152;
+      if (ct < 152) ct = 152;
+    }
+    p->chunk_tiles = ct < p->max_tiles ? ct : p->max_tiles;
+  }
+  if (p->chunk_tiles < 1) p->chunk_tiles = 1;
+  p->chunk_rows = p->chunk_tiles * TILE;
+  const size_t rows = (size_t)p->chunk_rows;
+
+  size_t o = 0;
+  auto put = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  p->s_status = put(sizeof(SavedHeader));
+  p->s_prefix = put(4 * (B + 1));
+  p->s_lnP = put(4 * (B ? B : 1));
+  const size_t ncell = B * T * U1;
+  p->s_lpb = put(4 * ncell);
+  p->s_lpl = put(4 * ncell);
+  p->s_lnPD = put(4 * ncell);
+  p->s_alpha = put(4 * ncell);
+  p->s_beta = put(4 * ncell);
+  if (d->mode == RNNT_UNTILED) {
+    p->s_z = put(rows * H * p->zelem);
+    p->s_h = put(rows * V * p->helem);
+  }
+  p->s_total = o;
+
+  o = 0;
+  p->w_pA = put(4 * B * T * H);
+  p->w_pL = put(4 * B * U1 * H);
+  p->w_dA = put(4 * B * T * H);
+  p->w_dLr = put(4 * B * U1 * H);
+  if (d->mode == RNNT_TILED) {
+    p->w_z = put(rows * H * p->zelem);
+    p->w_h = put(rows * V * p->helem);
+  }
+  if (!p->tc) {
+    p->w_dz = put(4 * rows * H);
+  } else {
+    p->w_dA16 = put(2 * B * T * H);
+    p->w_dLr16 = put(2 * B * U1 * H);
+    p->w_hAm = put(2 * B * T * HA);
+    p->w_hLm = put(2 * B * U1 * HL);
+  }
+  p->w_len = put(8 * (B ? B : 1));  // effective lengths of accepted samples (2 x int32 [B])
+  p->w_total = o;
+  return true;
+}
+
+SavedView saved_view(const Plan& p, void* saved) {
+  char* s = (char*)saved;
+  SavedView v;
+  SavedHeader* hdr = (SavedHeader*)(s + p.s_status);
+  v.status = &hdr->status;
+  v.total_tiles = &hdr->total_tiles;
+  v.prefix = (int32_t*)(s + p.s_prefix);
+  v.lnP = (float*)(s + p.s_lnP);
+  v.lpb = (float*)(s + p.s_lpb);
+  v.lpl = (float*)(s + p.s_lpl);
+  v.lnPD = (float*)(s + p.s_lnPD);
+  v.alpha = (float*)(s + p.s_alpha);
+  v.beta = (float*)(s + p.s_beta);
+  return v;
+}
+
+Shape shape_of(const Plan& p) { return Shape{p.B, p.T, p.U1, p.H, p.V, p.blank}; }
+
+bool aligned(const void* x) { return ((uintptr_t)x & (ALIGN - 1)) == 0; }
+
+#define RNNT_CHECK(expr)                               \
+  do {                                                 \
+    cudaError_t e_ = (expr);                           \
+    if (e_ != cudaSuccess) {                           \
+      if (getenv("RNNT_VERBOSE"))                      \
+        fprintf(stderr, "rnnt: %s -> %s (%s:%d)\n", #expr, cudaGetErrorString(e_), \
+                __FILE__, __LINE__);                   \
+      return RNNT_ERR_CUDA;                            \
+    }                                                  \
+  } while (0)
+
+// Launch with an optional profiling bracket (see include/rnnt_profile.h).
+#define LAUNCH(name, expr)              \
+  do {                                  \
+    rnnt::ProfScope ps_(name, st);      \
+    RNNT_CHECK(expr);                   \
+  } while (0)
+
+// Number of chunks to walk.  When every possible tile fits in one chunk no
+// synchronization is needed; otherwise read the actual tile count.
+rnnt_status chunk_count(const Plan& p, const SavedView& sv, cudaStream_t st, long long* n) {
+  const long long bound = cdiv(p.max_tiles, p.chunk_tiles);
+  if (bound <= 1) {
+    *n = bound;
+    return RNNT_OK;
+  }
+  int32_t total = 0;
+  RNNT_CHECK(cudaMemcpyAsync(&total, sv.total_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  RNNT_CHECK(cudaStreamSynchronize(st));
+  *n = cdiv(total, p.chunk_tiles);
+  return RNNT_OK;
+}
+
+ChunkArgs chunk_args(const Plan& p, const SavedView& sv, long long k, const int32_t* labels,
+                     const int32_t* T_len, const int32_t* U_len) {
+  ChunkArgs c;
+  c.sh = shape_of(p);
+  c.first_tile = k * p.chunk_tiles;
+  c.ntiles = p.chunk_tiles;
+  c.T_len = T_len;
+  c.U_len = U_len;
+  c.labels = labels;
+  c.sv = sv;
+  return c;
+}
+
+// Projections pA = hA W^A^T + b^Z [B*T,H] and pL = hL W^L^T [B*U1,H], fp32.
+rnnt_status projections(const Plan& p, const void* hA, const void* hL, const rnnt_params* pr,
+                        float* pA, float* pL, cudaStream_t st) {
+  const int bf = p.dtype == RNNT_BF16;
+  if (p.tc) {
+    RNNT_CHECK(tc_projection(p, hA, pr->WA, pr->bZ, p.B * p.T, p.HA, pA, st));
+    RNNT_CHECK(tc_projection(p, hL, pr->WL, nullptr, p.B * p.U1, p.HL, pL, st));
+    return RNNT_OK;
+  }
+  SimtGemm g{};
+  g.M = p.B * p.T; g.N = p.H; g.K = p.HA;
+  g.A = hA; g.sam = p.HA; g.sak = 1; g.a_bf16 = bf;
+  g.Bm = pr->WA; g.sbk = 1; g.sbn = p.HA; g.b_bf16 = bf;
+  g.C = pA; g.ldc = p.H; g.alpha = 1.f; g.bias = pr->bZ; g.bias_bf16 = bf;
+  LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  g.M = p.B * p.U1; g.K = p.HL;
+  g.A = hL; g.sam = p.HL;
+  g.Bm = pr->WL; g.sbn = p.HL;
+  g.C = pL; g.bias = nullptr;
+  LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  return RNNT_OK;
+}
+
+// Scores of a chunk on the fp32 path: Hs = Z W^O^T + b^O.
+rnnt_status simt_scores(const Plan& p, const rnnt_params* pr, const float* Z, float* Hs,
+                        long long rows, cudaStream_t st) {
+  const int bf = p.dtype == RNNT_BF16;
+  SimtGemm g{};
+  g.M = (int)rows; g.N = p.V; g.K = p.H;
+  g.A = Z; g.sam = p.H; g.sak = 1; g.a_bf16 = 0;
+  g.Bm = pr->WO; g.sbk = 1; g.sbn = p.H; g.b_bf16 = bf;
+  g.C = Hs; g.ldc = p.V; g.alpha = 1.f; g.bias = pr->bO; g.bias_bf16 = bf;
+  LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  return RNNT_OK;
+}
+
+rnnt_status check_common(const rnnt_dims* dims, const void* hA, const void* hL,
+                         const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                         const int32_t* U_len, void* saved, void* ws, size_t ws_bytes,
+                         Plan* p) {
+  if (!make_plan(dims, p)) return RNNT_ERR_INVALID_ARG;
+  if (!pr || !saved || !ws) return RNNT_ERR_INVALID_ARG;
+  if (!aligned(saved) || !aligned(ws)) return RNNT_ERR_INVALID_ARG;
+  if (p->B > 0 && (!hA || !hL || !labels || !T_len || !U_len)) return RNNT_ERR_INVALID_ARG;
+  if (!pr->WA || !pr->WL || !pr->WO) return RNNT_ERR_INVALID_ARG;
+  if (p->U1 > 1024) return RNNT_ERR_UNSUPPORTED_SHAPE;  // one thread per label position
+  if (p->tc) {
+    rnnt_status s = tc_check_shape(*p);
+    if (s != RNNT_OK) return s;
+  }
+  if (ws_bytes < p->w_total) return RNNT_ERR_WORKSPACE_TOO_SMALL;
+  if (p->mode == RNNT_UNTILED) {
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) == cudaSuccess && p->s_total > total_b)
+      return RNNT_ERR_WORKSPACE_TOO_SMALL;
+  }
+  return RNNT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rnnt_saved_bytes(const rnnt_dims* dims) {
+  Plan p;
+  return make_plan(dims, &p) ? p.s_total : 0;
+}
+
+size_t rnnt_workspace_bytes(const rnnt_dims* dims) {
+  Plan p;
+  return make_plan(dims, &p) ? p.w_total : 0;
+}
+
+rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out) {
+  Plan p;
+  if (!out || !make_plan(dims, &p)) return RNNT_ERR_INVALID_ARG;
+  out->status = p.s_status;
+  out->lnP = p.s_lnP;
+  out->lpb = p.s_lpb;
+  out->lpl = p.s_lpl;
+  out->lnPD = p.s_lnPD;
+  out->alpha = p.s_alpha;
+  out->beta = p.s_beta;
+  out->z = p.s_z;
+  out->h = p.s_h;
+  out->total = p.s_total;
+  return RNNT_OK;
+}
+
+const char* rnnt_status_string(rnnt_status s) {
+  switch (s) {
+    case RNNT_OK: return "ok";
+    case RNNT_ERR_INVALID_ARG: return "invalid argument";
+    case RNNT_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case RNNT_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case RNNT_ERR_LENGTH_RANGE: return "length out of range";
+    case RNNT_ERR_LABEL_RANGE: return "label out of range";
+    case RNNT_ERR_TIMEOUT: return "device wait timed out";
+    case RNNT_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
+                     rnnt_stream stream) {
+  Plan p;
+  rnnt_status st0 = check_common(dims, hA, hL, pr, labels, T_len, U_len, saved, ws, ws_bytes, &p);
+  if (st0 != RNNT_OK) return st0;
+  if (p.B > 0 && !loss) return RNNT_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const Shape sh = shape_of(p);
+  SavedView sv = saved_view(p, saved);
+  char* w = (char*)ws;
+  float* pA = (float*)(w + p.w_pA);
+  float* pL = (float*)(w + p.w_pL);
+
+  LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
+  if (p.B == 0) return RNNT_OK;
+  const size_t ncell = (size_t)p.B * p.T * p.U1;
+  LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY, ncell, st));
+  LAUNCH("fill_f32", launch_fill_f32(sv.lpl, -INFINITY, ncell, st));
+  LAUNCH("fill_f32", launch_fill_f32(sv.lnPD, -INFINITY, ncell, st));
+  LAUNCH("fill_f32", launch_fill_f32(sv.alpha, -INFINITY, ncell, st));
+  LAUNCH("fill_f32", launch_fill_f32(sv.beta, -INFINITY, ncell, st));
+  rnnt_status s = projections(p, hA, hL, pr, pA, pL, st);
+  if (s != RNNT_OK) return s;
+
+  const bool untiled = p.mode == RNNT_UNTILED;
+  void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
+  void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
+  if (p.tc) {
+    s = tc_forward_tiles(p, sv, pr, labels, T_len, U_len, pA, pL, untiled ? Z : nullptr,
+                         untiled ? Hs : nullptr, st);
+    if (s != RNNT_OK) return s;
+  } else {
+    long long nch = 0;
+    s = chunk_count(p, sv, st, &nch);
+    if (s != RNNT_OK) return s;
+    for (long long k = 0; k < nch; ++k) {
+      ChunkArgs c = chunk_args(p, sv, k, labels, T_len, U_len);
+      LAUNCH("build_z", launch_build_z(c, pA, pL, Z, 0, st));
+      s = simt_scores(p, pr, (const float*)Z, (float*)Hs, p.chunk_rows, st);
+      if (s != RNNT_OK) return s;
+      LAUNCH("lse_rows", launch_lse_rows(c, (const float*)Hs, st));
+    }
+  }
+  LAUNCH("alpha_beta", launch_alpha_beta(sh, T_len, U_len, sv, loss, st));
+  return RNNT_OK;
+}
+
+rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
+                     float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
+                     void* ws, size_t ws_bytes, rnnt_stream stream) {
+  Plan p;
+  rnnt_status st0 = check_common(dims, hA, hL, pr, labels, T_len, U_len, saved, ws, ws_bytes, &p);
+  if (st0 != RNNT_OK) return st0;
+  cudaStream_t st = (cudaStream_t)stream;
+  SavedView sv = saved_view(p, saved);
+  char* w = (char*)ws;
+  float* pA = (float*)(w + p.w_pA);
+  float* pL = (float*)(w + p.w_pL);
+  float* dA = (float*)(w + p.w_dA);
+  float* dLr = (float*)(w + p.w_dLr);
+  int32_t* Teff = (int32_t*)(w + p.w_len);
+  int32_t* Ueff = Teff + (p.B ? p.B : 1);
+  const int bf = p.dtype == RNNT_BF16;
+  const bool untiled = p.mode == RNNT_UNTILED;
+
+  // Outputs are overwritten; accumulated ones start from zero.
+  if (dWO) LAUNCH("zero", launch_zero(dWO, sizeof(float) * (size_t)p.V * p.H, st));
+  if (dbO) LAUNCH("zero", launch_zero(dbO, sizeof(float) * (size_t)p.V, st));
+  if (dbZ) LAUNCH("zero", launch_zero(dbZ, sizeof(float) * (size_t)p.H, st));
+  if (p.B == 0) {
+    if (dWA) LAUNCH("zero", launch_zero(dWA, sizeof(float) * (size_t)p.H * p.HA, st));
+    if (dWL) LAUNCH("zero", launch_zero(dWL, sizeof(float) * (size_t)p.H * p.HL, st));
+    return RNNT_OK;
+  }
+  LAUNCH("zero", launch_zero(dA, sizeof(float) * (size_t)p.B * p.T * p.H, st));
+  LAUNCH("zero", launch_zero(dLr, sizeof(float) * (size_t)p.B * p.U1 * p.H, st));
+  LAUNCH("eff_lengths", launch_eff_lengths(shape_of(p), sv, T_len, U_len, Teff, Ueff, st));
+
+  rnnt_status s;
+  if (!untiled) {
+    s = projections(p, hA, hL, pr, pA, pL, st);
+    if (s != RNNT_OK) return s;
+  }
+  void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
+  void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
+
+  if (p.tc) {
+    s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
+                          dA, dLr, dWO, dbO, st);
+    if (s != RNNT_OK) return s;
+    s = tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ, st);
+    return s;
+  }
+
+  long long nch = 0;
+  s = chunk_count(p, sv, st, &nch);
+  if (s != RNNT_OK) return s;
+  float* dZ = (float*)(w + p.w_dz);
+  for (long long k = 0; k < nch; ++k) {
+    ChunkArgs c = chunk_args(p, sv, k, labels, T_len, U_len);
+    if (!untiled) {
+      LAUNCH("build_z", launch_build_z(c, pA, pL, Z, 0, st));
+      s = simt_scores(p, pr, (const float*)Z, (float*)Hs, p.chunk_rows, st);
+      if (s != RNNT_OK) return s;
+    }
+    LAUNCH("dh_rows", launch_dh_rows(c, (float*)Hs, grad_loss, st));
+    // dz = dh W^O
+    SimtGemm g{};
+    g.M = (int)p.chunk_rows; g.N = p.H; g.K = p.V;
+    g.A = Hs; g.sam = p.V; g.sak = 1;
+    g.Bm = pr->WO; g.sbk = p.H; g.sbn = 1; g.b_bf16 = bf;
+    g.C = dZ; g.ldc = p.H; g.alpha = 1.f;
+    LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+    LAUNCH("da_reduce", launch_da_reduce(c, dZ, Z, 0, dA, dLr, st));
+    if (dWO) {  // dW^O += dh^T z
+      SimtGemm q{};
+      q.M = p.V; q.N = p.H; q.K = (int)p.chunk_rows;
+      q.A = Hs; q.sam = 1; q.sak = p.V;
+      q.Bm = Z; q.sbk = p.H; q.sbn = 1;
+      q.C = dWO; q.ldc = p.H; q.alpha = 1.f; q.accumulate = 1;
+      LAUNCH("simt_gemm", launch_simt_gemm(q, st));
+    }
+    if (dbO) LAUNCH("colsum", launch_colsum((const float*)Hs, p.chunk_rows, p.V, p.V, dbO, st));
+  }
+
+  // Encoder-side gradients from the reduced pre-activation gradients.
+  SimtGemm g{};
+  if (dhA) {  // dh^A = dA W^A
+    g = SimtGemm{};
+    g.M = p.B * p.T; g.N = p.HA; g.K = p.H;
+    g.A = dA; g.sam = p.H; g.sak = 1;
+    g.Bm = pr->WA; g.sbk = p.HA; g.sbn = 1; g.b_bf16 = bf;
+    g.C = dhA; g.ldc = p.HA; g.alpha = 1.f;
+    LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  }
+  if (dWA) {  // dW^A = dA^T hA over the frames of accepted samples
+    g = SimtGemm{};
+    g.M = p.H; g.N = p.HA; g.K = p.B * p.T;
+    g.A = dA; g.sam = 1; g.sak = p.H;
+    g.Bm = hA; g.sbk = p.HA; g.sbn = 1; g.b_bf16 = bf;
+    g.C = dWA; g.ldc = p.HA; g.alpha = 1.f;
+    g.kmask_len = Teff; g.kperiod = p.T; g.kmask_off = 0;
+    LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  }
+  if (dhL) {
+    g = SimtGemm{};
+    g.M = p.B * p.U1; g.N = p.HL; g.K = p.H;
+    g.A = dLr; g.sam = p.H; g.sak = 1;
+    g.Bm = pr->WL; g.sbk = p.HL; g.sbn = 1; g.b_bf16 = bf;
+    g.C = dhL; g.ldc = p.HL; g.alpha = 1.f;
+    LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  }
+  if (dWL) {
+    g = SimtGemm{};
+    g.M = p.H; g.N = p.HL; g.K = p.B * p.U1;
+    g.A = dLr; g.sam = 1; g.sak = p.H;
+    g.Bm = hL; g.sbk = p.HL; g.sbn = 1; g.b_bf16 = bf;
+    g.C = dWL; g.ldc = p.HL; g.alpha = 1.f;
+    g.kmask_len = Ueff; g.kperiod = p.U1; g.kmask_off = 0;
+    LAUNCH("simt_gemm", launch_simt_gemm(g, st));
+  }
+  if (dbZ) LAUNCH("colsum", launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, st));
+  return RNNT_OK;
+}
+
+rnnt_status rnnt_device_status(const rnnt_dims* dims, const void* saved, rnnt_stream stream,
+                               int32_t* word) {
+  Plan p;
+  if (!make_plan(dims, &p) || !saved) return RNNT_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t w = 0;
+  RNNT_CHECK(cudaMemcpyAsync(&w, (const char*)saved + p.s_status, sizeof(int32_t),
+                             cudaMemcpyDeviceToHost, st));
+  RNNT_CHECK(cudaStreamSynchronize(st));
+  if (word) *word = w;
+  const rnnt_status order[] = {RNNT_ERR_LENGTH_RANGE, RNNT_ERR_LABEL_RANGE, RNNT_ERR_TIMEOUT};
+  for (rnnt_status c : order)
+    if (w & status_bit(c)) return c;
+  return RNNT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// tc.h -- bf16 tensor-core (tcgen05 / TMEM / TMA) path of librnnt_gb300 (internal).
+#pragma once
+#include "common.cuh"
+
+namespace rnnt {
+
+// True when this build runs RNNT_BF16 problems on the tensor-core kernels.
+bool tc_path_enabled();
+// RNNT_OK or RNNT_ERR_UNSUPPORTED_SHAPE for shapes the tensor-core kernels cannot take.
+rnnt_status tc_check_shape(const Plan& p);
+// out[M,H] = X[M,K] W[H,K]^T (+ bias[H]), bf16 operands, fp32 result.
+cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const void* bias, int M,
+                          int K, float* out, cudaStream_t s);
+// Forward over every tile: lnPD, lpb, lpl into saved (and, when Zkeep/Hkeep are
+// given, the untiled mode's kept z and scores).
+rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
+                             const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
+                             const float* pA, const float* pL, void* Zkeep, void* Hkeep,
+                             cudaStream_t s);
+// Backward over every tile: dA, dLr (accumulated), dW^O, db^O.
+rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
+                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
+                              const float* grad_loss, const float* pA, const float* pL, void* Z,
+                              void* Hs, bool untiled, float* dA, float* dLr, float* dWO,
+                              float* dbO, cudaStream_t s);
+// dh^A, dW^A, dh^L, dW^L, db^Z from dA and dLr.
+rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
+                             const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,
+                             float* dA, float* dLr, float* dhA, float* dhL, float* dWA,
+                             float* dWL, float* dbZ, cudaStream_t s);
+
+}  // namespace rnnt

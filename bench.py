@@ -1,0 +1,351 @@
+"""Benchmark: RNN-T joint + output layer + transducer loss, forward + backward.
+
+One step = rnnt_fwd + rnnt_bwd over one batch of the synthetic workload (every
+row of the hot path: validation, projections, the tiled joint/output/LSE
+forward, alpha/beta, the tiled recompute backward, the encoder gradients).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is lattice cells B*T*(U+1) per second
+over all ranks with inputs already in HBM; `e2e` is the same metric through
+the C ABI with host buffers (pinned H2D of the inputs, D2H of the loss and all
+gradients inside the timed region).  Each rank runs its own batch (weak
+scaling); there is no data-path collective.  L2 is flushed (256 MiB write)
+before every timed step, outside the step's events.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RNN-T fwd+bwd lattice cells/s (B*T*(U+1)); peak HBM GB; % bf16 tensor peak"
+UNIT = "cells/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# Algorithmic tensor work of each tensor-core kernel, per valid lattice
+# position, in units of H*V flops (the projections and encoder GEMMs are
+# accounted per encoder row instead).
+KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 2.0,
+                            "tc_bwd_dwo": 2.0}
+
+
+def run_gpu_bench(args):
+    import numpy as np
+    import torch
+
+    import asr_tiled_tanh_gb300 as rn
+    from asr_tiled_tanh_gb300 import synthetic
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rn.load(build_if_missing=True)
+
+    wl = synthetic.WORKLOADS[args.workload]
+    inp = synthetic.make(wl, seed=wl.seed + 1000 * rank)
+    valid = inp.valid_cells()
+    nominal = wl.nominal_cells
+    r = rn.Rnnt.for_inputs(inp, tile_cells=args.tile_cells, device=dev)
+    d = {k: getattr(inp, k).to(dev) for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO", "labels",
+                                               "T_len", "U_len")}
+    params = rn.make_params(d["WA"], d["WL"], d["bZ"], d["WO"], d["bO"])
+    grads = r.alloc_grads()
+    loss = torch.empty(wl.B, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
+              stream=stream)
+        r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads,
+              stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, word = r.status()
+    if code != 0:
+        raise SystemExit(f"device status {code} word {word}")
+
+    # --- timed region: device-resident inputs ---------------------------------
+    torch.cuda.reset_peak_memory_stats(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    rn.rnnt_profile_start(1 << 16)
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    prof = rn.rnnt_profile_stop()
+    if dist:
+        dist.barrier()
+    peak_bytes = torch.cuda.max_memory_allocated(dev)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = nominal * world / (ms_max / 1e3)
+
+    # --- e2e: host buffers through the C ABI ----------------------------------
+    host_in = {k: getattr(inp, k).pin_memory() for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO",
+                                                          "labels", "T_len", "U_len")}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in grads.items()}
+    host_loss = torch.empty(wl.B, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_loss.numel() * 4
+
+    def e2e_step():
+        for k, v in host_in.items():
+            d[k].copy_(v, non_blocking=True)
+        step()
+        host_loss.copy_(loss, non_blocking=True)
+        for k, v in grads.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize()
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        es[i].record(stream)
+        e2e_step()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert np.isfinite(host_loss.numpy()).all()
+
+    # --- roofline of the dominant kernel ----------------------------------------
+    hbm_peak, tf_burst, tf_sust, peak_src = _peaks()
+    launches = sum(c for _, c in prof.values())
+    top = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("none", (0.0, 1))
+    top_name, (top_ms, top_n) = top
+    H, V = wl.H, wl.V
+    roof = None
+    if top_name in KERNEL_FLOPS_PER_CELL_HV:
+        flops_per_launch = KERNEL_FLOPS_PER_CELL_HV[top_name] * H * V * valid \
+            / max(1, top_n // args.steps)
+        ach = flops_per_launch / (top_ms / top_n / 1e3) / 1e12
+        peak = tf_burst
+        roof = {"kernel": top_name, "bound": "tensor", "achieved": round(ach, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        roof = {"kernel": top_name, "bound": "alu", "achieved": None, "peak": None,
+                "unit": "TFLOP/s", "frac": None, "traffic": None,
+                "note": "fp32 FFMA kernels; no tensor-core phase"}
+    shares = {k: round(v[0] / sum(x[0] for x in prof.values()), 4) for k, v in
+              sorted(prof.items(), key=lambda kv: -kv[1][0])}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "
+                               f"V={wl.V} {wl.dtype}", "B": wl.B, "T": wl.T, "U": wl.U,
+                   "H": wl.H, "V": wl.V, "tile_cells": int(r.dims.tile_cells),
+                   "nominal_cells": nominal, "valid_cells": valid,
+                   "l2": "flushed (256 MiB write) before each timed step",
+                   "parallelism": f"replicas x{world}"},
+        "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
+        "peak_hbm_gb": round(peak_bytes / 1e9, 4),
+        "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / tf_burst, 4),
+        "e2e": {"value": round(nominal * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "kernel_shares": shares,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def _oracle_sample(inp, nsamp):
+    import oracle
+    sub = inp.subset(list(range(nsamp)))
+    f = lambda t: t.double().numpy()
+    t0 = time.perf_counter()
+    oracle.rnnt(f(sub.hA), f(sub.hL), f(sub.WA), f(sub.WL), f(sub.bZ), f(sub.WO), f(sub.bO),
+                sub.labels.numpy(), sub.T_len.numpy(), sub.U_len.numpy())
+    return time.perf_counter() - t0, sub
+
+
+def cpu_baseline(inp, budget_s):
+    """The oracle, as it stands, on a bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    n = 1
+    dt, sub = _oracle_sample(inp, n)
+    if dt < budget_s / 3 and inp.wl.B > 1:
+        n = max(1, min(inp.wl.B, int(budget_s / max(dt, 1e-3))))
+        dt, sub = _oracle_sample(inp, n)
+    cells = sub.wl.T * sub.wl.U1 * n
+    return {"value": round(cells / dt, 2), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"first {n} sample(s) of the workload, fwd+bwd, fp64 "
+                      f"({sub.valid_cells()} valid of {cells} nominal cells)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from asr_tiled_tanh_gb300 import synthetic
+    import oracle
+    oracle.build()
+    wl = synthetic.WORKLOADS[args.workload]
+    inp = synthetic.make(wl)
+    # one step = the oracle on a bounded sample (1 sample of the workload)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        _oracle_sample(inp, 1)
+    times = []
+    for _ in range(args.steps):
+        dt, sub = _oracle_sample(inp, 1)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    cells = wl.T * wl.U1
+    value = cells / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+           "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "
+                                  f"V={wl.V} {wl.dtype}", "B": wl.B, "T": wl.T, "U": wl.U,
+                      "H": wl.H, "V": wl.V},
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "kind": "oracle",
+                            "cores": oracle.num_threads(),
+                            "sample": "sample 0 of the workload (full T, U), fwd+bwd, fp64, "
+                                      "per step"},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="small")
+    ap.add_argument("--tile-cells", type=int, default=0)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu_bench(args)
+
+
+if __name__ == "__main__":
+    main()

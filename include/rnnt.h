@@ -1,0 +1,168 @@
+/*
+ * rnnt.h -- C ABI of the GB300 (sm_103a) RNN-T joint network + output layer +
+ * transducer loss library (librnnt_gb300.so).
+ *
+ * The operation is the one stated in "Neural transducer training: reduced
+ * memory consumption with sample-wise computation" (arXiv 2211.16270), §2:
+ *   joint network  (Eq. 3-4)  z[b,t,u] = tanh(W^A hA[b,t] + W^L hL[b,u] + b^Z)
+ *   output layer   (Eq. 5-6)  h[b,t,u] = W^O z[b,t,u] + b^O
+ *   loss f^W_1..4  (Eq. 7-10) softmax denominator P_D, forward/backward
+ *                             variables alpha/beta, L = -sum_b ln P(y_b|x_b),
+ *                             and dh = dL/dh,
+ * followed by the backward pass through the output layer and joint network
+ * (§4, Algorithm 1: dtheta^J, dtheta^O and the encodings' gradients).  The
+ * execution follows the tiled scheme of the Flash RNN-T blog ("Compute it, use
+ * it, make room"): the forward keeps only the blank and label log-probabilities
+ * of each lattice position, the backward recomputes each tile of positions and
+ * overwrites its scores with their gradients ("Making each operation more
+ * efficient").  RNNT_UNTILED keeps the joint intermediates instead.
+ *
+ * Conventions (all calls):
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, except
+ *    the rnnt_dims / rnnt_params structs themselves, which are host memory.
+ *  - labels[b,0] is the prepended blank (§2) and is never read; the move from
+ *    label position u to u+1 emits labels[b,u+1].  hL row u is the label
+ *    context after u labels.  Lattice of sample b: t < T_len[b],
+ *    u <= U_len[b].  Rows of hA/hL and labels beyond a sample's lengths are
+ *    never read (they may hold anything, NaN included).
+ *  - The caller owns every buffer.  The library never allocates device
+ *    memory; it uses the `saved` and `ws` buffers it is given.
+ *  - Every call is asynchronous on `stream`, except where noted.  Calls that
+ *    share a `ws` or `saved` buffer must not run concurrently.
+ *  - Host-checkable problems (NULL pointers, bad dims, unsupported shapes,
+ *    buffers too small) return an error before anything is launched.
+ *    Problems only the device can see (lengths out of range, labels out of
+ *    range) set bits in the device status word kept in `saved`; the affected
+ *    sample gets loss NaN and contributes nothing to any gradient.  Read the
+ *    word with rnnt_device_status.  No kernel traps or asserts.
+ */
+#ifndef RNNT_GB300_H
+#define RNNT_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stand-in for cudaStream_t (same representation: a pointer). */
+typedef void* rnnt_stream;
+
+typedef enum {
+  RNNT_OK = 0,
+  RNNT_ERR_INVALID_ARG = 1,        /* NULL pointer, negative or zero size, bad enum */
+  RNNT_ERR_UNSUPPORTED_SHAPE = 2,  /* shape this build's kernels do not handle */
+  RNNT_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes < rnnt_workspace_bytes(), or an
+                                      untiled lattice that cannot be addressed */
+  RNNT_ERR_LENGTH_RANGE = 4,       /* device: some T_len not in [1,T] or U_len not in [0,U1-1] */
+  RNNT_ERR_LABEL_RANGE = 5,        /* device: some labels[b,1..U_len[b]] not in [0,V) */
+  RNNT_ERR_TIMEOUT = 6,            /* device: a bounded wait inside a kernel gave up */
+  RNNT_ERR_CUDA = 7                /* a CUDA runtime call failed (launch, copy, ...) */
+} rnnt_status;
+
+typedef enum { RNNT_F32 = 0, RNNT_BF16 = 1 } rnnt_dtype;
+typedef enum { RNNT_TILED = 0, RNNT_UNTILED = 1 } rnnt_mode;
+
+/* Problem description (host struct).
+ *   B, T, U1 (= U+1, label positions including the prepended blank), HA, HL
+ *   (encoding sizes), H (joint size), V (vocabulary), blank (blank id in [0,V)).
+ *   dtype: element type of hA, hL and every parameter (RNNT_F32 or RNNT_BF16).
+ *     RNNT_F32 runs fp32 FFMA kernels end to end; RNNT_BF16 runs the bf16
+ *     tensor-core path (tcgen05, fp32 accumulation).
+ *   mode: RNNT_TILED (recompute per tile in the backward; workspace set by
+ *     tile_cells) or RNNT_UNTILED (z and the scores are kept in `saved` for
+ *     every lattice position; no recompute).
+ *   tile_cells: lattice positions whose intermediates the backward holds at
+ *     once in tiled mode (the Flash RNN-T "tile"); rounded up to a multiple of
+ *     128.  0 selects a default.  Ignored in untiled mode. */
+typedef struct {
+  int B, T, U1, HA, HL, H, V, blank;
+  int dtype;
+  int mode;
+  long long tile_cells;
+} rnnt_dims;
+
+/* Parameters theta^J = {W^A [H,HA], W^L [H,HL], b^Z [H]} (§2, joint network)
+ * and theta^O = {W^O [V,H], b^O [V]} (§2, output layer); device pointers of
+ * dims.dtype.  bZ and bO may be NULL (zero bias). */
+typedef struct {
+  const void* WA;
+  const void* WL;
+  const void* bZ;
+  const void* WO;
+  const void* bO;
+} rnnt_params;
+
+/* Byte offsets of the arrays inside `saved` (see rnnt_saved_layout).
+ * lpb, lpl, lnPD, alpha, beta: fp32 [B,T,U1], natural-log values:
+ *   lnPD = ln sum_v exp h_v (the softmax denominator of Eq. 7), lpb =
+ *   h_blank - lnPD, lpl = h_{labels[b,u+1]} - lnPD (-inf on row u = U_len[b]),
+ *   alpha/beta the forward/backward variables of Eq. 8.  Every position
+ *   outside a sample's lattice holds -inf.
+ * lnP: fp32 [B], ln P(y_b|x_b) (NaN for a rejected sample).
+ * status: one int32, the device status word (bit k set = rnnt_status k+... see
+ *   rnnt_device_status).
+ * z, h: untiled mode only (otherwise 0): z [cells,H] and the scores / their
+ *   gradients [cells,V], element type = dims.dtype, rows in the library's
+ *   tile order (not [B,T,U1]). */
+typedef struct {
+  size_t status, lnP, lpb, lpl, lnPD, alpha, beta, z, h, total;
+} rnnt_saved_offsets;
+
+/* Bytes of the `saved` buffer that rnnt_fwd fills and rnnt_bwd reads:
+ * 20 B per lattice position [B,T,U1] plus small headers, and in untiled mode
+ * the kept z and scores.  Returns 0 if dims are invalid. */
+size_t rnnt_saved_bytes(const rnnt_dims* dims);
+
+/* Fill *out with the layout of `saved` for dims.  Returns RNNT_OK or
+ * RNNT_ERR_INVALID_ARG. */
+rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out);
+
+/* Bytes of the scratch buffer `ws` that rnnt_fwd and rnnt_bwd need: the joint
+ * projections W^A hA + b^Z [B,T,H] and W^L hL [B,U1,H] (fp32), the tile
+ * buffers (tile_cells x (H + V) elements in tiled mode), and the fp32
+ * gradient accumulators of the joint pre-activations.  Returns 0 if dims are
+ * invalid.  The buffer needs no initialisation and 256-byte alignment. */
+size_t rnnt_workspace_bytes(const rnnt_dims* dims);
+
+/* Forward pass.  Inputs: hA [B,T,HA], hL [B,U1,HL], params, labels [B,U1]
+ * int32, T_len [B], U_len [B] int32.  Outputs: loss [B] fp32 = -ln P(y_b|x_b)
+ * (the batch loss of Eq. 9 is their sum), and `saved` (rnnt_saved_bytes,
+ * 256-byte aligned) for rnnt_bwd.  ws: rnnt_workspace_bytes bytes.
+ * stream: a cudaStream_t (NULL = legacy default stream). */
+rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
+                     rnnt_stream stream);
+
+/* Backward pass for sum_b grad_loss[b] * loss[b] (grad_loss NULL = all ones).
+ * Takes the same inputs as the matching rnnt_fwd and the `saved` buffer it
+ * filled (untiled mode: the kept scores in `saved` are overwritten with their
+ * gradients, so a second rnnt_bwd on the same `saved` is not allowed).
+ * Outputs, all fp32 and OVERWRITTEN (not accumulated): dhA [B,T,HA],
+ * dhL [B,U1,HL], dWA [H,HA], dWL [H,HL], dbZ [H], dWO [V,H], dbO [V].  Rows
+ * beyond a sample's lengths are written as 0.  Any output pointer may be NULL
+ * to skip writing it (the work that feeds other outputs still runs).
+ * When the largest lattice the dims allow does not fit in one tile buffer,
+ * this call synchronizes `stream` once to read the number of tiles. */
+rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
+                     float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
+                     void* ws, size_t ws_bytes, rnnt_stream stream);
+
+/* Synchronize `stream` and read the device status word in `saved`.  Returns
+ * RNNT_OK if no device-side problem was recorded, else the first recorded
+ * code among RNNT_ERR_LENGTH_RANGE, RNNT_ERR_LABEL_RANGE, RNNT_ERR_TIMEOUT.
+ * If `word` is not NULL it receives the raw bitmask (bit k <=> status code k). */
+rnnt_status rnnt_device_status(const rnnt_dims* dims, const void* saved, rnnt_stream stream,
+                               int32_t* word);
+
+/* Static, human-readable name of a status code. */
+const char* rnnt_status_string(rnnt_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RNNT_GB300_H */

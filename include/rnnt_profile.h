@@ -1,0 +1,40 @@
+/*
+ * rnnt_profile.h -- per-kernel timing of librnnt_gb300, for measurement tools.
+ *
+ * Not part of the method (the pages define no instrumentation): while a
+ * profiling session is open, every kernel launch the library makes through
+ * rnnt_fwd / rnnt_bwd is bracketed by a pair of CUDA events recorded on the
+ * launch's own stream, so the device time of each kernel can be summed by
+ * name after the fact.  Recording an event is asynchronous; nothing is
+ * synchronized until rnnt_profile_stop.  Sessions are process-wide and not
+ * thread-safe.  Events are created by rnnt_profile_start (no device memory
+ * is allocated for them) and destroyed by rnnt_profile_stop.
+ */
+#ifndef RNNT_GB300_PROFILE_H
+#define RNNT_GB300_PROFILE_H
+
+#include "rnnt.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Open a session able to record `capacity` launches (further launches are
+ * counted but not timed).  RNNT_ERR_INVALID_ARG if capacity < 1 or a session
+ * is already open; RNNT_ERR_CUDA if the events cannot be created. */
+rnnt_status rnnt_profile_start(int capacity);
+
+/* Close the session: synchronize on the recorded events, sum the elapsed
+ * times per kernel name.  Returns the number of distinct kernel names (>= 0),
+ * or -1 if no session was open or the events could not be read. */
+int rnnt_profile_stop(void);
+
+/* Entry i (0 <= i < the count rnnt_profile_stop returned) of the last
+ * closed session: kernel name (static string), total milliseconds and the
+ * number of timed launches.  RNNT_ERR_INVALID_ARG if i is out of range. */
+rnnt_status rnnt_profile_entry(int i, const char** name, double* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RNNT_GB300_PROFILE_H */

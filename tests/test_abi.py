@@ -1,0 +1,93 @@
+"""The C-ABI library loads and exports what include/*.h declares (CPU only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import asr_tiled_tanh_gb300 as rn
+from asr_tiled_tanh_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return rn.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b(rnnt_[a-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert set(rn.EXPORTS) <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert rn.rnnt_status_string(code)
+    assert rn.rnnt_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("bad", [dict(B=-1), dict(T=0), dict(U1=0), dict(H=0), dict(V=0),
+                                 dict(blank=32), dict(blank=-1), dict(dtype=7), dict(mode=3),
+                                 dict(tile_cells=-5)])
+def test_invalid_dims_give_zero_sizes(lib, bad):
+    kw = dict(B=2, T=32, U1=9, HA=64, HL=64, H=64, V=32, blank=0, dtype=rn.RNNT_F32,
+              mode=rn.RNNT_TILED, tile_cells=0)
+    kw.update(bad)
+    d = rn.make_dims(**kw)
+    assert rn.rnnt_saved_bytes(d) == 0
+    assert rn.rnnt_workspace_bytes(d) == 0
+    with pytest.raises(rn.RnntError):
+        rn.rnnt_saved_layout(d)
+
+
+def test_saved_layout_is_aligned_and_sized(lib):
+    for mode in (rn.RNNT_TILED, rn.RNNT_UNTILED):
+        d = rn.make_dims(3, 37, 12, 24, 40, 48, 37, 0, rn.RNNT_F32, mode)
+        L = rn.rnnt_saved_layout(d)
+        n = 3 * 37 * 12
+        offs = [L.status, L.lnP, L.lpb, L.lpl, L.lnPD, L.alpha, L.beta]
+        assert all(o % 256 == 0 for o in offs)
+        assert sorted(offs) == offs
+        assert L.beta + 4 * n <= L.total == rn.rnnt_saved_bytes(d)
+        if mode == rn.RNNT_UNTILED:
+            assert L.z > L.beta and L.h > L.z
+        else:
+            assert L.z == 0 and L.h == 0
+
+
+def test_tile_buffer_tracks_tile_cells(lib):
+    # the tile workspace grows with tile_cells and not with the lattice size
+    big = dict(B=1024, T=1000, U1=101, HA=512, HL=512, H=512, V=4096, blank=0,
+               dtype=rn.RNNT_BF16, mode=rn.RNNT_TILED)
+    w1 = rn.rnnt_workspace_bytes(rn.make_dims(**big, tile_cells=128 * 152))
+    w2 = rn.rnnt_workspace_bytes(rn.make_dims(**big, tile_cells=128 * 304))
+    assert w2 > w1
+    per_cell_elems = 512 + 4096
+    assert w2 - w1 <= 128 * 152 * per_cell_elems * 8 + 4096
+    nominal_scores = 1024 * 1000 * 101 * 4096 * 2
+    assert w2 < nominal_scores / 50
+
+
+def test_untiled_saved_grows_with_lattice(lib):
+    small = rn.make_dims(8, 200, 51, 512, 512, 512, 1024, 0, rn.RNNT_BF16, rn.RNNT_UNTILED)
+    tiled = rn.make_dims(8, 200, 51, 512, 512, 512, 1024, 0, rn.RNNT_BF16, rn.RNNT_TILED)
+    assert rn.rnnt_saved_bytes(small) > 8 * 200 * 51 * 1024 * 2
+    assert rn.rnnt_saved_bytes(tiled) < 8 * 200 * 51 * 24 + 65536

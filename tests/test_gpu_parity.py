@@ -1,0 +1,188 @@
+"""GPU parity: the C-ABI library against the fp64 oracle on seeded inputs.
+
+Tolerances: fp32 inputs, loss relative error <= 1e-5 and gradient relative L2
+error <= 1e-4; bf16 inputs (the oracle gets the same bf16-rounded values),
+2e-3 and 1e-2.  The -inf pattern of every saved array (which positions are
+outside a lattice, which have no label transition) must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import asr_tiled_tanh_gb300 as rn
+from asr_tiled_tanh_gb300 import synthetic
+from tests.helpers import (GRAD_KEYS, assert_parity, rel_l2, run_gpu, run_oracle, to_device,
+                           valid_mask)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rn.load(build_if_missing=True)
+
+
+def test_tiny_fp32_workload():
+    inp = synthetic.make("tiny")
+    gpu = run_gpu(inp)
+    orc = run_oracle(inp)
+    assert gpu["status"] == (0, 0)
+    assert_parity(gpu, orc, inp)
+    m = valid_mask(inp)
+    for k in ("lpb", "lnPD", "alpha", "beta"):
+        np.testing.assert_allclose(gpu[k][m], getattr(orc, k)[m], rtol=2e-5, atol=2e-5)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_fp32_ragged_shapes_with_biases(seed):
+    # T, U+1, H, V not multiples of any tile size; HA != HL != H
+    inp = synthetic.custom(B=5, T=37, U=11, HA=24, HL=40, H=48, V=37, dtype="f32", seed=seed,
+                           t_frac=0.1, u_frac=0.0, bias_std=0.3)
+    g = np.random.default_rng(seed).uniform(0.5, 1.5, 5)
+    gpu = run_gpu(inp, grad_loss=g)
+    orc = run_oracle(inp, grad_loss=g)
+    assert_parity(gpu, orc, inp)
+
+
+def test_fp32_many_chunks_and_untiled_agree():
+    inp = synthetic.custom(B=3, T=40, U=9, HA=32, HL=32, H=32, V=40, dtype="f32", seed=3,
+                           bias_std=0.2)
+    orc = run_oracle(inp)
+    one_tile = run_gpu(inp, tile_cells=128)       # one tile per chunk: many chunks
+    untiled = run_gpu(inp, mode="untiled")
+    for r in (one_tile, untiled):
+        assert_parity(r, orc, inp)
+    np.testing.assert_array_equal(one_tile["loss"], untiled["loss"])
+
+
+def test_small_bf16_workload():
+    inp = synthetic.make("small")
+    gpu = run_gpu(inp)
+    orc = run_oracle(inp)
+    assert gpu["status"] == (0, 0)
+    errs = assert_parity(gpu, orc, inp)
+    print("small bf16 gradient rel L2:", errs)
+
+
+def test_bf16_ragged_shapes_with_biases():
+    inp = synthetic.custom(B=6, T=45, U=13, HA=64, HL=192, H=128, V=320, dtype="bf16", seed=5,
+                           t_frac=0.1, u_frac=0.0, bias_std=0.3)
+    g = np.linspace(0.5, 2.0, 6)
+    gpu = run_gpu(inp, grad_loss=g)
+    orc = run_oracle(inp, grad_loss=g)
+    assert_parity(gpu, orc, inp)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
+    H, V = (64, 64) if dtype == "f32" else (128, 256)
+    inp = synthetic.custom(B=4, T=50, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=7,
+                           bias_std=0.1)
+    runs = [run_gpu(inp, tile_cells=tc) for tc in (128, 128 * 3, 128 * 7, 0)]
+    runs.append(run_gpu(inp, mode="untiled"))
+    for r in runs[1:]:
+        np.testing.assert_array_equal(r["loss"], runs[0]["loss"])
+        for k in GRAD_KEYS:
+            assert rel_l2(r[k], runs[0][k]) < 1e-5, k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_padding_is_never_read(dtype):
+    H, V = (32, 48) if dtype == "f32" else (128, 128)
+    inp = synthetic.custom(B=4, T=33, U=10, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=11)
+    clean = run_gpu(inp)
+    dirty = synthetic.Inputs(inp.wl, inp.hA.clone(), inp.hL.clone(), inp.WA, inp.WL, inp.bZ,
+                             inp.WO, inp.bO, inp.labels.clone(), inp.T_len, inp.U_len)
+    for b in range(4):
+        Tb, Ub = int(inp.T_len[b]), int(inp.U_len[b])
+        dirty.hA[b, Tb:] = float("nan")
+        dirty.hL[b, Ub + 1:] = float("nan")
+        dirty.labels[b, Ub + 1:] = -3
+        dirty.labels[b, 0] = 10 ** 6
+    d = run_gpu(dirty)
+    assert d["status"] == (0, 0)
+    np.testing.assert_array_equal(clean["loss"], d["loss"])
+    for k in GRAD_KEYS:
+        assert np.all(np.isfinite(d[k])), k
+        assert rel_l2(d[k], clean[k]) < 1e-5, k
+    for b in range(4):
+        assert np.all(d["dhA"][b, int(inp.T_len[b]):] == 0)
+        assert np.all(d["dhL"][b, int(inp.U_len[b]) + 1:] == 0)
+
+
+def test_rejected_samples_are_flagged_and_isolated():
+    inp = synthetic.custom(B=5, T=20, U=6, HA=32, HL=32, H=32, V=24, dtype="f32", seed=13)
+    bad = synthetic.Inputs(inp.wl, inp.hA, inp.hL, inp.WA, inp.WL, inp.bZ, inp.WO, inp.bO,
+                           inp.labels.clone(), inp.T_len.clone(), inp.U_len.clone())
+    bad.T_len[1] = 21          # longer than T
+    bad.U_len[3] = 6
+    bad.labels[3, 2] = 24      # == V
+    gpu = run_gpu(bad)
+    code, word = gpu["status"]
+    assert code == 4  # the length error is reported first
+    assert word == (1 << 4) | (1 << 5)
+    assert np.isnan(gpu["loss"][1]) and np.isnan(gpu["loss"][3])
+    keep = [0, 2, 4]
+    sub = inp.subset(keep)
+    orc = run_oracle(sub)
+    np.testing.assert_allclose(gpu["loss"][keep], orc.loss, rtol=1e-5)
+    # the rejected samples contribute nothing: gradients equal the sub-batch's
+    for k in ("dWA", "dWL", "dbZ", "dWO", "dbO"):
+        assert rel_l2(gpu[k], orc.grads[k]) < 1e-4, k
+    assert np.all(gpu["dhA"][[1, 3]] == 0) and np.all(gpu["dhL"][[1, 3]] == 0)
+
+
+def test_batched_equals_sum_of_single_samples():
+    inp = synthetic.custom(B=4, T=30, U=7, HA=32, HL=32, H=32, V=40, dtype="f32", seed=17,
+                           bias_std=0.2)
+    full = run_gpu(inp)
+    acc = {k: 0.0 for k in ("dWA", "dWL", "dbZ", "dWO", "dbO")}
+    for b in range(4):
+        one = run_gpu(inp.subset([b]))
+        assert one["loss"][0] == full["loss"][b]
+        np.testing.assert_allclose(one["dhA"][0], full["dhA"][b], rtol=1e-5, atol=1e-7)
+        for k in acc:
+            acc[k] = acc[k] + one[k]
+    for k in acc:
+        assert rel_l2(acc[k], full[k]) < 1e-5, k
+
+
+def test_lattice_edges_single_frame_and_no_labels():
+    inp = synthetic.custom(B=4, T=17, U=9, HA=32, HL=32, H=32, V=24, dtype="f32", seed=19)
+    inp.T_len[:] = torch.tensor([1, 17, 1, 16], dtype=torch.int32)
+    inp.U_len[:] = torch.tensor([9, 0, 0, 8], dtype=torch.int32)
+    gpu = run_gpu(inp)
+    orc = run_oracle(inp)
+    assert_parity(gpu, orc, inp)
+
+
+def test_empty_batch():
+    inp = synthetic.custom(B=0, T=10, U=3, HA=16, HL=16, H=16, V=8, dtype="f32", seed=0)
+    r = rn.Rnnt.for_inputs(inp)
+    dev = to_device(inp)
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    loss = r.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    g = r.bwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    torch.cuda.synchronize()
+    assert loss.numel() == 0
+    for k in ("dWA", "dWL", "dbZ", "dWO", "dbO"):
+        assert torch.all(g[k] == 0), k
+
+
+def test_host_checked_errors():
+    inp = synthetic.custom(B=2, T=10, U=3, HA=16, HL=16, H=16, V=8, dtype="f32", seed=0)
+    dev = to_device(inp)
+    r = rn.Rnnt.for_inputs(inp)
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    loss = torch.empty(2, device="cuda")
+    small_ws = r.ws[: r.ws.numel() // 2]
+    code = rn.rnnt_fwd(r.dims, dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"],
+                       dev["U_len"], loss, r.saved, small_ws, check=False)
+    assert code == 3
+    code = rn.rnnt_fwd(r.dims, None, dev["hL"], params, dev["labels"], dev["T_len"],
+                       dev["U_len"], loss, r.saved, r.ws, check=False)
+    assert code == 1
+    bad_params = rn.make_params(None, dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    code = rn.rnnt_fwd(r.dims, dev["hA"], dev["hL"], bad_params, dev["labels"], dev["T_len"],
+                       dev["U_len"], loss, r.saved, r.ws, check=False)
+    assert code == 1

@@ -1,29 +1,959 @@
-// k_tc.cu -- bf16 tensor-core path (placeholder until the tcgen05 kernels land).
+// k_tc.cu -- bf16 tensor-core path of the RNN-T joint/output/loss library.
+//
+// One warp-specialized, persistent tcgen05 GEMM kernel serves every dense
+// contraction of the path; what differs is the epilogue that consumes each
+// 128 x BN fp32 accumulator tile from TMEM:
+//   EPI_STORE  C = A B^T (+ bias)           joint projections, dh^A, dh^L
+//   EPI_ATOMIC C += A B (split-K, fp32 red)  dW^O, dW^A, dW^L
+//   EPI_LSE    scores -> online log-sum-exp over V, blank/label log-probs
+//              (f^W_1 of Eq. 7 plus the gather of the two probabilities the
+//              Flash RNN-T kernel emits instead of a softmax)
+//   EPI_DH     scores -> dh = dL/dh (Eq. 10), written over the tile's score
+//              buffer ("it also overwrites the scores with their gradients")
+//   EPI_DA     dz -> da = dz (1 - z^2), reduced over u into dA[b,t] and over
+//              t into dLr[b,u] (joint-network backward, sample-wise paper §4)
+// Rows of the lattice GEMMs are lattice positions: M tile m of a chunk is the
+// 16 x 8 lattice tile (chunk's first tile + m), one position per TMEM lane.
+//
+// Roles (192 threads): warp 0 issues TMA loads into a ring of shared-memory
+// stages, warp 1 allocates TMEM and one thread issues tcgen05.mma into one of
+// two TMEM accumulators, warps 2-5 drain the other accumulator (tcgen05.ld)
+// through the epilogue.  mbarriers link the roles; every wait is bounded and a
+// timeout sets RNNT_ERR_TIMEOUT in the status word and winds the CTA down.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.h"
+#include "profile.h"
+#include "ptx.cuh"
 #include "tc.h"
+#include "../../include/rnnt_testing.h"
 
 namespace rnnt {
 
+namespace {
+
+constexpr int BM = 128;              // rows per tile (TMEM lanes)
+constexpr int BK = 64;               // K per stage: one 128-byte swizzle atom of bf16
+constexpr int NTHREADS = 192;
+constexpr int EPI_WARP0 = 2;         // first epilogue warp
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait, then give up
+constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
+
+enum { EPI_STORE = 0, EPI_ATOMIC = 1, EPI_LSE = 2, EPI_DH = 3, EPI_DA = 4 };
+
+struct TcParams {
+  int M, N, K;
+  int m_tiles, n_tiles, k_splits, kb_total, kb_per_split;
+  int units;
+  int row_complete;      // a unit is one M tile with all of its N tiles, in order
+  float* C;              // STORE / ATOMIC output, row-major with ldc
+  long long ldc;
+  const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
+  ChunkArgs ch;          // lattice epilogues: chunk, lengths, labels, saved arrays
+  const float* grad_loss;
+  __nv_bfloat16* Hout;   // LSE: kept scores (untiled) [rows][N]; DH: dh [rows][N]
+  const __nv_bfloat16* Zin;  // DA: z [rows][N]
+  float* dA;
+  float* dLr;
+  int32_t* status;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int EPI_SCRATCH = 4 * 32 * 33 * 4;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int STAGES_RAW = (SMEM_LIMIT - 1024 - EPI_SCRATCH - BAR_BYTES) / STAGE;
+  static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_SCRATCH + BAR_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+};
+
+struct Unit {
+  int m, n0, n1, kb0, kb1;  // M tile, N tiles [n0,n1), K blocks [kb0,kb1)
+};
+
+__device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
+  Unit w;
+  if (p.row_complete) {
+    w.m = u; w.n0 = 0; w.n1 = p.n_tiles; w.kb0 = 0; w.kb1 = p.kb_total;
+  } else {
+    const int ks = u % p.k_splits;
+    const int rest = u / p.k_splits;
+    const int n = rest % p.n_tiles;
+    w.m = rest / p.n_tiles;
+    w.n0 = n; w.n1 = n + 1;
+    w.kb0 = ks * p.kb_per_split;
+    w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
+  }
+  return w;
+}
+
+__device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (p.status) atomicOr(p.status, status_bit(RNNT_ERR_TIMEOUT));
+}
+
+// Lattice coordinates of M tile m of a chunk, and of one of its rows (TMEM lane).
+struct TileRef {
+  bool exists;  // the tile is one of the actual tiles of the batch
+  int b, t0, u0, Tb, Ub;
+};
+
+__device__ __forceinline__ TileRef tile_ref(const ChunkArgs& c, int m) {
+  TileRef r{};
+  const long long g = c.first_tile + m;
+  if (m >= c.ntiles || g >= *c.sv.total_tiles) return r;
+  TileCoord tc = decode_tile(c.sv.prefix, c.T_len, c.U_len, c.sh.B, g);
+  r.exists = true;
+  r.b = tc.b; r.t0 = tc.t0; r.u0 = tc.u0; r.Tb = tc.Tb; r.Ub = tc.Ub;
+  return r;
+}
+
+struct RowCell {
+  bool valid;   // inside its sample's lattice
+  int b, t, u, Tb, Ub;
+};
+
+__device__ __forceinline__ RowCell row_of(const TileRef& tr, int row) {
+  RowCell r{};
+  r.b = tr.b; r.Tb = tr.Tb; r.Ub = tr.Ub;
+  r.t = tr.t0 + row / TU;
+  r.u = tr.u0 + row % TU;
+  r.valid = tr.exists && r.t < tr.Tb && r.u <= tr.Ub;
+  return r;
+}
+
+__device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) {
+  return __bfloat162float(p[i]);
+}
+
+// Select v[j] for a runtime j in [0,32) without local memory.
+__device__ __forceinline__ float pick32(const float* v, int j) {
+  float r = 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) r = (k == j) ? v[k] : r;
+  return r;
+}
+
+template <int BN, int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(NTHREADS, 1)
+k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+          const TcParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + STAGES * C::A_BYTES;
+  float* scratch = (float*)(smem + STAGES * C::STAGE);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * C::STAGE + C::EPI_SCRATCH);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_holder = (uint32_t*)(done_bar + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+
+  const int warp = ptx::warp_id(), lane = ptx::lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&acc_full[a], 1);
+      ptx::mbar_init(&acc_empty[a], 128);
+    }
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (ptx::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
+      for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        if (w.kb1 <= w.kb0) continue;
+        for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!ptx::mbar_wait(&empty[stage], phase ^ 1, WAIT_NS)) {
+              report_timeout(p, abort_flag);
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE);
+            unsigned char* a = sA + stage * C::A_BYTES;
+            unsigned char* b = sB + stage * C::B_BYTES;
+            if (!A_MN) {
+              ptx::tma_load_2d(a, &tmA, &full[stage], kb * BK, w.m * BM);
+            } else {
+              ptx::tma_load_2d(a, &tmA, &full[stage], w.m * BM, kb * BK);
+              ptx::tma_load_2d(a + 64 * 128, &tmA, &full[stage], w.m * BM + 64, kb * BK);
+            }
+            if (!B_MN) {
+              ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                ptx::tma_load_2d(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j, kb * BK);
+            }
+            issued[stage] = (int)phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+      // Wind-down: every fill this thread issued must have landed before the
+      // CTA may exit (normally all of them were consumed already).
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s] >= 0 && !ptx::mbar_wait(&full[s], (uint32_t)issued[s], WAIT_NS))
+          report_timeout(p, abort_flag);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (ptx::elect_one()) {
+      constexpr uint32_t IDESC = ptx::idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        if (w.kb1 <= w.kb0) continue;
+        for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
+          if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, WAIT_NS)) {
+            report_timeout(p, abort_flag);
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          bool ok = true;
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!ptx::mbar_wait(&full[stage], phase, WAIT_NS)) {
+              report_timeout(p, abort_flag);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a0 = ptx::smem_u32(sA + stage * C::A_BYTES);
+            const uint32_t b0 = ptx::smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: 16 elements = 32 bytes along the swizzled row.
+              // MN-major: 16 K rows = two 8-row groups of 1024 bytes.
+              const uint64_t ad = A_MN ? ptx::sdesc_sw128(a0 + k * 2048, 64 * 128, 1024)
+                                       : ptx::sdesc_sw128(a0 + k * 32, 16, 1024);
+              const uint64_t bd = B_MN ? ptx::sdesc_sw128(b0 + k * 2048, 64 * 128, 1024)
+                                       : ptx::sdesc_sw128(b0 + k * 32, 16, 1024);
+              ptx::mma_bf16(d_tmem, ad, bd, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          ptx::mma_commit(&acc_full[acc]);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+      }
+      // all issued MMAs complete before TMEM is released
+      ptx::mma_commit(done_bar);
+      if (!ptx::mbar_wait(done_bar, 0, WAIT_NS)) report_timeout(p, abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int sub = warp & 3;          // TMEM lane quarter of this warp
+    const int row = sub * 32 + lane;   // accumulator row owned by this thread
+    float* wscr = scratch + (warp - EPI_WARP0) * 32 * 33;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+      const Unit w = unit_of(p, u);
+      if (w.kb1 <= w.kb0) continue;
+      // per-unit state of the lattice epilogues
+      TileRef tr{};
+      RowCell rc{};
+      float run_max = -INFINITY, run_sum = 0.f, h_blank = 0.f, h_lab = 0.f;
+      int lab = -1;
+      float pb = 0.f, pl = 0.f, gam = 0.f, lnPD = 0.f, g = 1.f;
+      if (EPI == EPI_LSE || EPI == EPI_DH || EPI == EPI_DA) {
+        tr = tile_ref(p.ch, w.m);
+        rc = row_of(tr, row);
+      }
+      if ((EPI == EPI_LSE || EPI == EPI_DH) && rc.valid && rc.u < rc.Ub)
+        lab = p.ch.labels[(size_t)rc.b * p.ch.sh.U1 + rc.u + 1];
+      if (EPI == EPI_DH && rc.valid) {
+        const SavedView& sv = p.ch.sv;
+        const int U1 = p.ch.sh.U1;
+        const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * U1 + rc.u;
+        const float lnP = sv.lnP[rc.b];
+        const float a = sv.alpha[cell];
+        float bn;
+        if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
+        else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
+        pb = __expf(a + sv.lpb[cell] + bn - lnP);
+        pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
+        gam = pb + pl;
+        lnPD = sv.lnPD[cell];
+        g = p.grad_loss ? p.grad_loss[rc.b] : 1.f;
+      }
+      for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
+        if (!ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
+          report_timeout(p, abort_flag);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(sub * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          ptx::tmem_ld32(tbase + c * 32, v);
+          ptx::tmem_ld_wait();
+          const int col0 = n * BN + c * 32;
+          if (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
+            const long long grow = (long long)w.m * BM + row;
+            if (grow < p.M && col0 < p.N) {
+              float* dst = p.C + grow * p.ldc + col0;
+              if (EPI == EPI_STORE) {
+                if (p.bias) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] += (col0 + j < p.N) ? bf(p.bias, col0 + j) : 0.f;
+                }
+                if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
+#pragma unroll
+                  for (int j = 0; j < 32; j += 4)
+                    *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                } else {
+                  for (int j = 0; j < 32 && col0 + j < p.N; ++j) dst[j] = v[j];
+                }
+              } else {
+                for (int j = 0; j < 32 && col0 + j < p.N; ++j) ptx::red_add_f32(dst + j, v[j]);
+              }
+            }
+          } else if (EPI == EPI_LSE) {
+            if (rc.valid) {
+              const int nv = min(32, p.N - col0);
+              float cm = -INFINITY;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (p.bias) v[j] += (j < nv) ? bf(p.bias, col0 + j) : 0.f;
+                cm = (j < nv) ? fmaxf(cm, v[j]) : cm;
+              }
+              const float nm = fmaxf(run_max, cm);
+              const float L2E = 1.4426950408889634f;
+              float s = run_sum * ptx::ex2((run_max - nm) * L2E);
+              const float nmL = nm * L2E;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) s += (j < nv) ? ptx::ex2(fmaf(v[j], L2E, -nmL)) : 0.f;
+              run_sum = s;
+              run_max = nm;
+              const int jb = p.ch.sh.blank - col0;
+              if (jb >= 0 && jb < 32) h_blank = pick32(v, jb);
+              const int jl = lab - col0;
+              if (jl >= 0 && jl < 32) h_lab = pick32(v, jl);
+              if (p.Hout) {  // untiled mode keeps the scores
+                __nv_bfloat16* dst = p.Hout + ((long long)w.m * BM + row) * p.N + col0;
+                for (int j = 0; j < nv; j += 2) {
+                  if (j + 1 < nv) *(__nv_bfloat162*)(dst + j) = __floats2bfloat162_rn(v[j], v[j + 1]);
+                  else dst[j] = __float2bfloat16_rn(v[j]);
+                }
+              }
+            }
+          } else if (EPI == EPI_DH) {
+            const int nv = min(32, p.N - col0);
+            __nv_bfloat16* dst = p.Hout + ((long long)w.m * BM + row) * p.N + col0;
+            float d[32];
+            if (rc.valid) {
+              const float L2E = 1.4426950408889634f;
+              const float nl = lnPD * L2E;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float h = v[j] + ((p.bias && j < nv) ? bf(p.bias, col0 + j) : 0.f);
+                float x = gam * ptx::ex2(fmaf(h, L2E, -nl));
+                if (col0 + j == p.ch.sh.blank) x -= pb;
+                if (col0 + j == lab) x -= pl;
+                d[j] = g * x;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) d[j] = 0.f;
+            }
+            if (w.m < p.ch.ntiles) {
+              if (nv == 32 && (p.N & 7) == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                  __nv_bfloat162 q0 = __floats2bfloat162_rn(d[j], d[j + 1]);
+                  __nv_bfloat162 q1 = __floats2bfloat162_rn(d[j + 2], d[j + 3]);
+                  __nv_bfloat162 q2 = __floats2bfloat162_rn(d[j + 4], d[j + 5]);
+                  __nv_bfloat162 q3 = __floats2bfloat162_rn(d[j + 6], d[j + 7]);
+                  uint4 pk;
+                  pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
+                  pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
+                  *(uint4*)(dst + j) = pk;
+                }
+              } else {
+                for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
+              }
+            }
+          } else if (EPI == EPI_DA) {
+            // Transpose the warp's 32 rows x 32 columns through shared memory:
+            // lane = column, then sum over the tile's u (dA) and t (dLr).
+#pragma unroll
+            for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = v[j];
+            __syncwarp();
+            const int col = col0 + lane;
+            if (col < p.N) {
+              // this warp's rows are tile positions sub*32 .. sub*32+31:
+              // t = t0 + sub*4 + r/8, u = u0 + r%8
+              float sum_u[TU];
+#pragma unroll
+              for (int k = 0; k < TU; ++k) sum_u[k] = 0.f;
+              const long long rbase = (long long)w.m * BM + sub * 32;
+              const int tw = tr.t0 + sub * 4;
+#pragma unroll
+              for (int tq = 0; tq < 4; ++tq) {
+                const int t = tw + tq;
+                float st = 0.f;
+#pragma unroll
+                for (int k = 0; k < TU; ++k) {
+                  const int r = tq * TU + k;
+                  const int uu = tr.u0 + k;
+                  float da = 0.f;
+                  if (tr.exists && t < tr.Tb && uu <= tr.Ub) {
+                    const float z = bf(p.Zin, (rbase + r) * p.N + col);
+                    da = wscr[r * 33 + lane] * (1.f - z * z);
+                  }
+                  st += da;
+                  sum_u[k] += da;
+                }
+                if (tr.exists && t < tr.Tb)
+                  ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + t) * p.N + col, st);
+              }
+              if (tr.exists && tw < tr.Tb) {
+#pragma unroll
+                for (int k = 0; k < TU; ++k) {
+                  const int uu = tr.u0 + k;
+                  if (uu <= tr.Ub)
+                    ptx::red_add_f32(p.dLr + ((size_t)tr.b * p.ch.sh.U1 + uu) * p.N + col,
+                                     sum_u[k]);
+                }
+              }
+            }
+            __syncwarp();
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&acc_empty[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (EPI == EPI_LSE && rc.valid && !*abort_flag) {
+        const SavedView& sv = p.ch.sv;
+        const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * p.ch.sh.U1 + rc.u;
+        const float ld = run_max + __logf(run_sum);
+        sv.lnPD[cell] = ld;
+        sv.lpb[cell] = h_blank - ld;
+        sv.lpl[cell] = (rc.u < rc.Ub) ? h_lab - ld : -INFINITY;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace
+}  // namespace rnnt
+
+// ===========================================================================
+// Elementwise helpers of the tensor-core path.
+namespace rnnt {
+namespace {
+
+// z rows of a chunk in bf16: tanh(pA[b,t] + pL[b,u]) (joint network, Eq. 3-4),
+// 0 on rows outside the lattice.  One block per tile, 8 consecutive h per thread.
+__global__ void __launch_bounds__(256)
+k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
+               __nv_bfloat16* __restrict__ Z) {
+  __shared__ TileRef tr;
+  if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
+  __syncthreads();
+  const int H = c.sh.H;
+  const int H8 = H / 8;
+  const long long row0 = (long long)blockIdx.x * TILE;
+  for (int e = threadIdx.x; e < TILE * H8; e += blockDim.x) {
+    const int i = e / H8, k8 = (e - i * H8) * 8;
+    const RowCell rc = row_of(tr, i);
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (rc.valid) {
+      const float4* a = (const float4*)(pA + ((size_t)rc.b * c.sh.T + rc.t) * H + k8);
+      const float4* l = (const float4*)(pL + ((size_t)rc.b * c.sh.U1 + rc.u) * H + k8);
+      const float4 a0 = a[0], a1 = a[1], l0 = l[0], l1 = l[1];
+      __nv_bfloat162 q0 = __floats2bfloat162_rn(tanhf(a0.x + l0.x), tanhf(a0.y + l0.y));
+      __nv_bfloat162 q1 = __floats2bfloat162_rn(tanhf(a0.z + l0.z), tanhf(a0.w + l0.w));
+      __nv_bfloat162 q2 = __floats2bfloat162_rn(tanhf(a1.x + l1.x), tanhf(a1.y + l1.y));
+      __nv_bfloat162 q3 = __floats2bfloat162_rn(tanhf(a1.z + l1.z), tanhf(a1.w + l1.w));
+      out.x = *(uint32_t*)&q0; out.y = *(uint32_t*)&q1;
+      out.z = *(uint32_t*)&q2; out.w = *(uint32_t*)&q3;
+    }
+    *(uint4*)(Z + (row0 + i) * H + k8) = out;
+  }
+}
+
+// dh from kept bf16 scores, in place (untiled mode; no recompute).
+__global__ void __launch_bounds__(256)
+k_dh_rows_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float* __restrict__ grad_loss) {
+  __shared__ TileRef tr;
+  if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
+  __syncthreads();
+  const int V = c.sh.V, lane = threadIdx.x & 31, U1 = c.sh.U1;
+  for (int i = threadIdx.x >> 5; i < TILE; i += blockDim.x >> 5) {
+    __nv_bfloat16* h = Hs + ((long long)blockIdx.x * TILE + i) * V;
+    const RowCell rc = row_of(tr, i);
+    if (!rc.valid) {
+      for (int v = lane; v < V; v += 32) h[v] = __float2bfloat16_rn(0.f);
+      continue;
+    }
+    const SavedView& sv = c.sv;
+    const size_t cell = ((size_t)rc.b * c.sh.T + rc.t) * U1 + rc.u;
+    const float lnP = sv.lnP[rc.b];
+    const float a = sv.alpha[cell];
+    float bn;
+    if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
+    else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
+    const float pb = __expf(a + sv.lpb[cell] + bn - lnP);
+    const float pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
+    const int y = (rc.u < rc.Ub) ? c.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
+    const float g = grad_loss ? grad_loss[rc.b] : 1.f;
+    const float lnPD = sv.lnPD[cell], gam = pb + pl;
+    for (int v = lane; v < V; v += 32) {
+      float d = gam * __expf(__bfloat162float(h[v]) - lnPD);
+      if (v == c.sh.blank) d -= pb;
+      if (v == y) d -= pl;
+      h[v] = __float2bfloat16_rn(g * d);
+    }
+  }
+}
+
+// out[n] += sum over rows of a bf16 [R][N] matrix.
+__global__ void __launch_bounds__(256)
+k_colsum_bf16(const __nv_bfloat16* __restrict__ X, long long R, int N, float* __restrict__ out,
+              long long rows_per) {
+  const int n = blockIdx.x * 256 + threadIdx.x;
+  if (n >= N) return;
+  const long long r0 = (long long)blockIdx.y * rows_per;
+  const long long r1 = min(R, r0 + rows_per);
+  float s = 0.f;
+  for (long long r = r0; r < r1; ++r) s += __bfloat162float(X[r * N + n]);
+  atomicAdd(out + n, s);
+}
+
+// bf16 copy of an fp32 [R][N] matrix.
+__global__ void k_f32_to_bf16(const float* __restrict__ x, __nv_bfloat16* __restrict__ y,
+                              size_t n) {
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n; i += stride) y[i] = __float2bfloat16_rn(x[i]);
+}
+
+// Copy of a bf16 [B*P][N] matrix whose row (b, q) is kept iff q < len[b], else 0.
+__global__ void k_mask_rows_bf16(const __nv_bfloat16* __restrict__ x,
+                                 __nv_bfloat16* __restrict__ y, int B, int P, int N,
+                                 const int32_t* __restrict__ len) {
+  const size_t n = (size_t)B * P * N;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n; i += stride) {
+    const size_t row = i / N;
+    const int b = (int)(row / P), q = (int)(row % P);
+    y[i] = (q < len[b]) ? x[i] : __float2bfloat16_rn(0.f);
+  }
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+int elementwise_grid(size_t n) {
+  size_t g = (n + 255) / 256;
+  const size_t cap = (size_t)num_sms() * 16;
+  return (int)std::max<size_t>(1, std::min(g, cap));
+}
+
+// ---- tensor maps ----------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] (cols contiguous), box 64 x box_rows,
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// One GEMM: C-shaped problem M x N x K with A = [M][K] (a_mn = 0) or [K][M]
+// (a_mn = 1) and B = [N][K] (b_mn = 0) or [K][N] (b_mn = 1), all bf16.
+struct GemmDesc {
+  const void* A;
+  int a_mn;
+  const void* B;
+  int b_mn;
+  int M, N, K;
+};
+
+template <int BN, int AMN, int BMN, int EPI>
+cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStream_t s) {
+  using C = Cfg<BN>;
+  CUtensorMap ta, tb;
+  const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64) : make_tmap(&ta, g.A, g.M, g.K, BM);
+  const bool ok_b = BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN, AMN, BMN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.m_tiles = (int)cdiv(g.M, BM);
+  p.n_tiles = (int)cdiv(g.N, BN);
+  p.kb_total = (int)cdiv(g.K, BK);
+  if (p.k_splits < 1) p.k_splits = 1;
+  p.kb_per_split = (int)cdiv(p.kb_total, p.k_splits);
+  p.k_splits = (int)cdiv(p.kb_total, p.kb_per_split);
+  p.units = p.row_complete ? p.m_tiles : p.m_tiles * p.n_tiles * p.k_splits;
+  if (p.units <= 0 || g.K <= 0) return cudaSuccess;
+  const int grid = std::min(p.units, max_units > 0 ? max_units : num_sms());
+  k_tc_gemm<BN, AMN, BMN, EPI><<<grid, NTHREADS, C::SMEM, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, cudaStream_t s) {
+  const int code = (bn == 256 ? 4 : 0) | (g.a_mn ? 2 : 0) | (g.b_mn ? 1 : 0);
+  switch (code) {
+    case 0: return launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
+    case 1: return launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
+    case 2: return launch_gemm_t<128, 1, 0, EPI>(g, p, 0, s);
+    case 3: return launch_gemm_t<128, 1, 1, EPI>(g, p, 0, s);
+    case 4: return launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s);
+    case 5: return launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s);
+    case 6: return launch_gemm_t<256, 1, 0, EPI>(g, p, 0, s);
+    default: return launch_gemm_t<256, 1, 1, EPI>(g, p, 0, s);
+  }
+}
+
+int pick_bn(int N) {
+  // the tile width that wastes the fewest MMA columns (ties: the wider one)
+  const long long w256 = cdiv(N, 256) * 256, w128 = cdiv(N, 128) * 128;
+  return w256 <= w128 ? 256 : 128;
+}
+
+// Split K so that about two units land on each SM, each with >= 4 K blocks.
+int pick_splits(int units_mn, int K) {
+  const int kb = (int)cdiv(K, BK);
+  int want = (2 * num_sms() + units_mn - 1) / units_mn;
+  want = std::min(want, std::max(1, kb / 4));
+  return std::max(1, want);
+}
+
+#define TC_CHECK(expr)                                   \
+  do {                                                   \
+    cudaError_t e_ = (expr);                             \
+    if (e_ != cudaSuccess) return e_;                    \
+  } while (0)
+
+}  // namespace
+
+// ===========================================================================
+// Entry points used by the C ABI (tc.h).
+
 bool tc_path_enabled() { return false; }
-rnnt_status tc_check_shape(const Plan&) { return RNNT_ERR_UNSUPPORTED_SHAPE; }
-cudaError_t tc_projection(const Plan&, const void*, const void*, const void*, int, int, float*,
-                          cudaStream_t) {
-  return cudaErrorNotSupported;
+
+rnnt_status tc_check_shape(const Plan& p) {
+  if (p.H % 8 || p.V % 8 || p.HA % 8 || p.HL % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
+  if (!encode_fn()) return RNNT_ERR_CUDA;
+  return RNNT_OK;
 }
-rnnt_status tc_forward_tiles(const Plan&, const SavedView&, const rnnt_params*, const int32_t*,
-                             const int32_t*, const int32_t*, const float*, const float*, void*,
-                             void*, cudaStream_t) {
-  return RNNT_ERR_UNSUPPORTED_SHAPE;
+
+cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const void* bias, int M,
+                          int K, float* out, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  ProfScope ps("tc_projection", s);
+  GemmDesc g{X, 0, W, 0, M, p.H, K};
+  TcParams tp{};
+  tp.C = out;
+  tp.ldc = p.H;
+  tp.bias = (const __nv_bfloat16*)bias;
+  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H), s);
 }
-rnnt_status tc_backward_tiles(const Plan&, const SavedView&, const rnnt_params*, const int32_t*,
-                              const int32_t*, const int32_t*, const float*, const float*,
-                              const float*, void*, void*, bool, float*, float*, float*, float*,
-                              cudaStream_t) {
-  return RNNT_ERR_UNSUPPORTED_SHAPE;
+
+namespace {
+
+rnnt_status chunk_total(const Plan& p, const SavedView& sv, cudaStream_t st, long long* n) {
+  const long long bound = cdiv(p.max_tiles, p.chunk_tiles);
+  if (bound <= 1) {
+    *n = bound;
+    return RNNT_OK;
+  }
+  int32_t total = 0;
+  if (cudaMemcpyAsync(&total, sv.total_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return RNNT_ERR_CUDA;
+  *n = cdiv(total, p.chunk_tiles);
+  return RNNT_OK;
 }
-rnnt_status tc_encoder_grads(const Plan&, char*, const void*, const void*, const rnnt_params*,
-                             const int32_t*, const int32_t*, float*, float*, float*, float*,
-                             float*, float*, float*, cudaStream_t) {
-  return RNNT_ERR_UNSUPPORTED_SHAPE;
+
+ChunkArgs make_chunk(const Plan& p, const SavedView& sv, long long k, const int32_t* labels,
+                     const int32_t* T_len, const int32_t* U_len) {
+  ChunkArgs c;
+  c.sh = Shape{p.B, p.T, p.U1, p.H, p.V, p.blank};
+  c.first_tile = k * p.chunk_tiles;
+  c.ntiles = p.chunk_tiles;
+  c.T_len = T_len;
+  c.U_len = U_len;
+  c.labels = labels;
+  c.sv = sv;
+  return c;
+}
+
+}  // namespace
+
+rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
+                             const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
+                             const float* pA, const float* pL, void* Zkeep, void* Hkeep,
+                             cudaStream_t s) {
+  // the z buffer: the kept z (untiled) or the tile workspace (caller's ws)
+  __nv_bfloat16* Z = (__nv_bfloat16*)Zkeep;
+  if (!Z) return RNNT_ERR_INVALID_ARG;
+  long long nch = 0;
+  rnnt_status st = chunk_total(p, sv, s, &nch);
+  if (st != RNNT_OK) return st;
+  for (long long k = 0; k < nch; ++k) {
+    ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
+    {
+      ProfScope ps("tc_build_z", s);
+      k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    }
+    ProfScope ps("tc_fwd_tiles", s);
+    GemmDesc g{Z, 0, pr->WO, 0, (int)p.chunk_rows, p.V, p.H};
+    TcParams tp{};
+    tp.row_complete = 1;
+    tp.bias = (const __nv_bfloat16*)pr->bO;
+    tp.ch = c;
+    tp.Hout = (__nv_bfloat16*)Hkeep;
+    tp.status = sv.status;
+    if (launch_gemm<EPI_LSE>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  return RNNT_OK;
+}
+
+rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
+                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
+                              const float* grad_loss, const float* pA, const float* pL, void* Zv,
+                              void* Hv, bool untiled, float* dA, float* dLr, float* dWO,
+                              float* dbO, cudaStream_t s) {
+  __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
+  __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
+  long long nch = 0;
+  rnnt_status st = chunk_total(p, sv, s, &nch);
+  if (st != RNNT_OK) return st;
+  const int rows = (int)p.chunk_rows;
+  for (long long k = 0; k < nch; ++k) {
+    ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
+    if (!untiled) {
+      {
+        ProfScope ps("tc_build_z", s);
+        k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+        if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      }
+      // recompute the tile's scores and overwrite them with dh
+      ProfScope ps("tc_bwd_dh", s);
+      GemmDesc g{Z, 0, pr->WO, 0, rows, p.V, p.H};
+      TcParams tp{};
+      tp.row_complete = 1;
+      tp.bias = (const __nv_bfloat16*)pr->bO;
+      tp.ch = c;
+      tp.grad_loss = grad_loss;
+      tp.Hout = Hs;
+      tp.status = sv.status;
+      if (launch_gemm<EPI_DH>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    } else {
+      ProfScope ps("tc_dh_kept", s);
+      k_dh_rows_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, Hs, grad_loss);
+      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    }
+    {  // dz = dh W^O, da = dz (1 - z^2) reduced into dA and dLr
+      ProfScope ps("tc_bwd_dz", s);
+      GemmDesc g{Hs, 0, pr->WO, 1, rows, p.H, p.V};
+      TcParams tp{};
+      tp.ch = c;
+      tp.Zin = Z;
+      tp.dA = dA;
+      tp.dLr = dLr;
+      tp.status = sv.status;
+      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H), s) != cudaSuccess) return RNNT_ERR_CUDA;
+    }
+    if (dWO) {  // dW^O += dh^T z, split over the chunk's rows
+      ProfScope ps("tc_bwd_dwo", s);
+      GemmDesc g{Hs, 1, Z, 1, p.V, p.H, rows};
+      TcParams tp{};
+      const int bn = pick_bn(p.H);
+      tp.k_splits = pick_splits((int)(cdiv(p.V, BM) * cdiv(p.H, bn)), rows);
+      tp.C = dWO;
+      tp.ldc = p.H;
+      tp.status = sv.status;
+      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    }
+    if (dbO) {
+      ProfScope ps("tc_colsum_dh", s);
+      long long rows_per = 512;
+      if (cdiv(rows, rows_per) > 65535) rows_per = cdiv(rows, 65535);
+      dim3 grid((unsigned)cdiv(p.V, 256), (unsigned)cdiv(rows, rows_per));
+      k_colsum_bf16<<<grid, 256, 0, s>>>(Hs, rows, p.V, dbO, rows_per);
+      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    }
+  }
+  return RNNT_OK;
+}
+
+rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
+                             const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,
+                             float* dA, float* dLr, float* dhA, float* dhL, float* dWA,
+                             float* dWL, float* dbZ, cudaStream_t s) {
+  __nv_bfloat16* dA16 = (__nv_bfloat16*)(ws + p.w_dA16);
+  __nv_bfloat16* dLr16 = (__nv_bfloat16*)(ws + p.w_dLr16);
+  __nv_bfloat16* hAm = (__nv_bfloat16*)(ws + p.w_hAm);
+  __nv_bfloat16* hLm = (__nv_bfloat16*)(ws + p.w_hLm);
+  const size_t nA = (size_t)p.B * p.T * p.H, nL = (size_t)p.B * p.U1 * p.H;
+  {
+    ProfScope ps("tc_enc_prep", s);
+    k_f32_to_bf16<<<elementwise_grid(nA), 256, 0, s>>>(dA, dA16, nA);
+    k_f32_to_bf16<<<elementwise_grid(nL), 256, 0, s>>>(dLr, dLr16, nL);
+    if (dWA) {
+      const size_t n = (size_t)p.B * p.T * p.HA;
+      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, s>>>((const __nv_bfloat16*)hA, hAm, p.B,
+                                                           p.T, p.HA, Teff);
+    }
+    if (dWL) {
+      const size_t n = (size_t)p.B * p.U1 * p.HL;
+      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, s>>>((const __nv_bfloat16*)hL, hLm, p.B,
+                                                           p.U1, p.HL, Ueff);
+    }
+    if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  ProfScope ps("tc_enc_grads", s);
+  const int MA = p.B * p.T, ML = p.B * p.U1;
+  if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
+    GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};
+    TcParams tp{};
+    tp.C = dhA;
+    tp.ldc = p.HA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA), s) != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  if (dhL) {
+    GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
+    TcParams tp{};
+    tp.C = dhL;
+    tp.ldc = p.HL;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL), s) != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  if (dWA) {  // dW^A = dA^T hA: A = dA16 as [K=MA][M=H], B = hAm as [K=MA][N=HA]
+    if (launch_zero(dWA, sizeof(float) * (size_t)p.H * p.HA, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    GemmDesc g{dA16, 1, hAm, 1, p.H, p.HA, MA};
+    TcParams tp{};
+    const int bn = pick_bn(p.HA);
+    tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HA, bn)), MA);
+    tp.C = dWA;
+    tp.ldc = p.HA;
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  if (dWL) {
+    if (launch_zero(dWL, sizeof(float) * (size_t)p.H * p.HL, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    GemmDesc g{dLr16, 1, hLm, 1, p.H, p.HL, ML};
+    TcParams tp{};
+    const int bn = pick_bn(p.HL);
+    tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HL, bn)), ML);
+    tp.C = dWL;
+    tp.ldc = p.HL;
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+  }
+  if (dbZ) {
+    if (launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, s) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+  }
+  return RNNT_OK;
 }
 
 }  // namespace rnnt
+
+// ===========================================================================
+// Test hook (include/rnnt_testing.h): one raw GEMM through the same kernel.
+extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A, int a_mn,
+                                              const void* B, int b_mn, float* C, int accumulate,
+                                              int k_splits, int bn, void* stream) {
+  using namespace rnnt;
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C) return RNNT_ERR_INVALID_ARG;
+  if ((a_mn ? M : K) % 8 || (b_mn ? N : K) % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
+  if (bn != 128 && bn != 256) return RNNT_ERR_INVALID_ARG;
+  if (!encode_fn()) return RNNT_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmDesc g{A, a_mn, B, b_mn, M, N, K};
+  TcParams tp{};
+  tp.C = C;
+  tp.ldc = N;
+  tp.k_splits = k_splits;
+  cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, s)
+                             : launch_gemm<EPI_STORE>(g, tp, bn, s);
+  return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
+}

@@ -308,8 +308,8 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
   void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
   if (p.tc) {
-    s = tc_forward_tiles(p, sv, pr, labels, T_len, U_len, pA, pL, untiled ? Z : nullptr,
-                         untiled ? Hs : nullptr, st);
+    s = tc_forward_tiles(p, sv, pr, labels, T_len, U_len, pA, pL, Z, untiled ? Hs : nullptr,
+                         st);
     if (s != RNNT_OK) return s;
   } else {
     long long nch = 0;

@@ -770,10 +770,9 @@ ChunkArgs make_chunk(const Plan& p, const SavedView& sv, long long k, const int3
 
 rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
-                             const float* pA, const float* pL, void* Zkeep, void* Hkeep,
+                             const float* pA, const float* pL, void* Zv, void* Hkeep,
                              cudaStream_t s) {
-  // the z buffer: the kept z (untiled) or the tile workspace (caller's ws)
-  __nv_bfloat16* Z = (__nv_bfloat16*)Zkeep;
+  __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   if (!Z) return RNNT_ERR_INVALID_ARG;
   long long nch = 0;
   rnnt_status st = chunk_total(p, sv, s, &nch);

@@ -11,11 +11,12 @@ rnnt_status tc_check_shape(const Plan& p);
 // out[M,H] = X[M,K] W[H,K]^T (+ bias[H]), bf16 operands, fp32 result.
 cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const void* bias, int M,
                           int K, float* out, cudaStream_t s);
-// Forward over every tile: lnPD, lpb, lpl into saved (and, when Zkeep/Hkeep are
-// given, the untiled mode's kept z and scores).
+// Forward over every tile: lnPD, lpb, lpl into saved.  Z is the z buffer (the
+// tile workspace, or the kept z in untiled mode); Hkeep, when given, receives
+// the scores (untiled mode).
 rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
-                             const float* pA, const float* pL, void* Zkeep, void* Hkeep,
+                             const float* pA, const float* pL, void* Z, void* Hkeep,
                              cudaStream_t s);
 // Backward over every tile: dA, dLr (accumulated), dW^O, db^O.
 rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,

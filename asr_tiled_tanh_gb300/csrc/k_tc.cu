@@ -716,7 +716,7 @@ int pick_splits(int units_mn, int K) {
 // ===========================================================================
 // Entry points used by the C ABI (tc.h).
 
-bool tc_path_enabled() { return false; }
+bool tc_path_enabled() { return true; }
 
 rnnt_status tc_check_shape(const Plan& p) {
   if (p.H % 8 || p.V % 8 || p.HA % 8 || p.HL % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;

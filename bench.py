@@ -101,6 +101,21 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
                             "tc_bwd_dwo": 2.0}
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(cells_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job cells/s: every rank processes its own batch (weak scaling)."""
+    return cells_per_rank * world / (ms / 1e3)
+
+
 def run_gpu_bench(args):
     import numpy as np
     import torch
@@ -170,12 +185,8 @@ def run_gpu_bench(args):
     peak_bytes = torch.cuda.max_memory_allocated(dev)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = nominal * world / (ms_max / 1e3)
+    ms_max = reduce_max(ms, dist, dev)
+    value = job_value(nominal, world, ms_max)
 
     # --- e2e: host buffers through the C ABI ----------------------------------
     host_in = {k: getattr(inp, k).pin_memory() for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO",
@@ -206,11 +217,7 @@ def run_gpu_bench(args):
         e2e_step()
         ee[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps, dist, dev)
     assert np.isfinite(host_loss.numpy()).all()
 
     # --- roofline of the dominant kernel ----------------------------------------
@@ -249,7 +256,7 @@ def run_gpu_bench(args):
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / tf_burst, 4),
-        "e2e": {"value": round(nominal * world / (e2e_ms / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(job_value(nominal, world, e2e_ms), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),

@@ -147,7 +147,7 @@ def run_gpu_bench(args):
     grads = r.alloc_grads()
     loss = torch.empty(wl.B, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
 
     def step():
         r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
@@ -173,7 +173,8 @@ def run_gpu_bench(args):
     with ClockSampler(dev.index) as clk:
         t0 = time.perf_counter()
         for i in range(args.steps):
-            flush.fill_(i & 0xff)
+            if args.flush_mb > 0:
+                flush.fill_(i & 0xff)
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -189,36 +190,38 @@ def run_gpu_bench(args):
     value = job_value(nominal, world, ms_max)
 
     # --- e2e: host buffers through the C ABI ----------------------------------
-    host_in = {k: getattr(inp, k).pin_memory() for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO",
-                                                          "labels", "T_len", "U_len")}
-    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in grads.items()}
-    host_loss = torch.empty(wl.B, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_loss.numel() * 4
+    e2e_ms, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        host_in = {k: getattr(inp, k).pin_memory() for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO",
+                                                              "labels", "T_len", "U_len")}
+        host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in grads.items()}
+        host_loss = torch.empty(wl.B, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_loss.numel() * 4
 
-    def e2e_step():
-        for k, v in host_in.items():
-            d[k].copy_(v, non_blocking=True)
-        step()
-        host_loss.copy_(loss, non_blocking=True)
-        for k, v in grads.items():
-            host_out[k].copy_(v, non_blocking=True)
+        def e2e_step():
+            for k, v in host_in.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            host_loss.copy_(loss, non_blocking=True)
+            for k, v in grads.items():
+                host_out[k].copy_(v, non_blocking=True)
 
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
-    torch.cuda.synchronize()
-    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        es[i].record(stream)
-        e2e_step()
-        ee[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps, dist, dev)
-    assert np.isfinite(host_loss.numpy()).all()
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps, dist, dev)
+        assert np.isfinite(host_loss.numpy()).all()
 
     # --- roofline of the dominant kernel ----------------------------------------
     hbm_peak, tf_burst, tf_sust, peak_src = _peaks()
@@ -256,9 +259,10 @@ def run_gpu_bench(args):
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / tf_burst, 4),
-        "e2e": {"value": round(job_value(nominal, world, e2e_ms), 1), "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_ms is None else {
+            "value": round(job_value(nominal, world, e2e_ms), 1), "unit": UNIT,
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "roofline": roof,
         "kernel_shares": shares,
@@ -345,6 +349,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush-mb", type=int, default=256,
+                    help="L2 flush buffer written before each timed step (0: none; profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3

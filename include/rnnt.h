@@ -101,8 +101,8 @@ typedef struct {
  *   alpha/beta the forward/backward variables of Eq. 8.  Every position
  *   outside a sample's lattice holds -inf.
  * lnP: fp32 [B], ln P(y_b|x_b) (NaN for a rejected sample).
- * status: one int32, the device status word (bit k set = rnnt_status k+... see
- *   rnnt_device_status).
+ * status: one int32, the device status word: bit k is set when a problem with
+ *   rnnt_status code k was detected (see rnnt_device_status).
  * z, h: untiled mode only (otherwise 0): z [cells,H] and the scores / their
  *   gradients [cells,V], element type = dims.dtype, rows in the library's
  *   tile order (not [B,T,U1]). */
@@ -151,6 +151,31 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
                      float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
                      void* ws, size_t ws_bytes, rnnt_stream stream);
+
+/* Size of the fixed device scratch array used by rnnt_fwd_noalloc. */
+#define RNNT_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Forward pass for callers that cannot allocate device memory at all: hosts
+ * that reserve every byte up front and forbid cudaMalloc afterwards, plugin
+ * interfaces that pass inputs and outputs but no allocator, and latency-
+ * critical loops where an allocation (or its failure) is not acceptable.
+ * The pages have no counterpart; it is a deployment convenience.
+ * Same arguments and results as rnnt_fwd, minus `ws`/`ws_bytes`: the scratch
+ * comes from one static device array of RNNT_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * that every GPU loading this library holds until the process exits.
+ * Returns RNNT_ERR_WORKSPACE_TOO_SMALL, before doing anything else, when
+ * rnnt_workspace_bytes(dims) exceeds that size (use a smaller tile_cells, or
+ * rnnt_fwd with your own buffer).  The first call on a device looks up the
+ * array's device address on that device (cudaGetSymbolAddress, with the
+ * device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array and it keeps the last call's
+ * contents; the forward needs none of it cleared.  Calls whose work overlaps
+ * on the GPU (other streams, other host threads) race on the array and must
+ * be serialized by the caller.  Allocates nothing. */
+rnnt_status rnnt_fwd_noalloc(const rnnt_dims* dims, const void* hA, const void* hL,
+                             const rnnt_params* params, const int32_t* labels,
+                             const int32_t* T_len, const int32_t* U_len, float* loss,
+                             void* saved, rnnt_stream stream);
 
 /* Synchronize `stream` and read the device status word in `saved`.  Returns
  * RNNT_OK if no device-side problem was recorded, else the first recorded

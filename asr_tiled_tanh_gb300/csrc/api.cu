@@ -323,7 +323,7 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
       LAUNCH("lse_rows", launch_lse_rows(c, (const float*)Hs, st));
     }
   }
-  LAUNCH("alpha_beta", launch_alpha_beta(sh, T_len, U_len, sv, loss, st));
+  LAUNCH("alpha_beta", launch_alpha_beta(sh, T_len, U_len, sv, loss, p.tc, st));
   return RNNT_OK;
 }
 

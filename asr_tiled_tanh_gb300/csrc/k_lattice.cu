@@ -7,12 +7,11 @@
 // and the per-sample loss -ln P(y_b|x_b).
 //
 // The recursion is walked along anti-diagonals d = t + u: every position of
-// a diagonal depends only on the previous diagonal, so one thread per label
-// position u advances the whole front at once.  The value handed from
-// position u-1 (alpha) or u+1 (beta) moves by a warp shuffle, and across warp
-// boundaries through a double-buffered shared-memory slot with one barrier
-// per diagonal.  The log-probabilities of the diagonals ahead are prefetched
-// into a register ring so the front never waits on a global load.
+// a diagonal depends only on the previous diagonal, so one warp advances the
+// whole front of a sample at once, each lane owning the label positions
+// u = lane + 32 j.  The value handed from position u-1 (alpha) or u+1 (beta)
+// moves by warp shuffles.  The log-probabilities of the diagonals ahead are
+// prefetched into a register ring so the front never waits on a global load.
 #include "kernels.h"
 
 namespace rnnt {
@@ -164,111 +163,149 @@ cudaError_t launch_eff_lengths(const Shape& sh, SavedView sv, const int32_t* T_l
 }
 
 // ---------------------------------------------------------------------------
-// alpha (blockIdx.y == 0) and beta (blockIdx.y == 1) of sample blockIdx.x.
-// Thread u owns label position u.  Step s walks diagonal d = s (alpha) or
-// d = T_b + U_b - 1 - s (beta); the thread's position on it is (d - u, u).
+// alpha (warp 0) and beta (warp 1) of sample blockIdx.x, one warp each.
+// Lane l owns label positions u = l + 32 j (j < NJ).  Step s walks diagonal
+// d = s (alpha) or d = T_b + U_b - 1 - s (beta); position (d - u, u).
 //   alpha(t,u) = logaddexp(alpha(t-1,u) + lpb(t-1,u), alpha(t,u-1) + lpl(t,u-1))
 //   beta(t,u)  = logaddexp(beta(t+1,u) + lpb(t,u),    beta(t,u+1) + lpl(t,u))
-// with alpha(0,0) = 0, beta(T_b,U_b) := 0 (the final blank leaves the
-// lattice) and -inf everywhere else outside the lattice.
-constexpr int AB_PF = 8;
+// with alpha(0,0) = 0, beta(T_b,U_b) := 0 (the final blank leaves the lattice)
+// and -inf everywhere else outside the lattice.  Every value a position needs
+// from a neighbour comes from the previous diagonal, so one diagonal is one
+// round of warp shuffles (no block barrier).  The log-probabilities of the PF
+// diagonals ahead sit in a register ring.
+template <bool FAST>
+__device__ __forceinline__ float lae(float a, float b) {
+  const float m = fmaxf(a, b);
+  if (m == -INFINITY) return -INFINITY;
+  const float d = -fabsf(a - b);
+  if (FAST) {
+    // ln(1 + e^d) = ln2 * log2(1 + 2^(d log2 e))
+    float e, l;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(d * 1.4426950408889634f));
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + e));
+    return m + 0.6931471805599453f * l;
+  }
+  return m + log1pf(expf(d));
+}
 
-__global__ void k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len,
-                             const int32_t* __restrict__ U_len, SavedView sv,
-                             float* __restrict__ loss) {
-  __shared__ float xbuf[2][32];
+template <int NJ, int PF, bool FAST>
+__global__ void __launch_bounds__(64)
+k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
+             SavedView sv, float* __restrict__ loss) {
   const int b = blockIdx.x;
-  const bool is_beta = blockIdx.y != 0;
+  const bool is_beta = threadIdx.x >= 32;
+  const int lane = threadIdx.x & 31;
   if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample: stays -inf / NaN
   const int Tb = T_len[b], Ub = U_len[b];
   const int U1 = sh.U1;
-  const int u = threadIdx.x, lane = u & 31, w = u >> 5, NW = blockDim.x >> 5;
   const size_t base = (size_t)b * sh.T * U1;
   const float* __restrict__ LPB = sv.lpb + base;
   const float* __restrict__ LPL = sv.lpl + base;
   float* __restrict__ OUT = (is_beta ? sv.beta : sv.alpha) + base;
   const int ndiag = Tb + Ub;
-  const bool u_ok = u <= Ub;
-  if (threadIdx.x < 64) (&xbuf[0][0])[threadIdx.x] = -INFINITY;
-  __syncthreads();
 
-  float rb[AB_PF], rl[AB_PF];
+  float rb[PF][NJ], rl[PF][NJ];
 #pragma unroll
-  for (int k = 0; k < AB_PF; ++k) {
+  for (int k = 0; k < PF; ++k) {
     const int d = is_beta ? ndiag - 1 - k : k;
-    const int t = d - u;
-    const bool in = k < ndiag && u_ok && t >= 0 && t < Tb;
-    rb[k] = in ? LPB[(size_t)t * U1 + u] : -INFINITY;
-    rl[k] = in ? LPL[(size_t)t * U1 + u] : -INFINITY;
-  }
-  float own = -INFINITY;   // alpha: alpha+lpb of the own position one diagonal back
-                           // beta:  beta of the own position one diagonal back
-  float send = -INFINITY;  // alpha: alpha+lpl handed to u+1; beta: beta handed to u-1
-
-  for (int sb = 0; sb < ndiag; sb += AB_PF) {
 #pragma unroll
-    for (int k = 0; k < AB_PF; ++k) {
+    for (int j = 0; j < NJ; ++j) {
+      const int u = lane + 32 * j, t = d - u;
+      const bool in = k < ndiag && u <= Ub && t >= 0 && t < Tb;
+      rb[k][j] = in ? LPB[(size_t)t * U1 + u] : -INFINITY;
+      rl[k][j] = in ? LPL[(size_t)t * U1 + u] : -INFINITY;
+    }
+  }
+  float own[NJ], send[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
+
+  for (int sb = 0; sb < ndiag; sb += PF) {
+#pragma unroll
+    for (int k = 0; k < PF; ++k) {
       const int s = sb + k;
-      if (s < ndiag) {  // uniform over the block
+      if (s < ndiag) {  // uniform over the warp
         const int d = is_beta ? ndiag - 1 - s : s;
-        const int t = d - u;
-        const float lb = rb[k], ll = rl[k];
-        {
-          const int s2 = s + AB_PF;
-          const int d2 = is_beta ? ndiag - 1 - s2 : s2;
-          const int t2 = d2 - u;
-          const bool in2 = s2 < ndiag && u_ok && t2 >= 0 && t2 < Tb;
-          rb[k] = in2 ? LPB[(size_t)t2 * U1 + u] : -INFINITY;
-          rl[k] = in2 ? LPL[(size_t)t2 * U1 + u] : -INFINITY;
-        }
-        float nb;
-        if (!is_beta) {
-          nb = __shfl_up_sync(0xffffffffu, send, 1);
-          if (lane == 0) nb = (w > 0) ? xbuf[(s + 1) & 1][w - 1] : -INFINITY;
-        } else {
-          nb = __shfl_down_sync(0xffffffffu, send, 1);
-          if (lane == 31) nb = (w < NW - 1) ? xbuf[(s + 1) & 1][w + 1] : -INFINITY;
-        }
-        float val = -INFINITY;
-        const bool in = u_ok && t >= 0 && t < Tb;
-        if (in) {
+        float nb[NJ];
+        // neighbour values from the previous diagonal
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
           if (!is_beta) {
-            val = (s == 0) ? 0.f : logaddexp_f(own, nb);
+            float x = __shfl_up_sync(0xffffffffu, send[j], 1);
+            const float y = __shfl_sync(0xffffffffu, j > 0 ? send[j - 1] : -INFINITY, 31);
+            nb[j] = lane == 0 ? y : x;
           } else {
-            const float from_t = (t + 1 < Tb) ? own : (u == Ub ? 0.f : -INFINITY);
-            val = logaddexp_f(from_t + lb, nb + ll);
+            float x = __shfl_down_sync(0xffffffffu, send[j], 1);
+            const float y = __shfl_sync(0xffffffffu, j + 1 < NJ ? send[j + 1] : -INFINITY, 0);
+            nb[j] = lane == 31 ? y : x;
           }
-          OUT[(size_t)t * U1 + u] = val;
         }
-        if (!is_beta) {
-          own = val + lb;
-          send = val + ll;
-        } else {
-          own = val;
-          send = val;
-        }
-        if (NW > 1) {
-          if (!is_beta && lane == 31) xbuf[s & 1][w] = send;
-          if (is_beta && lane == 0) xbuf[s & 1][w] = send;
-          __syncthreads();
+        const int s2 = s + PF;
+        const int d2 = is_beta ? ndiag - 1 - s2 : s2;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int u = lane + 32 * j, t = d - u;
+          const float lb = rb[k][j], ll = rl[k][j];
+          {
+            const int t2 = d2 - u;
+            const bool in2 = s2 < ndiag && u <= Ub && t2 >= 0 && t2 < Tb;
+            rb[k][j] = in2 ? LPB[(size_t)t2 * U1 + u] : -INFINITY;
+            rl[k][j] = in2 ? LPL[(size_t)t2 * U1 + u] : -INFINITY;
+          }
+          float val = -INFINITY;
+          if (u <= Ub && t >= 0 && t < Tb) {
+            if (!is_beta) {
+              val = (s == 0) ? 0.f : lae<FAST>(own[j], nb[j]);
+            } else {
+              const float from_t = (t + 1 < Tb) ? own[j] : (u == Ub ? 0.f : -INFINITY);
+              val = lae<FAST>(from_t + lb, nb[j] + ll);
+            }
+            OUT[(size_t)t * U1 + u] = val;
+          }
+          if (!is_beta) {
+            own[j] = val + lb;   // alpha + lpb: the blank move to (t+1, u)
+            send[j] = val + ll;  // alpha + lpl: the label move to (t, u+1)
+          } else {
+            own[j] = val;
+            send[j] = val;
+          }
         }
       }
     }
   }
-  // ln P = alpha(T_b-1, U_b) + lpb(T_b-1, U_b): the own value of thread U_b
+  // ln P = alpha(T_b-1, U_b) + lpb(T_b-1, U_b): the own value at u = U_b
   // after the last diagonal.
-  if (!is_beta && u == Ub) {
-    sv.lnP[b] = own;
-    loss[b] = -own;
+  if (!is_beta) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (lane + 32 * j == Ub) {
+        sv.lnP[b] = own[j];
+        loss[b] = -own[j];
+      }
+    }
   }
 }
 
-cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
-                              SavedView sv, float* loss, cudaStream_t s) {
-  if (sh.B == 0) return cudaSuccess;
-  const int threads = (int)cdiv(sh.U1, 32) * 32;
-  k_alpha_beta<<<dim3(sh.B, 2), threads, 0, s>>>(sh, T_len, U_len, sv, loss);
+template <bool FAST>
+static cudaError_t launch_ab(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                             SavedView sv, float* loss, cudaStream_t s) {
+  const int nj = (int)cdiv(sh.U1, 32);
+  dim3 g(sh.B), blk(64);
+  if (nj <= 1) k_alpha_beta<1, 16, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else if (nj <= 2) k_alpha_beta<2, 16, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else if (nj <= 4) k_alpha_beta<4, 12, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else if (nj <= 8) k_alpha_beta<8, 6, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else if (nj <= 16) k_alpha_beta<16, 3, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else k_alpha_beta<32, 1, FAST><<<g, blk, 0, s>>>(sh, T_len, U_len, sv, loss);
   return cudaGetLastError();
+}
+
+cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                              SavedView sv, float* loss, bool fast, cudaStream_t s) {
+  if (sh.B == 0) return cudaSuccess;
+  if (sh.U1 > 1024) return cudaErrorInvalidValue;
+  return fast ? launch_ab<true>(sh, T_len, U_len, sv, loss, s)
+              : launch_ab<false>(sh, T_len, U_len, sv, loss, s);
 }
 
 }  // namespace rnnt

@@ -58,6 +58,7 @@ struct TcParams {
   const __nv_bfloat16* Zin;  // DA: z [rows][N]
   float* dA;
   float* dLr;
+  float* dbO;            // DH: column sums of dh accumulated here (may be NULL)
   int32_t* status;
 };
 
@@ -133,12 +134,195 @@ __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
 }
 
+// 32 bias values of columns col0.. (0 beyond N or without a bias).
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int N, int col0,
+                                            float* bb) {
+  if (!bias) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bb[j] = 0.f;
+    return;
+  }
+  if (col0 + 32 <= N && (N & 7) == 0) {
+    const uint4* q = (const uint4*)(bias + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = __ldg(q + i);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h2 = *(const __nv_bfloat162*)&u[k];
+        bb[i * 8 + 2 * k] = __low2float(h2);
+        bb[i * 8 + 2 * k + 1] = __high2float(h2);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bb[j] = (col0 + j < N) ? bf(bias, col0 + j) : 0.f;
+  }
+}
+
+// 32 bf16 values at p (16-byte aligned) widened to fp32.
+__device__ __forceinline__ void unpack32(const uint4* q, float* out) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162 h2 = *(const __nv_bfloat162*)&u[k];
+      out[i * 8 + 2 * k] = __low2float(h2);
+      out[i * 8 + 2 * k + 1] = __high2float(h2);
+    }
+  }
+}
+
 // Select v[j] for a runtime j in [0,32) without local memory.
 __device__ __forceinline__ float pick32(const float* v, int j) {
   float r = 0.f;
 #pragma unroll
   for (int k = 0; k < 32; ++k) r = (k == j) ? v[k] : r;
   return r;
+}
+
+// ---- lattice epilogues, per TMEM lane (one lattice position per thread) ----
+constexpr float kLog2e = 1.4426950408889634f;
+
+// f^W_1 (Eq. 7) as an online log-sum-exp over the V scores of the position,
+// plus the blank and label scores; only these leave the SM.
+struct LseState {
+  float run_max, run_sum, h_blank, h_lab;
+  int lab;
+};
+
+__device__ __forceinline__ void lse_init(LseState& st, const TcParams& p, const RowCell& rc) {
+  st.run_max = -INFINITY;
+  st.run_sum = 0.f;
+  st.h_blank = 0.f;
+  st.h_lab = 0.f;
+  st.lab = (rc.valid && rc.u < rc.Ub) ? p.ch.labels[(size_t)rc.b * p.ch.sh.U1 + rc.u + 1] : -1;
+}
+
+// 32 scores v[] (accumulator values, bias not yet added) of columns col0.. .
+// keep: where to store the scores (untiled mode), or NULL.
+__device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const RowCell& rc,
+                                          float* v, int col0, __nv_bfloat16* keep) {
+  if (!rc.valid) return;
+  const int nv = min(32, p.N - col0);
+  float bb[32];
+  load_bias32(p.bias, p.N, col0, bb);
+  float cm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] += bb[j];
+    cm = (j < nv) ? fmaxf(cm, v[j]) : cm;
+  }
+  const float nm = fmaxf(st.run_max, cm);
+  float s = st.run_sum * ptx::ex2((st.run_max - nm) * kLog2e);
+  const float nmL = nm * kLog2e;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) s += (j < nv) ? ptx::ex2(fmaf(v[j], kLog2e, -nmL)) : 0.f;
+  st.run_sum = s;
+  st.run_max = nm;
+  const int jb = p.ch.sh.blank - col0;
+  if (jb >= 0 && jb < 32) st.h_blank = pick32(v, jb);
+  const int jl = st.lab - col0;
+  if (jl >= 0 && jl < 32) st.h_lab = pick32(v, jl);
+  if (keep) {
+    for (int j = 0; j < nv; j += 2) {
+      if (j + 1 < nv) *(__nv_bfloat162*)(keep + j) = __floats2bfloat162_rn(v[j], v[j + 1]);
+      else keep[j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p,
+                                           const RowCell& rc) {
+  if (!rc.valid) return;
+  const SavedView& sv = p.ch.sv;
+  const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * p.ch.sh.U1 + rc.u;
+  const float ld = st.run_max + __logf(st.run_sum);
+  sv.lnPD[cell] = ld;
+  sv.lpb[cell] = st.h_blank - ld;
+  sv.lpl[cell] = (rc.u < rc.Ub) ? st.h_lab - ld : -INFINITY;
+}
+
+// f^W_4 (Eq. 10): dh_v = g ((pb + pl) softmax_v - pb [v = blank] - pl [v = label]).
+struct DhState {
+  float pb, pl, gam, lnPD, g;
+  int lab;
+};
+
+__device__ __forceinline__ void dh_init(DhState& st, const TcParams& p, const RowCell& rc) {
+  st.pb = st.pl = st.gam = st.lnPD = 0.f;
+  st.g = 1.f;
+  st.lab = -1;
+  if (!rc.valid) return;
+  const SavedView& sv = p.ch.sv;
+  const int U1 = p.ch.sh.U1;
+  const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * U1 + rc.u;
+  const float lnP = sv.lnP[rc.b];
+  const float a = sv.alpha[cell];
+  float bn;
+  if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
+  else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
+  st.pb = __expf(a + sv.lpb[cell] + bn - lnP);
+  st.pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
+  st.gam = st.pb + st.pl;
+  st.lnPD = sv.lnPD[cell];
+  st.g = p.grad_loss ? p.grad_loss[rc.b] : 1.f;
+  st.lab = (rc.u < rc.Ub) ? p.ch.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
+}
+
+// dh of 32 columns written as bf16 to dst (0 for positions outside the
+// lattice); when dbO is given, the warp's 32 rows are also summed per column
+// (through the warp's shared-memory scratch) and added to dbO.
+__device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
+                                         const float* v, int col0, __nv_bfloat16* dst,
+                                         float* wscr, bool write) {
+  const int nv = min(32, p.N - col0);
+  float d[32];
+  if (rc.valid) {
+    float bb[32];
+    load_bias32(p.bias, p.N, col0, bb);
+    const float nl = st.lnPD * kLog2e;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float x = st.gam * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -nl));
+      if (col0 + j == p.ch.sh.blank) x -= st.pb;
+      if (col0 + j == st.lab) x -= st.pl;
+      d[j] = st.g * x;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) d[j] = 0.f;
+  }
+  if (write) {
+    if (nv == 32 && (p.N & 7) == 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        __nv_bfloat162 q0 = __floats2bfloat162_rn(d[j], d[j + 1]);
+        __nv_bfloat162 q1 = __floats2bfloat162_rn(d[j + 2], d[j + 3]);
+        __nv_bfloat162 q2 = __floats2bfloat162_rn(d[j + 4], d[j + 5]);
+        __nv_bfloat162 q3 = __floats2bfloat162_rn(d[j + 6], d[j + 7]);
+        uint4 pk;
+        pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
+        pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
+        *(uint4*)(dst + j) = pk;
+      }
+    } else {
+      for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
+    }
+  }
+  if (p.dbO) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = d[j];
+    __syncwarp();
+    float cs = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) cs += wscr[r * 33 + lane];
+    if (col0 + lane < p.N && cs != 0.f) ptx::red_add_f32(p.dbO + col0 + lane, cs);
+    __syncwarp();
+  }
 }
 
 template <int BN, int A_MN, int B_MN, int EPI>
@@ -293,30 +477,14 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       // per-unit state of the lattice epilogues
       TileRef tr{};
       RowCell rc{};
-      float run_max = -INFINITY, run_sum = 0.f, h_blank = 0.f, h_lab = 0.f;
-      int lab = -1;
-      float pb = 0.f, pl = 0.f, gam = 0.f, lnPD = 0.f, g = 1.f;
+      LseState ls;
+      DhState ds;
       if (EPI == EPI_LSE || EPI == EPI_DH || EPI == EPI_DA) {
         tr = tile_ref(p.ch, w.m);
         rc = row_of(tr, row);
       }
-      if ((EPI == EPI_LSE || EPI == EPI_DH) && rc.valid && rc.u < rc.Ub)
-        lab = p.ch.labels[(size_t)rc.b * p.ch.sh.U1 + rc.u + 1];
-      if (EPI == EPI_DH && rc.valid) {
-        const SavedView& sv = p.ch.sv;
-        const int U1 = p.ch.sh.U1;
-        const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * U1 + rc.u;
-        const float lnP = sv.lnP[rc.b];
-        const float a = sv.alpha[cell];
-        float bn;
-        if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
-        else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
-        pb = __expf(a + sv.lpb[cell] + bn - lnP);
-        pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
-        gam = pb + pl;
-        lnPD = sv.lnPD[cell];
-        g = p.grad_loss ? p.grad_loss[rc.b] : 1.f;
-      }
+      if (EPI == EPI_LSE) lse_init(ls, p, rc);
+      if (EPI == EPI_DH) dh_init(ds, p, rc);
       for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
         if (!ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
           report_timeout(p, abort_flag);
@@ -336,8 +504,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               float* dst = p.C + grow * p.ldc + col0;
               if (EPI == EPI_STORE) {
                 if (p.bias) {
+                  float bb[32];
+                  load_bias32(p.bias, p.N, col0, bb);
 #pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] += (col0 + j < p.N) ? bf(p.bias, col0 + j) : 0.f;
+                  for (int j = 0; j < 32; ++j) v[j] += bb[j];
                 }
                 if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
@@ -346,117 +516,70 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 } else {
                   for (int j = 0; j < 32 && col0 + j < p.N; ++j) dst[j] = v[j];
                 }
+              } else if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) ptx::red_add_v4(dst + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
               } else {
                 for (int j = 0; j < 32 && col0 + j < p.N; ++j) ptx::red_add_f32(dst + j, v[j]);
               }
             }
           } else if (EPI == EPI_LSE) {
-            if (rc.valid) {
-              const int nv = min(32, p.N - col0);
-              float cm = -INFINITY;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if (p.bias) v[j] += (j < nv) ? bf(p.bias, col0 + j) : 0.f;
-                cm = (j < nv) ? fmaxf(cm, v[j]) : cm;
-              }
-              const float nm = fmaxf(run_max, cm);
-              const float L2E = 1.4426950408889634f;
-              float s = run_sum * ptx::ex2((run_max - nm) * L2E);
-              const float nmL = nm * L2E;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) s += (j < nv) ? ptx::ex2(fmaf(v[j], L2E, -nmL)) : 0.f;
-              run_sum = s;
-              run_max = nm;
-              const int jb = p.ch.sh.blank - col0;
-              if (jb >= 0 && jb < 32) h_blank = pick32(v, jb);
-              const int jl = lab - col0;
-              if (jl >= 0 && jl < 32) h_lab = pick32(v, jl);
-              if (p.Hout) {  // untiled mode keeps the scores
-                __nv_bfloat16* dst = p.Hout + ((long long)w.m * BM + row) * p.N + col0;
-                for (int j = 0; j < nv; j += 2) {
-                  if (j + 1 < nv) *(__nv_bfloat162*)(dst + j) = __floats2bfloat162_rn(v[j], v[j + 1]);
-                  else dst[j] = __float2bfloat16_rn(v[j]);
-                }
-              }
-            }
+            lse_chunk(ls, p, rc, v, col0,
+                      p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
           } else if (EPI == EPI_DH) {
-            const int nv = min(32, p.N - col0);
-            __nv_bfloat16* dst = p.Hout + ((long long)w.m * BM + row) * p.N + col0;
-            float d[32];
-            if (rc.valid) {
-              const float L2E = 1.4426950408889634f;
-              const float nl = lnPD * L2E;
+            dh_chunk(ds, p, rc, v, col0, p.Hout + ((long long)w.m * BM + row) * p.N + col0, wscr,
+                     w.m < p.ch.ntiles);
+          } else if (EPI == EPI_DA) {
+            // da = dz (1 - z^2) on the thread's own row, then transpose the
+            // warp's 32 rows x 32 columns through shared memory (lane =
+            // column) and sum over the tile's u (dA) and t (dLr).
+            float da[32];
+            if (rc.valid && col0 + 32 <= p.N && (p.N & 7) == 0) {
+              uint4 zq[4];
+              const uint4* zp = (const uint4*)(p.Zin + ((long long)w.m * BM + row) * p.N + col0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) zq[i] = __ldg(zp + i);
+              float z[32];
+              unpack32(zq, z);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) da[j] = v[j] * (1.f - z[j] * z[j]);
+            } else if (rc.valid) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                const float h = v[j] + ((p.bias && j < nv) ? bf(p.bias, col0 + j) : 0.f);
-                float x = gam * ptx::ex2(fmaf(h, L2E, -nl));
-                if (col0 + j == p.ch.sh.blank) x -= pb;
-                if (col0 + j == lab) x -= pl;
-                d[j] = g * x;
+                const float z = (col0 + j < p.N)
+                                    ? bf(p.Zin, ((long long)w.m * BM + row) * p.N + col0 + j) : 0.f;
+                da[j] = (col0 + j < p.N) ? v[j] * (1.f - z * z) : 0.f;
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) d[j] = 0.f;
+              for (int j = 0; j < 32; ++j) da[j] = 0.f;
             }
-            if (w.m < p.ch.ntiles) {
-              if (nv == 32 && (p.N & 7) == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                  __nv_bfloat162 q0 = __floats2bfloat162_rn(d[j], d[j + 1]);
-                  __nv_bfloat162 q1 = __floats2bfloat162_rn(d[j + 2], d[j + 3]);
-                  __nv_bfloat162 q2 = __floats2bfloat162_rn(d[j + 4], d[j + 5]);
-                  __nv_bfloat162 q3 = __floats2bfloat162_rn(d[j + 6], d[j + 7]);
-                  uint4 pk;
-                  pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
-                  pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
-                  *(uint4*)(dst + j) = pk;
-                }
-              } else {
-                for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
-              }
-            }
-          } else if (EPI == EPI_DA) {
-            // Transpose the warp's 32 rows x 32 columns through shared memory:
-            // lane = column, then sum over the tile's u (dA) and t (dLr).
-#pragma unroll
-            for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = v[j];
+            for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = da[j];
             __syncwarp();
             const int col = col0 + lane;
-            if (col < p.N) {
-              // this warp's rows are tile positions sub*32 .. sub*32+31:
-              // t = t0 + sub*4 + r/8, u = u0 + r%8
+            const int tw = tr.t0 + sub * 4;  // this warp's rows: t = tw + r/8, u = u0 + r%8
+            if (col < p.N && tr.exists && tw < tr.Tb) {
               float sum_u[TU];
 #pragma unroll
               for (int k = 0; k < TU; ++k) sum_u[k] = 0.f;
-              const long long rbase = (long long)w.m * BM + sub * 32;
-              const int tw = tr.t0 + sub * 4;
 #pragma unroll
               for (int tq = 0; tq < 4; ++tq) {
-                const int t = tw + tq;
                 float st = 0.f;
 #pragma unroll
                 for (int k = 0; k < TU; ++k) {
-                  const int r = tq * TU + k;
-                  const int uu = tr.u0 + k;
-                  float da = 0.f;
-                  if (tr.exists && t < tr.Tb && uu <= tr.Ub) {
-                    const float z = bf(p.Zin, (rbase + r) * p.N + col);
-                    da = wscr[r * 33 + lane] * (1.f - z * z);
-                  }
-                  st += da;
-                  sum_u[k] += da;
+                  const float x = wscr[(tq * TU + k) * 33 + lane];
+                  st += x;
+                  sum_u[k] += x;
                 }
-                if (tr.exists && t < tr.Tb)
-                  ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + t) * p.N + col, st);
+                if (tw + tq < tr.Tb)
+                  ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + tw + tq) * p.N + col, st);
               }
-              if (tr.exists && tw < tr.Tb) {
 #pragma unroll
-                for (int k = 0; k < TU; ++k) {
-                  const int uu = tr.u0 + k;
-                  if (uu <= tr.Ub)
-                    ptx::red_add_f32(p.dLr + ((size_t)tr.b * p.ch.sh.U1 + uu) * p.N + col,
-                                     sum_u[k]);
-                }
+              for (int k = 0; k < TU; ++k) {
+                if (tr.u0 + k <= tr.Ub)
+                  ptx::red_add_f32(p.dLr + ((size_t)tr.b * p.ch.sh.U1 + tr.u0 + k) * p.N + col,
+                                   sum_u[k]);
               }
             }
             __syncwarp();
@@ -466,14 +589,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         ptx::mbar_arrive(&acc_empty[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      if (EPI == EPI_LSE && rc.valid && !*abort_flag) {
-        const SavedView& sv = p.ch.sv;
-        const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * p.ch.sh.U1 + rc.u;
-        const float ld = run_max + __logf(run_sum);
-        sv.lnPD[cell] = ld;
-        sv.lpb[cell] = h_blank - ld;
-        sv.lpl[cell] = (rc.u < rc.Ub) ? h_lab - ld : -INFINITY;
-      }
+      if (EPI == EPI_LSE && !*abort_flag) lse_finish(ls, p, rc);
     }
   }
   ptx::tc_fence_before();
@@ -495,14 +611,16 @@ namespace {
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
+  // block (x = tile, y = quarter of its 128 rows)
   __shared__ TileRef tr;
   if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
   __syncthreads();
   const int H = c.sh.H;
   const int H8 = H / 8;
+  const int r0 = blockIdx.y * (TILE / 4);
   const long long row0 = (long long)blockIdx.x * TILE;
-  for (int e = threadIdx.x; e < TILE * H8; e += blockDim.x) {
-    const int i = e / H8, k8 = (e - i * H8) * 8;
+  for (int e = threadIdx.x; e < (TILE / 4) * H8; e += blockDim.x) {
+    const int i = r0 + e / H8, k8 = (e % H8) * 8;
     const RowCell rc = row_of(tr, i);
     uint4 out = make_uint4(0, 0, 0, 0);
     if (rc.valid) {
@@ -697,11 +815,11 @@ int pick_bn(int N) {
   return w256 <= w128 ? 256 : 128;
 }
 
-// Split K so that about two units land on each SM, each with >= 4 K blocks.
+// Split K so that the units fill the SMs once, each with >= 8 K blocks.
 int pick_splits(int units_mn, int K) {
   const int kb = (int)cdiv(K, BK);
-  int want = (2 * num_sms() + units_mn - 1) / units_mn;
-  want = std::min(want, std::max(1, kb / 4));
+  int want = (num_sms() + units_mn - 1) / units_mn;
+  want = std::min(want, std::max(1, kb / 8));
   return std::max(1, want);
 }
 
@@ -781,7 +899,7 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     {
       ProfScope ps("tc_build_z", s);
-      k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+      k_build_z_bf16<<<dim3((unsigned)c.ntiles, 4), 256, 0, s>>>(c, pA, pL, Z);
       if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
     }
     ProfScope ps("tc_fwd_tiles", s);
@@ -813,7 +931,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
     if (!untiled) {
       {
         ProfScope ps("tc_build_z", s);
-        k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+        k_build_z_bf16<<<dim3((unsigned)c.ntiles, 4), 256, 0, s>>>(c, pA, pL, Z);
         if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
       }
       // recompute the tile's scores and overwrite them with dh
@@ -825,6 +943,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.ch = c;
       tp.grad_loss = grad_loss;
       tp.Hout = Hs;
+      tp.dbO = dbO;
       tp.status = sv.status;
       if (launch_gemm<EPI_DH>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
@@ -854,7 +973,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.status = sv.status;
       if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
-    if (dbO) {
+    if (dbO && untiled) {  // the tiled path sums dh inside the dh epilogue
       ProfScope ps("tc_colsum_dh", s);
       long long rows_per = 512;
       if (cdiv(rows, rows_per) > 65535) rows_per = cdiv(rows, 65535);

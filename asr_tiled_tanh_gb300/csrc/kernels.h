@@ -12,8 +12,9 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 cudaError_t launch_index(const Shape& sh, const int32_t* labels, const int32_t* T_len,
                          const int32_t* U_len, SavedView sv, float* loss, cudaStream_t s);
 // alpha/beta wavefronts over every sample's lattice; writes lnP and loss.
+// fast: approximate ex2/lg2 in logaddexp (bf16 path); else expf/log1pf.
 cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
-                              SavedView sv, float* loss, cudaStream_t s);
+                              SavedView sv, float* loss, bool fast, cudaStream_t s);
 
 // Effective lengths for masked contractions over encoder rows: T_len[b] and
 // U_len[b]+1 for accepted samples, 0 for rejected ones.

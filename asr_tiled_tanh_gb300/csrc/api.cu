@@ -58,9 +58,9 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
     if (d->tile_cells > 0) {
       ct = cdiv(d->tile_cells, TILE);
     } else {
-      // default: about 64 MiB of tile buffers, at least one tile per SM
+      // default: at most 512 MiB of tile buffers, in whole waves of 152 tiles
       const long long per_tile = (long long)TILE * (H * p->zelem + V * p->helem);
-      ct = (64LL << 20) / per_tile;
+      ct = (512LL << 20) / per_tile;
       ct = ct / 152 * 152;
       if (ct < 152) ct = 152;
     }
@@ -296,11 +296,10 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
   LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
   if (p.B == 0) return RNNT_OK;
   const size_t ncell = (size_t)p.B * p.T * p.U1;
-  LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY, ncell, st));
-  LAUNCH("fill_f32", launch_fill_f32(sv.lpl, -INFINITY, ncell, st));
-  LAUNCH("fill_f32", launch_fill_f32(sv.lnPD, -INFINITY, ncell, st));
-  LAUNCH("fill_f32", launch_fill_f32(sv.alpha, -INFINITY, ncell, st));
-  LAUNCH("fill_f32", launch_fill_f32(sv.beta, -INFINITY, ncell, st));
+  // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
+  (void)ncell;
+  LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY,
+                                     (p.s_beta - p.s_lpb) / 4 + (size_t)p.B * p.T * p.U1, st));
   rnnt_status s = projections(p, hA, hL, pr, pA, pL, st);
   if (s != RNNT_OK) return s;
 

@@ -37,8 +37,9 @@ namespace {
 
 constexpr int BM = 128;              // rows per tile (TMEM lanes)
 constexpr int BK = 64;               // K per stage: one 128-byte swizzle atom of bf16
-constexpr int NTHREADS = 192;
-constexpr int EPI_WARP0 = 2;         // first epilogue warp
+constexpr int NTHREADS = 320;
+constexpr int EPI_WARP0 = 2;         // first of 8 epilogue warps (two per TMEM lane quarter)
+constexpr int EPI_THREADS = 256;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait, then give up
 constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
 
@@ -67,11 +68,13 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int EPI_SCRATCH = 4 * 32 * 33 * 4;
+  static constexpr int EPI_SCRATCH = 8 * 32 * 17 * 4;   // per epilogue warp: 32 rows x 16 cols
+  static constexpr int COMB_BYTES = 2 * 128 * 4 * 4;     // LSE halves, double-buffered
   static constexpr int BAR_BYTES = 256;
-  static constexpr int STAGES_RAW = (SMEM_LIMIT - 1024 - EPI_SCRATCH - BAR_BYTES) / STAGE;
+  static constexpr int STAGES_RAW =
+      (SMEM_LIMIT - 1024 - EPI_SCRATCH - COMB_BYTES - BAR_BYTES) / STAGE;
   static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_SCRATCH + BAR_BYTES;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_SCRATCH + COMB_BYTES + BAR_BYTES;
   static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
 };
 
@@ -313,15 +316,22 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
     }
   }
   if (p.dbO) {
-    const int lane = threadIdx.x & 31;
+    // column sums of the warp's 32 rows, 16 columns at a time through the
+    // warp's scratch: lane = (column c, row half h)
+    const int lane = threadIdx.x & 31, c = lane & 15, h = lane >> 4;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = d[j];
-    __syncwarp();
-    float cs = 0.f;
+    for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) cs += wscr[r * 33 + lane];
-    if (col0 + lane < p.N && cs != 0.f) ptx::red_add_f32(p.dbO + col0 + lane, cs);
-    __syncwarp();
+      for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = d[half * 16 + j];
+      __syncwarp();
+      float cs = 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) cs += wscr[(h * 16 + r) * 17 + c];
+      cs += __shfl_xor_sync(0xffffffffu, cs, 16);
+      const int col = col0 + half * 16 + c;
+      if (h == 0 && col < p.N && cs != 0.f) ptx::red_add_f32(p.dbO + col, cs);
+      __syncwarp();
+    }
   }
 }
 
@@ -336,13 +346,15 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   unsigned char* sA = smem;
   unsigned char* sB = smem + STAGES * C::A_BYTES;
   float* scratch = (float*)(smem + STAGES * C::STAGE);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * C::STAGE + C::EPI_SCRATCH);
+  float* comb = (float*)(smem + STAGES * C::STAGE + C::EPI_SCRATCH);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * C::STAGE + C::EPI_SCRATCH + C::COMB_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
-  uint32_t* tmem_holder = (uint32_t*)(done_bar + 1);
+  uint64_t* comb_bar = done_bar + 1;  // [2]: the second half's LSE partials are in `comb`
+  uint32_t* tmem_holder = (uint32_t*)(comb_bar + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
   const int warp = ptx::warp_id(), lane = ptx::lane_id();
@@ -353,7 +365,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], 128);
+      ptx::mbar_init(&acc_empty[a], EPI_THREADS);
+      ptx::mbar_init(&comb_bar[a], 128);
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -466,14 +479,21 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sub = warp & 3;          // TMEM lane quarter of this warp
-    const int row = sub * 32 + lane;   // accumulator row owned by this thread
-    float* wscr = scratch + (warp - EPI_WARP0) * 32 * 33;
+    // Eight warps: warp w drains TMEM lane quarter (w & 3) and, of each
+    // accumulator's 32-column chunks, the even ones (first four warps) or the
+    // odd ones (last four).  The next chunk's tcgen05.ld is in flight while
+    // the current one is processed.
+    const int sub = warp & 3;                    // TMEM lane quarter of this warp
+    const int hf = (warp - EPI_WARP0) >> 2;      // which chunks: c % 2 == hf
+    const int row = sub * 32 + lane;             // accumulator row owned by this thread
+    float* wscr = scratch + (warp - EPI_WARP0) * 32 * 17;
+    constexpr int NCH = BN / 32;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
       const Unit w = unit_of(p, u);
       if (w.kb1 <= w.kb0) continue;
+      const int uidx = u / gridDim.x;   // this CTA's unit counter
       // per-unit state of the lattice epilogues
       TileRef tr{};
       RowCell rc{};
@@ -485,18 +505,23 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       }
       if (EPI == EPI_LSE) lse_init(ls, p, rc);
       if (EPI == EPI_DH) dh_init(ds, p, rc);
-      for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
-        if (!ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
+      bool ok = true;
+      for (int n = w.n0; n < w.n1; ++n) {
+        if (*abort_flag || !ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
           report_timeout(p, abort_flag);
+          ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(sub * 32) << 16);
+        float v[32], vn[32];
+        ptx::tmem_ld32(tbase + hf * 32, v);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(v);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          ptx::tmem_ld32(tbase + c * 32, v);
-          ptx::tmem_ld_wait();
+        for (int c = hf; c < NCH; c += 2) {
+          const bool more = c + 2 < NCH;
+          if (more) ptx::tmem_ld32(tbase + (c + 2) * 32, vn);
           const int col0 = n * BN + c * 32;
           if (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
             const long long grow = (long long)w.m * BM + row;
@@ -518,7 +543,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 }
               } else if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) ptx::red_add_v4(dst + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 32; j += 4)
+                  ptx::red_add_v4(dst + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
               } else {
                 for (int j = 0; j < 32 && col0 + j < p.N; ++j) ptx::red_add_f32(dst + j, v[j]);
               }
@@ -530,9 +556,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             dh_chunk(ds, p, rc, v, col0, p.Hout + ((long long)w.m * BM + row) * p.N + col0, wscr,
                      w.m < p.ch.ntiles);
           } else if (EPI == EPI_DA) {
-            // da = dz (1 - z^2) on the thread's own row, then transpose the
-            // warp's 32 rows x 32 columns through shared memory (lane =
-            // column) and sum over the tile's u (dA) and t (dLr).
+            // da = dz (1 - z^2) on the thread's own row, then 16-column halves
+            // of the warp's 32 x 32 block are transposed through the warp's
+            // scratch (lane = column c, row half h) and summed over the tile's
+            // u (into dA[b,t]) and t (into dLr[b,u]).
             float da[32];
             if (rc.valid && col0 + 32 <= p.N && (p.N & 7) == 0) {
               uint4 zq[4];
@@ -554,42 +581,87 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
               for (int j = 0; j < 32; ++j) da[j] = 0.f;
             }
+            const int cc = lane & 15, h = lane >> 4;
+            const int tw = tr.t0 + sub * 4;   // rows r of this warp: t = tw + r/8, u = u0 + r%8
 #pragma unroll
-            for (int j = 0; j < 32; ++j) wscr[lane * 33 + j] = da[j];
-            __syncwarp();
-            const int col = col0 + lane;
-            const int tw = tr.t0 + sub * 4;  // this warp's rows: t = tw + r/8, u = u0 + r%8
-            if (col < p.N && tr.exists && tw < tr.Tb) {
-              float sum_u[TU];
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-              for (int k = 0; k < TU; ++k) sum_u[k] = 0.f;
+              for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = da[half * 16 + j];
+              __syncwarp();
+              // this lane: column col0 + half*16 + cc, rows h*16 .. h*16+15
+              // (t = tw + 2h and tw + 2h + 1, u = u0 .. u0+7)
+              float sum_u[TU], st[2];
 #pragma unroll
-              for (int tq = 0; tq < 4; ++tq) {
-                float st = 0.f;
+              for (int q = 0; q < 2; ++q) {
+                st[q] = 0.f;
 #pragma unroll
                 for (int k = 0; k < TU; ++k) {
-                  const float x = wscr[(tq * TU + k) * 33 + lane];
-                  st += x;
-                  sum_u[k] += x;
+                  const float x = wscr[(h * 16 + q * TU + k) * 17 + cc];
+                  st[q] += x;
+                  sum_u[k] = (q == 0) ? x : sum_u[k] + x;
                 }
-                if (tw + tq < tr.Tb)
-                  ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + tw + tq) * p.N + col, st);
               }
 #pragma unroll
-              for (int k = 0; k < TU; ++k) {
-                if (tr.u0 + k <= tr.Ub)
-                  ptx::red_add_f32(p.dLr + ((size_t)tr.b * p.ch.sh.U1 + tr.u0 + k) * p.N + col,
-                                   sum_u[k]);
+              for (int k = 0; k < TU; ++k) sum_u[k] += __shfl_xor_sync(0xffffffffu, sum_u[k], 16);
+              const int col = col0 + half * 16 + cc;
+              if (col < p.N && tr.exists && tw < tr.Tb) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int t = tw + 2 * h + q;
+                  if (t < tr.Tb)
+                    ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + t) * p.N + col, st[q]);
+                }
+                // the two row halves split the 8 label positions: h=0 -> u0..u0+3
+#pragma unroll
+                for (int k = 0; k < TU / 2; ++k) {
+                  const int kk = h * (TU / 2) + k;
+                  const float x = h ? sum_u[TU / 2 + k] : sum_u[k];
+                  if (tr.u0 + kk <= tr.Ub)
+                    ptx::red_add_f32(p.dLr + ((size_t)tr.b * p.ch.sh.U1 + tr.u0 + kk) * p.N + col,
+                                     x);
+                }
               }
+              __syncwarp();
             }
-            __syncwarp();
+          }
+          if (more) {
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(vn);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = vn[j];
           }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&acc_empty[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      if (EPI == EPI_LSE && !*abort_flag) lse_finish(ls, p, rc);
+      if (EPI == EPI_LSE && ok) {
+        // combine the two column halves of each row: the second half hands
+        // its partial (max, sum, blank score, label score) to the first
+        float* cb = comb + (uidx & 1) * 128 * 4 + row * 4;
+        if (hf == 1) {
+          cb[0] = ls.run_max;
+          cb[1] = ls.run_sum;
+          cb[2] = ls.h_blank;
+          cb[3] = ls.h_lab;
+          ptx::mbar_arrive(&comb_bar[uidx & 1]);
+        } else if (ptx::mbar_wait(&comb_bar[uidx & 1], (uint32_t)(uidx >> 1) & 1u, WAIT_NS)) {
+          const float m1 = cb[0], s1 = cb[1];
+          const float nm = fmaxf(ls.run_max, m1);
+          float sum = 0.f;
+          if (ls.run_max != -INFINITY) sum += ls.run_sum * ptx::ex2((ls.run_max - nm) * kLog2e);
+          if (m1 != -INFINITY) sum += s1 * ptx::ex2((m1 - nm) * kLog2e);
+          ls.run_max = nm;
+          ls.run_sum = sum;
+          // each score column lives in exactly one half: take it from there
+          const int bchunk = (p.ch.sh.blank % BN) / 32;
+          if ((bchunk & 1) == 1) ls.h_blank = cb[2];
+          if (ls.lab >= 0 && (((ls.lab % BN) / 32) & 1) == 1) ls.h_lab = cb[3];
+          lse_finish(ls, p, rc);
+        } else {
+          report_timeout(p, abort_flag);
+        }
+      }
     }
   }
   ptx::tc_fence_before();

@@ -137,6 +137,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Make the compiler treat 32 registers as written here (after tcgen05.wait::ld),
+// so no use of a tcgen05.ld destination is scheduled before the wait.
+__device__ __forceinline__ void reg_fence32(float* v) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) asm volatile("" : "+f"(v[j])::"memory");
+}
 
 // ---- descriptors ----------------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle.  For a K-major operand

@@ -346,17 +346,27 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
   const int bf = p.dtype == RNNT_BF16;
   const bool untiled = p.mode == RNNT_UNTILED;
 
-  // Outputs are overwritten; accumulated ones start from zero.
-  if (dWO) LAUNCH("zero", launch_zero(dWO, sizeof(float) * (size_t)p.V * p.H, st));
-  if (dbO) LAUNCH("zero", launch_zero(dbO, sizeof(float) * (size_t)p.V, st));
-  if (dbZ) LAUNCH("zero", launch_zero(dbZ, sizeof(float) * (size_t)p.H, st));
+  // Outputs are overwritten; accumulated ones start from zero (one launch).
   if (p.B == 0) {
-    if (dWA) LAUNCH("zero", launch_zero(dWA, sizeof(float) * (size_t)p.H * p.HA, st));
-    if (dWL) LAUNCH("zero", launch_zero(dWL, sizeof(float) * (size_t)p.H * p.HL, st));
+    ZeroList z0{};
+    void* ps0[5] = {dWO, dbO, dbZ, dWA, dWL};
+    size_t bs0[5] = {sizeof(float) * (size_t)p.V * p.H, sizeof(float) * (size_t)p.V,
+                     sizeof(float) * (size_t)p.H, sizeof(float) * (size_t)p.H * p.HA,
+                     sizeof(float) * (size_t)p.H * p.HL};
+    for (int i = 0; i < 5; ++i) { z0.p[z0.n] = ps0[i]; z0.bytes[z0.n] = bs0[i]; ++z0.n; }
+    LAUNCH("zero", launch_zero_many(z0, st));
     return RNNT_OK;
   }
-  LAUNCH("zero", launch_zero(dA, sizeof(float) * (size_t)p.B * p.T * p.H, st));
-  LAUNCH("zero", launch_zero(dLr, sizeof(float) * (size_t)p.B * p.U1 * p.H, st));
+  {
+    ZeroList z{};
+    void* ps[7] = {dWO, dbO, dbZ, dA, dLr, dWA, dWL};
+    size_t bs[7] = {sizeof(float) * (size_t)p.V * p.H, sizeof(float) * (size_t)p.V,
+                    sizeof(float) * (size_t)p.H, sizeof(float) * (size_t)p.B * p.T * p.H,
+                    sizeof(float) * (size_t)p.B * p.U1 * p.H, sizeof(float) * (size_t)p.H * p.HA,
+                    sizeof(float) * (size_t)p.H * p.HL};
+    for (int i = 0; i < 7; ++i) { z.p[z.n] = ps[i]; z.bytes[z.n] = bs[i]; ++z.n; }
+    LAUNCH("zero", launch_zero_many(z, st));
+  }
   LAUNCH("eff_lengths", launch_eff_lengths(shape_of(p), sv, T_len, U_len, Teff, Ueff, st));
 
   rnnt_status s;

@@ -57,6 +57,36 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+__global__ void k_zero_many(ZeroList z) {
+  const int i = blockIdx.y;
+  unsigned char* p = (unsigned char*)z.p[i];
+  const size_t n16 = z.bytes[i] / 16;
+  size_t k = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; k < n16; k += stride) ((uint4*)p)[k] = make_uint4(0, 0, 0, 0);
+  if (blockIdx.x == 0 && threadIdx.x < z.bytes[i] % 16) p[n16 * 16 + threadIdx.x] = 0;
+}
+
+cudaError_t launch_zero_many(const ZeroList& z, cudaStream_t s) {
+  ZeroList c{};
+  size_t biggest = 0;
+  for (int i = 0; i < z.n && i < 8; ++i) {
+    if (!z.p[i] || !z.bytes[i]) continue;
+    if (((uintptr_t)z.p[i] & 15) != 0) {
+      cudaError_t e = launch_zero(z.p[i], z.bytes[i], s);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    c.p[c.n] = z.p[i];
+    c.bytes[c.n] = z.bytes[i];
+    biggest = biggest > z.bytes[i] ? biggest : z.bytes[i];
+    ++c.n;
+  }
+  if (c.n == 0) return cudaSuccess;
+  k_zero_many<<<dim3(grid_for(biggest / 16 + 1, 256), c.n), 256, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Validation + per-sample tile counts + exclusive prefix sum (one block).
 // A sample is rejected (0 tiles, loss NaN) when T_len is outside [1,T],
@@ -175,9 +205,9 @@ cudaError_t launch_eff_lengths(const Shape& sh, SavedView sv, const int32_t* T_l
 // diagonals ahead sit in a register ring.
 template <bool FAST>
 __device__ __forceinline__ float lae(float a, float b) {
+  // branch-free: when both are -inf, d = -inf and the result is m = -inf
   const float m = fmaxf(a, b);
-  if (m == -INFINITY) return -INFINITY;
-  const float d = -fabsf(a - b);
+  const float d = (m == -INFINITY) ? -INFINITY : fminf(a, b) - m;
   if (FAST) {
     // ln(1 + e^d) = ln2 * log2(1 + 2^(d log2 e))
     float e, l;
@@ -205,15 +235,17 @@ k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restr
   const int ndiag = Tb + Ub;
 
   float rb[PF][NJ], rl[PF][NJ];
+  // The ring holds raw loads from clamped (always valid) addresses; positions
+  // outside the lattice are masked where the values are used, so no
+  // instruction waits on a load before its diagonal comes up.
 #pragma unroll
   for (int k = 0; k < PF; ++k) {
     const int d = is_beta ? ndiag - 1 - k : k;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int u = lane + 32 * j, t = d - u;
-      const bool in = k < ndiag && u <= Ub && t >= 0 && t < Tb;
-      rb[k][j] = in ? LPB[(size_t)t * U1 + u] : -INFINITY;
-      rl[k][j] = in ? LPL[(size_t)t * U1 + u] : -INFINITY;
+      const int u = min(lane + 32 * j, Ub), t = min(max(d - (lane + 32 * j), 0), Tb - 1);
+      rb[k][j] = LPB[(size_t)t * U1 + u];
+      rl[k][j] = LPL[(size_t)t * U1 + u];
     }
   }
   float own[NJ], send[NJ];
@@ -245,15 +277,16 @@ k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restr
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
           const int u = lane + 32 * j, t = d - u;
-          const float lb = rb[k][j], ll = rl[k][j];
+          const bool in = u <= Ub && t >= 0 && t < Tb;
+          const float lb = in ? rb[k][j] : -INFINITY;
+          const float ll = in ? rl[k][j] : -INFINITY;
           {
-            const int t2 = d2 - u;
-            const bool in2 = s2 < ndiag && u <= Ub && t2 >= 0 && t2 < Tb;
-            rb[k][j] = in2 ? LPB[(size_t)t2 * U1 + u] : -INFINITY;
-            rl[k][j] = in2 ? LPL[(size_t)t2 * U1 + u] : -INFINITY;
+            const int uc = min(u, Ub), t2 = min(max(d2 - u, 0), Tb - 1);
+            rb[k][j] = LPB[(size_t)t2 * U1 + uc];
+            rl[k][j] = LPL[(size_t)t2 * U1 + uc];
           }
           float val = -INFINITY;
-          if (u <= Ub && t >= 0 && t < Tb) {
+          if (in) {
             if (!is_beta) {
               val = (s == 0) ? 0.f : lae<FAST>(own[j], nb[j]);
             } else {

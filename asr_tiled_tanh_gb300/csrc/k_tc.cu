@@ -45,6 +45,12 @@ constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
 
 enum { EPI_STORE = 0, EPI_ATOMIC = 1, EPI_LSE = 2, EPI_DH = 3, EPI_DA = 4 };
 
+// Per-epilogue-warp shared scratch: either 32 rows x 16 fp32 (+1 pad) for
+// column transposes, or 32 rows x 32 bf16 at an 80-byte pitch for staging
+// row chunks so that global accesses cover 8 rows x 64 B per instruction.
+constexpr int WSCR_BYTES = 2560;
+constexpr int STAGE_PITCH = 80;
+
 struct TcParams {
   int M, N, K;
   int m_tiles, n_tiles, k_splits, kb_total, kb_per_split;
@@ -68,7 +74,7 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int EPI_SCRATCH = 8 * 32 * 17 * 4;   // per epilogue warp: 32 rows x 16 cols
+  static constexpr int EPI_SCRATCH = 8 * WSCR_BYTES;     // per epilogue warp staging area
   static constexpr int COMB_BYTES = 2 * 128 * 4 * 4;     // LSE halves, double-buffered
   static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_RAW =
@@ -137,31 +143,22 @@ __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
 }
 
-// 32 bias values of columns col0.. (0 beyond N or without a bias).
-__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int N, int col0,
-                                            float* bb) {
-  if (!bias) {
+// 32 bias values of columns col0.. as packed bf16 (0 beyond N or without a
+// bias); widened with unpack32 where they are used.
+__device__ __forceinline__ void load_bias_q(const __nv_bfloat16* bias, int N, int col0,
+                                            uint4* q) {
+  if (bias && col0 + 32 <= N && (N & 7) == 0) {
+    const uint4* src = (const uint4*)(bias + col0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) bb[j] = 0.f;
+    for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
     return;
   }
-  if (col0 + 32 <= N && (N & 7) == 0) {
-    const uint4* q = (const uint4*)(bias + col0);
+  __nv_bfloat16 h[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 w = __ldg(q + i);
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  for (int j = 0; j < 32; ++j)
+    h[j] = (bias && col0 + j < N) ? bias[col0 + j] : __float2bfloat16_rn(0.f);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __nv_bfloat162 h2 = *(const __nv_bfloat162*)&u[k];
-        bb[i * 8 + 2 * k] = __low2float(h2);
-        bb[i * 8 + 2 * k + 1] = __high2float(h2);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) bb[j] = (col0 + j < N) ? bf(bias, col0 + j) : 0.f;
-  }
+  for (int i = 0; i < 4; ++i) q[i] = *(const uint4*)(h + 8 * i);
 }
 
 // 32 bf16 values at p (16-byte aligned) widened to fp32.
@@ -176,6 +173,60 @@ __device__ __forceinline__ void unpack32(const uint4* q, float* out) {
       out[i * 8 + 2 * k + 1] = __high2float(h2);
     }
   }
+}
+
+// The warp's 32 rows x 32 bf16 columns (lane = row, q = its 64 bytes) written
+// to global memory at rows base_row .. +31, columns col0 .. +31 (ld elements
+// per row), through the warp's staging area: each store instruction then
+// covers 8 consecutive rows' 64-byte pieces instead of 32 scattered rows.
+__device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4* q,
+                                                __nv_bfloat16* gbase, long long ld,
+                                                bool row_ok_mask_all) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * STAGE_PITCH + i * 16) = q[i];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), piece = lane & 3;
+    const uint4 x = *(const uint4*)(stg + r * STAGE_PITCH + piece * 16);
+    if (row_ok_mask_all) *(uint4*)(gbase + (long long)r * ld + piece * 8) = x;
+  }
+  __syncwarp();
+}
+
+// The reverse: each lane gets its own row's 32 bf16 (64 bytes) of rows
+// base_row .. +31, loaded with 8 rows per instruction and redistributed
+// through the staging area.
+__device__ __forceinline__ void load_rows_bf16(unsigned char* stg, const __nv_bfloat16* gbase,
+                                               long long ld, uint4* q) {
+  const int lane = threadIdx.x & 31;
+  uint4 x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), piece = lane & 3;
+    x[i] = __ldg((const uint4*)(gbase + (long long)r * ld + piece * 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), piece = lane & 3;
+    *(uint4*)(stg + r * STAGE_PITCH + piece * 16) = x[i];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = *(const uint4*)(stg + lane * STAGE_PITCH + i * 16);
+  __syncwarp();
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* d) {
+  __nv_bfloat162 q0 = __floats2bfloat162_rn(d[0], d[1]);
+  __nv_bfloat162 q1 = __floats2bfloat162_rn(d[2], d[3]);
+  __nv_bfloat162 q2 = __floats2bfloat162_rn(d[4], d[5]);
+  __nv_bfloat162 q3 = __floats2bfloat162_rn(d[6], d[7]);
+  uint4 pk;
+  pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
+  pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
+  return pk;
 }
 
 // Select v[j] for a runtime j in [0,32) without local memory.
@@ -207,11 +258,10 @@ __device__ __forceinline__ void lse_init(LseState& st, const TcParams& p, const 
 // 32 scores v[] (accumulator values, bias not yet added) of columns col0.. .
 // keep: where to store the scores (untiled mode), or NULL.
 __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const RowCell& rc,
-                                          float* v, int col0, __nv_bfloat16* keep) {
+                                          float* v, const float* bb, int col0,
+                                          __nv_bfloat16* keep) {
   if (!rc.valid) return;
   const int nv = min(32, p.N - col0);
-  float bb[32];
-  load_bias32(p.bias, p.N, col0, bb);
   float cm = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -275,50 +325,33 @@ __device__ __forceinline__ void dh_init(DhState& st, const TcParams& p, const Ro
   st.lab = (rc.u < rc.Ub) ? p.ch.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
 }
 
-// dh of 32 columns written as bf16 to dst (0 for positions outside the
-// lattice); when dbO is given, the warp's 32 rows are also summed per column
-// (through the warp's shared-memory scratch) and added to dbO.
+// dh of 32 columns; the warp's 32 rows are written as bf16 to rows
+// wrow0 .. +31 of the dh buffer (0 for positions outside the lattice); when
+// dbO is given, the rows are also summed per column through the warp's
+// scratch and added to dbO.  bb: the 32 bias values.  All lanes take part.
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
-                                         const float* v, int col0, __nv_bfloat16* dst,
-                                         float* wscr, bool write) {
+                                         const float* v, const float* bb, int col0,
+                                         long long wrow0, float* wscr, bool write) {
   const int nv = min(32, p.N - col0);
   float d[32];
   if (rc.valid) {
-    float bb[32];
-    load_bias32(p.bias, p.N, col0, bb);
     const float nl = st.lnPD * kLog2e;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       float x = st.gam * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -nl));
       if (col0 + j == p.ch.sh.blank) x -= st.pb;
       if (col0 + j == st.lab) x -= st.pl;
-      d[j] = st.g * x;
+      d[j] = (j < nv) ? st.g * x : 0.f;
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j) d[j] = 0.f;
   }
-  if (write) {
-    if (nv == 32 && (p.N & 7) == 0) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        __nv_bfloat162 q0 = __floats2bfloat162_rn(d[j], d[j + 1]);
-        __nv_bfloat162 q1 = __floats2bfloat162_rn(d[j + 2], d[j + 3]);
-        __nv_bfloat162 q2 = __floats2bfloat162_rn(d[j + 4], d[j + 5]);
-        __nv_bfloat162 q3 = __floats2bfloat162_rn(d[j + 6], d[j + 7]);
-        uint4 pk;
-        pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
-        pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
-        *(uint4*)(dst + j) = pk;
-      }
-    } else {
-      for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
-    }
-  }
+  const int lane = threadIdx.x & 31;
   if (p.dbO) {
     // column sums of the warp's 32 rows, 16 columns at a time through the
     // warp's scratch: lane = (column c, row half h)
-    const int lane = threadIdx.x & 31, c = lane & 15, h = lane >> 4;
+    const int c = lane & 15, h = lane >> 4;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -331,6 +364,18 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       const int col = col0 + half * 16 + c;
       if (h == 0 && col < p.N && cs != 0.f) ptx::red_add_f32(p.dbO + col, cs);
       __syncwarp();
+    }
+  }
+  if (write) {
+    __nv_bfloat16* gbase = p.Hout + wrow0 * p.N + col0;
+    if (nv == 32 && (p.N & 7) == 0) {
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = pack8_bf16(d + 8 * i);
+      store_rows_bf16((unsigned char*)wscr, q, gbase, p.N, true);
+    } else {
+      __nv_bfloat16* dst = gbase + (long long)lane * p.N;
+      for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
     }
   }
 }
@@ -486,7 +531,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const int sub = warp & 3;                    // TMEM lane quarter of this warp
     const int hf = (warp - EPI_WARP0) >> 2;      // which chunks: c % 2 == hf
     const int row = sub * 32 + lane;             // accumulator row owned by this thread
-    float* wscr = scratch + (warp - EPI_WARP0) * 32 * 17;
+    float* wscr = (float*)((unsigned char*)scratch + (warp - EPI_WARP0) * WSCR_BYTES);
     constexpr int NCH = BN / 32;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -516,6 +561,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(sub * 32) << 16);
         float v[32], vn[32];
         ptx::tmem_ld32(tbase + hf * 32, v);
+        // bias values of the current chunk; the next chunk's are loaded early
+        constexpr bool USE_BIAS = (EPI == EPI_STORE || EPI == EPI_LSE || EPI == EPI_DH);
+        uint4 bq[4];
+        if (USE_BIAS) load_bias_q(p.bias, p.N, n * BN + hf * 32, bq);
         ptx::tmem_ld_wait();
         ptx::reg_fence32(v);
 #pragma unroll 1
@@ -523,17 +572,17 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           const bool more = c + 2 < NCH;
           if (more) ptx::tmem_ld32(tbase + (c + 2) * 32, vn);
           const int col0 = n * BN + c * 32;
+          uint4 bqn[4];
+          if (USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
+          float bb[32];
+          if (USE_BIAS) unpack32(bq, bb);
           if (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
             const long long grow = (long long)w.m * BM + row;
             if (grow < p.M && col0 < p.N) {
               float* dst = p.C + grow * p.ldc + col0;
               if (EPI == EPI_STORE) {
-                if (p.bias) {
-                  float bb[32];
-                  load_bias32(p.bias, p.N, col0, bb);
 #pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] += bb[j];
-                }
+                for (int j = 0; j < 32; ++j) v[j] += bb[j];
                 if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
                   for (int j = 0; j < 32; j += 4)
@@ -550,10 +599,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               }
             }
           } else if (EPI == EPI_LSE) {
-            lse_chunk(ls, p, rc, v, col0,
+            lse_chunk(ls, p, rc, v, bb, col0,
                       p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
           } else if (EPI == EPI_DH) {
-            dh_chunk(ds, p, rc, v, col0, p.Hout + ((long long)w.m * BM + row) * p.N + col0, wscr,
+            dh_chunk(ds, p, rc, v, bb, col0, (long long)w.m * BM + sub * 32, wscr,
                      w.m < p.ch.ntiles);
           } else if (EPI == EPI_DA) {
             // da = dz (1 - z^2) on the thread's own row, then 16-column halves
@@ -561,15 +610,14 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // scratch (lane = column c, row half h) and summed over the tile's
             // u (into dA[b,t]) and t (into dLr[b,u]).
             float da[32];
-            if (rc.valid && col0 + 32 <= p.N && (p.N & 7) == 0) {
+            if (tr.exists && col0 + 32 <= p.N && (p.N & 7) == 0) {
               uint4 zq[4];
-              const uint4* zp = (const uint4*)(p.Zin + ((long long)w.m * BM + row) * p.N + col0);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) zq[i] = __ldg(zp + i);
+              load_rows_bf16((unsigned char*)wscr,
+                             p.Zin + ((long long)w.m * BM + sub * 32) * p.N + col0, p.N, zq);
               float z[32];
               unpack32(zq, z);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) da[j] = v[j] * (1.f - z[j] * z[j]);
+              for (int j = 0; j < 32; ++j) da[j] = rc.valid ? v[j] * (1.f - z[j] * z[j]) : 0.f;
             } else if (rc.valid) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
@@ -629,6 +677,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             ptx::reg_fence32(vn);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = vn[j];
+            if (USE_BIAS) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) bq[i] = bqn[i];
+            }
           }
         }
         ptx::tc_fence_before();
@@ -699,10 +751,12 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
       const float4* a = (const float4*)(pA + ((size_t)rc.b * c.sh.T + rc.t) * H + k8);
       const float4* l = (const float4*)(pL + ((size_t)rc.b * c.sh.U1 + rc.u) * H + k8);
       const float4 a0 = a[0], a1 = a[1], l0 = l[0], l1 = l[1];
-      __nv_bfloat162 q0 = __floats2bfloat162_rn(tanhf(a0.x + l0.x), tanhf(a0.y + l0.y));
-      __nv_bfloat162 q1 = __floats2bfloat162_rn(tanhf(a0.z + l0.z), tanhf(a0.w + l0.w));
-      __nv_bfloat162 q2 = __floats2bfloat162_rn(tanhf(a1.x + l1.x), tanhf(a1.y + l1.y));
-      __nv_bfloat162 q3 = __floats2bfloat162_rn(tanhf(a1.z + l1.z), tanhf(a1.w + l1.w));
+      // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
+      using ptx::tanh_approx;
+      __nv_bfloat162 q0 = __floats2bfloat162_rn(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
+      __nv_bfloat162 q1 = __floats2bfloat162_rn(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
+      __nv_bfloat162 q2 = __floats2bfloat162_rn(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
+      __nv_bfloat162 q3 = __floats2bfloat162_rn(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
       out.x = *(uint32_t*)&q0; out.y = *(uint32_t*)&q1;
       out.z = *(uint32_t*)&q2; out.w = *(uint32_t*)&q3;
     }
@@ -868,22 +922,37 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
 
 template <int EPI>
 cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, cudaStream_t s) {
-  const int code = (bn == 256 ? 4 : 0) | (g.a_mn ? 2 : 0) | (g.b_mn ? 1 : 0);
-  switch (code) {
-    case 0: return launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
-    case 1: return launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
-    case 2: return launch_gemm_t<128, 1, 0, EPI>(g, p, 0, s);
-    case 3: return launch_gemm_t<128, 1, 1, EPI>(g, p, 0, s);
-    case 4: return launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s);
-    case 5: return launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s);
-    case 6: return launch_gemm_t<256, 1, 0, EPI>(g, p, 0, s);
-    default: return launch_gemm_t<256, 1, 1, EPI>(g, p, 0, s);
+  // Only the operand layouts each epilogue is used with are instantiated:
+  // the lattice epilogues take K-major scores/z (and an MN-major W^O for dz);
+  // the plain store and atomic epilogues take every layout.
+  if constexpr (EPI == EPI_LSE || EPI == EPI_DH) {
+    if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
+    return bn == 256 ? launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s)
+                     : launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
+  } else if constexpr (EPI == EPI_DA) {
+    if (g.a_mn || !g.b_mn) return cudaErrorInvalidValue;
+    return bn == 256 ? launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s)
+                     : launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
+  } else {
+    const int code = (bn == 256 ? 4 : 0) | (g.a_mn ? 2 : 0) | (g.b_mn ? 1 : 0);
+    switch (code) {
+      case 0: return launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
+      case 1: return launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
+      case 2: return launch_gemm_t<128, 1, 0, EPI>(g, p, 0, s);
+      case 3: return launch_gemm_t<128, 1, 1, EPI>(g, p, 0, s);
+      case 4: return launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s);
+      case 5: return launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s);
+      case 6: return launch_gemm_t<256, 1, 0, EPI>(g, p, 0, s);
+      default: return launch_gemm_t<256, 1, 1, EPI>(g, p, 0, s);
+    }
   }
 }
 
-int pick_bn(int N) {
-  // the tile width that wastes the fewest MMA columns (ties: the wider one)
+int pick_bn(int N, long long M = 1LL << 40) {
+  // the tile width that wastes the fewest MMA columns (ties: the wider one),
+  // unless 256-wide tiles leave more than half of the SMs without a tile
   const long long w256 = cdiv(N, 256) * 256, w128 = cdiv(N, 128) * 128;
+  if (cdiv(M, BM) * cdiv(N, 256) < num_sms() / 2) return 128;
   return w256 <= w128 ? 256 : 128;
 }
 
@@ -923,7 +992,7 @@ cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const voi
   tp.C = out;
   tp.ldc = p.H;
   tp.bias = (const __nv_bfloat16*)bias;
-  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H), s);
+  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), s);
 }
 
 namespace {
@@ -1032,7 +1101,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.dA = dA;
       tp.dLr = dLr;
       tp.status = sv.status;
-      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H), s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
     if (dWO) {  // dW^O += dh^T z, split over the chunk's rows
       ProfScope ps("tc_bwd_dwo", s);
@@ -1089,17 +1158,16 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     TcParams tp{};
     tp.C = dhA;
     tp.ldc = p.HA;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA), s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dhL) {
     GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
     TcParams tp{};
     tp.C = dhL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL), s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dWA) {  // dW^A = dA^T hA: A = dA16 as [K=MA][M=H], B = hAm as [K=MA][N=HA]
-    if (launch_zero(dWA, sizeof(float) * (size_t)p.H * p.HA, s) != cudaSuccess) return RNNT_ERR_CUDA;
     GemmDesc g{dA16, 1, hAm, 1, p.H, p.HA, MA};
     TcParams tp{};
     const int bn = pick_bn(p.HA);
@@ -1109,7 +1177,6 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dWL) {
-    if (launch_zero(dWL, sizeof(float) * (size_t)p.H * p.HL, s) != cudaSuccess) return RNNT_ERR_CUDA;
     GemmDesc g{dLr16, 1, hLm, 1, p.H, p.HL, ML};
     TcParams tp{};
     const int bn = pick_bn(p.HL);

@@ -7,6 +7,13 @@ namespace rnnt {
 // ---- lattice bookkeeping and the loss recursion (k_lattice.cu) -----------
 cudaError_t launch_fill_f32(float* p, float v, size_t n, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
+// Zero up to 8 buffers (16-byte aligned pointers) in one launch; NULL entries are skipped.
+struct ZeroList {
+  void* p[8];
+  size_t bytes[8];
+  int n;
+};
+cudaError_t launch_zero_many(const ZeroList& z, cudaStream_t s);
 // Validate lengths/labels, build the per-sample tile prefix sum, reset the
 // status word, mark rejected samples (loss = lnP = NaN).
 cudaError_t launch_index(const Shape& sh, const int32_t* labels, const int32_t* T_len,

@@ -20,22 +20,23 @@ def to_device(inp: synthetic.Inputs, device="cuda"):
 
 
 def run_gpu(inp: synthetic.Inputs, mode="tiled", tile_cells=0, grad_loss=None, dev=None,
-            want_grad=True):
+            want_grad=True, keep_saved=True):
     """Forward (+ backward) through the C ABI; returns host numpy arrays."""
     dev = dev if dev is not None else to_device(inp)
     r = rn.Rnnt.for_inputs(inp, mode=mode, tile_cells=tile_cells)
     params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
     loss = r.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
-    sa = r.saved_arrays()
-    out = dict(loss=loss.double().cpu().numpy(),
-               **{k: getattr(sa, k).double().cpu().numpy() for k in ("lnP", "lpb", "lpl", "lnPD",
-                                                                      "alpha", "beta")})
+    out = dict(loss=loss.double().cpu().numpy())
+    if keep_saved:
+        sa = r.saved_arrays()
+        out.update({k: getattr(sa, k).double().cpu().numpy()
+                    for k in ("lnP", "lpb", "lpl", "lnPD", "alpha", "beta")})
     if want_grad:
         g = None if grad_loss is None else torch.as_tensor(grad_loss, dtype=torch.float32,
                                                            device="cuda")
         grads = r.bwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"],
                       grad_loss=g)
-        out.update({k: v.double().cpu().numpy() for k, v in grads.items()})
+        out.update({k: v.cpu().numpy() for k, v in grads.items()})
     code, word = r.status()
     out["status"] = (code, word)
     torch.cuda.synchronize()

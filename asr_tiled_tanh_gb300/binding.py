@@ -98,7 +98,7 @@ def load(build_if_missing: bool = False):
     lib.rnnt_testing_gemm_bf16.restype = ctypes.c_int
     lib.rnnt_testing_gemm_bf16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                            ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
-                                           ctypes.c_int, ctypes.c_int, P]
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
     _lib = lib
     return lib
 
@@ -204,10 +204,11 @@ def rnnt_profile_stop() -> dict:
 
 
 def rnnt_testing_gemm_bf16(A, a_mn, B, b_mn, C, M, N, K, accumulate=0, k_splits=1, bn=256,
-                           stream=None):
+                           cluster=1, stream=None):
     """The library's tcgen05 GEMM alone (include/rnnt_testing.h)."""
     _check(load().rnnt_testing_gemm_bf16(M, N, K, _p(A), a_mn, _p(B), b_mn, _p(C), accumulate,
-                                         k_splits, bn, _stream(stream)), "rnnt_testing_gemm_bf16")
+                                         k_splits, bn, cluster, _stream(stream)),
+           "rnnt_testing_gemm_bf16")
 
 
 # --- convenience: buffers owned by torch -------------------------------------

@@ -54,7 +54,8 @@ constexpr int STAGE_PITCH = 80;
 struct TcParams {
   int M, N, K;
   int m_tiles, n_tiles, k_splits, kb_total, kb_per_split;
-  int units;
+  int units;             // including the padding units of a ragged last cluster group
+  int m_groups;          // M tiles in groups of the cluster size
   int row_complete;      // a unit is one M tile with all of its N tiles, in order
   float* C;              // STORE / ATOMIC output, row-major with ldc
   long long ldc;
@@ -88,15 +89,23 @@ struct Unit {
   int m, n0, n1, kb0, kb1;  // M tile, N tiles [n0,n1), K blocks [kb0,kb1)
 };
 
+// Unit u of a cluster of CL CTAs: consecutive units differ only in M (by the
+// CTA's rank in the cluster), so the CTAs of a cluster always need the same
+// B tiles at the same time.  M tiles past the matrix are padding: their A
+// loads are zero-filled and their epilogues write nothing.
+template <int CL>
 __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
   Unit w;
+  const int r = u % CL;
+  int rest = u / CL;
   if (p.row_complete) {
-    w.m = u; w.n0 = 0; w.n1 = p.n_tiles; w.kb0 = 0; w.kb1 = p.kb_total;
+    w.m = rest * CL + r; w.n0 = 0; w.n1 = p.n_tiles; w.kb0 = 0; w.kb1 = p.kb_total;
   } else {
-    const int ks = u % p.k_splits;
-    const int rest = u / p.k_splits;
+    const int ks = rest % p.k_splits;
+    rest /= p.k_splits;
     const int n = rest % p.n_tiles;
-    w.m = rest / p.n_tiles;
+    const int mg = rest / p.n_tiles;
+    w.m = mg * CL + r;
     w.n0 = n; w.n1 = n + 1;
     w.kb0 = ks * p.kb_per_split;
     w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
@@ -380,11 +389,17 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   }
 }
 
-template <int BN, int A_MN, int B_MN, int EPI>
+template <int BN, int A_MN, int B_MN, int EPI, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const TcParams p) {
   using C = Cfg<BN>;
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+  static_assert(!B_MN || BN / 64 >= CL, "each CTA of a cluster loads whole 64-column B boxes");
+  // CTAs of a cluster share each B stage: CTA r loads slice r and multicasts it
+  const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0;
+  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
+  const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
   constexpr int STAGES = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -406,7 +421,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], CL);  // released by the MMAs of every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
@@ -427,6 +442,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CL > 1) ptx::cluster_sync();  // peers' barriers are initialised before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -436,8 +452,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       int stage = 0;
       uint32_t phase = 0;
       int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
-      for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+      for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -454,12 +470,24 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               ptx::tma_load_2d(a, &tmA, &full[stage], w.m * BM, kb * BK);
               ptx::tma_load_2d(a + 64 * 128, &tmA, &full[stage], w.m * BM + 64, kb * BK);
             }
-            if (!B_MN) {
-              ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
+            if (CL == 1) {
+              if (!B_MN) {
+                ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                  ptx::tma_load_2d(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j, kb * BK);
+              }
+            } else if (!B_MN) {
+              // rows [crank * BN/CL, +BN/CL) of the B tile, to every CTA of the cluster
+              ptx::tma_load_2d_mc(b + crank * (BN / CL) * 128, &tmB, &full[stage], kb * BK,
+                                  n * BN + (int)crank * (BN / CL), kMask);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
-                ptx::tma_load_2d(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j, kb * BK);
+                if (j % CL == (int)crank)
+                  ptx::tma_load_2d_mc(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j,
+                                      kb * BK, kMask);
             }
             issued[stage] = (int)phase;
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -480,8 +508,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
-        const Unit w = unit_of(p, u);
+      for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, WAIT_NS)) {
@@ -510,7 +538,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                                        : ptx::sdesc_sw128(b0 + k * 32, 16, 1024);
               ptx::mma_bf16(d_tmem, ad, bd, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(&empty[stage]);
+            if (CL == 1) ptx::mma_commit(&empty[stage]);
+            else ptx::mma_commit_mc(&empty[stage], kMask);
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
@@ -535,10 +564,10 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     constexpr int NCH = BN / 32;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
-      const Unit w = unit_of(p, u);
+    for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
+      const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
       if (w.kb1 <= w.kb0) continue;
-      const int uidx = u / gridDim.x;   // this CTA's unit counter
+      const int uidx = gi / n_clusters;   // this CTA's unit counter
       // per-unit state of the lattice epilogues
       TileRef tr{};
       RowCell rc{};
@@ -718,6 +747,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CL > 1) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
@@ -892,58 +922,117 @@ struct GemmDesc {
   int M, N, K;
 };
 
-template <int BN, int AMN, int BMN, int EPI>
+template <int BN, int AMN, int BMN, int EPI, int CL>
 cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStream_t s) {
   using C = Cfg<BN>;
+  auto kern = k_tc_gemm<BN, AMN, BMN, EPI, CL>;
   CUtensorMap ta, tb;
   const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64) : make_tmap(&ta, g.A, g.M, g.K, BM);
-  const bool ok_b = BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN);
+  const bool ok_b =
+      BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN / CL);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<BN, AMN, BMN, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static int max_clusters = -1;  // per instantiation
+  if (max_clusters < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    max_clusters = num_sms();
+    if (CL > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CL;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(CL * 64);
+      cfg.blockDim = dim3(NTHREADS);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+        n = num_sms() / CL;
+      max_clusters = n;
+    }
   }
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.m_tiles = (int)cdiv(g.M, BM);
+  p.m_groups = (int)cdiv(p.m_tiles, CL);
   p.n_tiles = (int)cdiv(g.N, BN);
   p.kb_total = (int)cdiv(g.K, BK);
   if (p.k_splits < 1) p.k_splits = 1;
   p.kb_per_split = (int)cdiv(p.kb_total, p.k_splits);
   p.k_splits = (int)cdiv(p.kb_total, p.kb_per_split);
-  p.units = p.row_complete ? p.m_tiles : p.m_tiles * p.n_tiles * p.k_splits;
-  if (p.units <= 0 || g.K <= 0) return cudaSuccess;
-  const int grid = std::min(p.units, max_units > 0 ? max_units : num_sms());
-  k_tc_gemm<BN, AMN, BMN, EPI><<<grid, NTHREADS, C::SMEM, s>>>(ta, tb, p);
-  return cudaGetLastError();
+  const int groups = p.row_complete ? p.m_groups : p.m_groups * p.n_tiles * p.k_splits;
+  p.units = groups * CL;
+  if (groups <= 0 || g.K <= 0) return cudaSuccess;
+  const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
+  const int grid_groups = std::min(groups, cap);
+  if (CL == 1) {
+    kern<<<grid_groups, NTHREADS, C::SMEM, s>>>(ta, tb, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid_groups * CL);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
+// Cluster size used for a GEMM: CTAs of a cluster share B tiles over TMA
+// multicast.  Needs at least CL M tiles (padding units cover the rest).
+
 template <int EPI>
-cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, cudaStream_t s) {
-  // Only the operand layouts each epilogue is used with are instantiated:
-  // the lattice epilogues take K-major scores/z (and an MN-major W^O for dz);
-  // the plain store and atomic epilogues take every layout.
+cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, int cl, cudaStream_t s) {
+  // Only the operand layouts / cluster sizes each epilogue is used with are
+  // instantiated: the lattice epilogues take K-major scores/z (and an
+  // MN-major W^O for dz); the store and atomic epilogues take every layout.
+  if (g.M <= BM) cl = 1;
   if constexpr (EPI == EPI_LSE || EPI == EPI_DH) {
     if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
-    return bn == 256 ? launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s)
-                     : launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
+    if (bn == 256) {
+      if (cl >= 4) return launch_gemm_t<256, 0, 0, EPI, 4>(g, p, 0, s);
+      if (cl == 2) return launch_gemm_t<256, 0, 0, EPI, 2>(g, p, 0, s);
+      return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
+    }
+    return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
   } else if constexpr (EPI == EPI_DA) {
     if (g.a_mn || !g.b_mn) return cudaErrorInvalidValue;
-    return bn == 256 ? launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s)
-                     : launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
+    if (bn == 256) {
+      if (cl >= 4) return launch_gemm_t<256, 0, 1, EPI, 4>(g, p, 0, s);
+      if (cl == 2) return launch_gemm_t<256, 0, 1, EPI, 2>(g, p, 0, s);
+      return launch_gemm_t<256, 0, 1, EPI, 1>(g, p, 0, s);
+    }
+    if (cl >= 2) return launch_gemm_t<128, 0, 1, EPI, 2>(g, p, 0, s);
+    return launch_gemm_t<128, 0, 1, EPI, 1>(g, p, 0, s);
   } else {
+    if (EPI == EPI_ATOMIC && g.a_mn && g.b_mn && cl > 1) {
+      if (bn == 256) {
+        if (cl >= 4) return launch_gemm_t<256, 1, 1, EPI, 4>(g, p, 0, s);
+        return launch_gemm_t<256, 1, 1, EPI, 2>(g, p, 0, s);
+      }
+      return launch_gemm_t<128, 1, 1, EPI, 2>(g, p, 0, s);
+    }
+    if (EPI == EPI_STORE && !g.a_mn && !g.b_mn && cl > 1 && bn == 256)
+      return launch_gemm_t<256, 0, 0, EPI, 2>(g, p, 0, s);
     const int code = (bn == 256 ? 4 : 0) | (g.a_mn ? 2 : 0) | (g.b_mn ? 1 : 0);
     switch (code) {
-      case 0: return launch_gemm_t<128, 0, 0, EPI>(g, p, 0, s);
-      case 1: return launch_gemm_t<128, 0, 1, EPI>(g, p, 0, s);
-      case 2: return launch_gemm_t<128, 1, 0, EPI>(g, p, 0, s);
-      case 3: return launch_gemm_t<128, 1, 1, EPI>(g, p, 0, s);
-      case 4: return launch_gemm_t<256, 0, 0, EPI>(g, p, 0, s);
-      case 5: return launch_gemm_t<256, 0, 1, EPI>(g, p, 0, s);
-      case 6: return launch_gemm_t<256, 1, 0, EPI>(g, p, 0, s);
-      default: return launch_gemm_t<256, 1, 1, EPI>(g, p, 0, s);
+      case 0: return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
+      case 1: return launch_gemm_t<128, 0, 1, EPI, 1>(g, p, 0, s);
+      case 2: return launch_gemm_t<128, 1, 0, EPI, 1>(g, p, 0, s);
+      case 3: return launch_gemm_t<128, 1, 1, EPI, 1>(g, p, 0, s);
+      case 4: return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
+      case 5: return launch_gemm_t<256, 0, 1, EPI, 1>(g, p, 0, s);
+      case 6: return launch_gemm_t<256, 1, 0, EPI, 1>(g, p, 0, s);
+      default: return launch_gemm_t<256, 1, 1, EPI, 1>(g, p, 0, s);
     }
   }
 }
@@ -963,6 +1052,9 @@ int pick_splits(int units_mn, int K) {
   want = std::min(want, std::max(1, kb / 8));
   return std::max(1, want);
 }
+
+// Cluster size of the lattice GEMMs (scores, dh, dz, dW^O).
+constexpr int kClusterLattice = 2;
 
 #define TC_CHECK(expr)                                   \
   do {                                                   \
@@ -992,7 +1084,7 @@ cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const voi
   tp.C = out;
   tp.ldc = p.H;
   tp.bias = (const __nv_bfloat16*)bias;
-  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), s);
+  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), 1, s);
 }
 
 namespace {
@@ -1051,7 +1143,7 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     tp.ch = c;
     tp.Hout = (__nv_bfloat16*)Hkeep;
     tp.status = sv.status;
-    if (launch_gemm<EPI_LSE>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_LSE>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   return RNNT_OK;
 }
@@ -1086,7 +1178,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.Hout = Hs;
       tp.dbO = dbO;
       tp.status = sv.status;
-      if (launch_gemm<EPI_DH>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
       ProfScope ps("tc_dh_kept", s);
       k_dh_rows_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, Hs, grad_loss);
@@ -1101,7 +1193,8 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.dA = dA;
       tp.dLr = dLr;
       tp.status = sv.status;
-      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), kClusterLattice, s) != cudaSuccess)
+        return RNNT_ERR_CUDA;
     }
     if (dWO) {  // dW^O += dh^T z, split over the chunk's rows
       ProfScope ps("tc_bwd_dwo", s);
@@ -1112,7 +1205,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.C = dWO;
       tp.ldc = p.H;
       tp.status = sv.status;
-      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
     if (dbO && untiled) {  // the tiled path sums dh inside the dh epilogue
       ProfScope ps("tc_colsum_dh", s);
@@ -1158,14 +1251,14 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     TcParams tp{};
     tp.C = dhA;
     tp.ldc = p.HA;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), 1, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dhL) {
     GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
     TcParams tp{};
     tp.C = dhL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), 1, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dWA) {  // dW^A = dA^T hA: A = dA16 as [K=MA][M=H], B = hAm as [K=MA][N=HA]
     GemmDesc g{dA16, 1, hAm, 1, p.H, p.HA, MA};
@@ -1174,7 +1267,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HA, bn)), MA);
     tp.C = dWA;
     tp.ldc = p.HA;
-    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dWL) {
     GemmDesc g{dLr16, 1, hLm, 1, p.H, p.HL, ML};
@@ -1183,7 +1276,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HL, bn)), ML);
     tp.C = dWL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dbZ) {
     if (launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, s) != cudaSuccess)
@@ -1198,11 +1291,12 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
 // Test hook (include/rnnt_testing.h): one raw GEMM through the same kernel.
 extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A, int a_mn,
                                               const void* B, int b_mn, float* C, int accumulate,
-                                              int k_splits, int bn, void* stream) {
+                                              int k_splits, int bn, int cluster, void* stream) {
   using namespace rnnt;
   if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C) return RNNT_ERR_INVALID_ARG;
   if ((a_mn ? M : K) % 8 || (b_mn ? N : K) % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
   if (bn != 128 && bn != 256) return RNNT_ERR_INVALID_ARG;
+  if (cluster != 1 && cluster != 2 && cluster != 4) return RNNT_ERR_INVALID_ARG;
   if (!encode_fn()) return RNNT_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   GemmDesc g{A, a_mn, B, b_mn, M, N, K};
@@ -1210,7 +1304,7 @@ extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A
   tp.C = C;
   tp.ldc = N;
   tp.k_splits = k_splits;
-  cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, s)
-                             : launch_gemm<EPI_STORE>(g, tp, bn, s);
+  cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, cluster, s)
+                             : launch_gemm<EPI_STORE>(g, tp, bn, cluster, s);
   return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
 }

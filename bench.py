@@ -101,6 +101,32 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
                             "tc_bwd_dwo": 2.0}
 
 
+def kernel_source_hash() -> str:
+    """sha1 of the tensor-core kernel sources (the ncu traffic figures are only
+    valid for the source they were captured from)."""
+    import hashlib
+    h = hashlib.sha1()
+    for f in ("k_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summaries in profiles/ (a line `traffic <kernel> <workload> <bytes> src=<sha>`),
+    or None when absent or taken from different kernel source."""
+    import glob
+    import re
+    want = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(path):
+            m = re.match(r"\s*traffic\s+(\S+)\s+(\S+)\s+(\d+)\s+src=(\w+)", line)
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == want:
+                return int(m.group(3))
+    return None
+
+
 def reduce_max(x: float, dist, device) -> float:
     """Max of a per-rank float over all ranks (the slowest rank sets the job time)."""
     if dist is None:
@@ -237,7 +263,10 @@ def run_gpu_bench(args):
         peak = tf_burst
         roof = {"kernel": top_name, "bound": "tensor", "achieved": round(ach, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                "traffic": None, "peak_source": f"{peak_src} bf16 burst"}
+                "traffic": recorded_traffic(top_name, wl.name),
+                "peak_source": f"{peak_src} bf16 burst",
+                "flops_per_launch": flops_per_launch, "launches": top_n,
+                "avg_launch_ms": top_ms / top_n}
     else:
         roof = {"kernel": top_name, "bound": "alu", "achieved": None, "peak": None,
                 "unit": "TFLOP/s", "frac": None, "traffic": None,

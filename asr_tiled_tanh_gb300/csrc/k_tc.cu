@@ -155,32 +155,34 @@ __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) {
 // 32 bias values of columns col0.. as packed bf16 (0 beyond N or without a
 // bias); widened with unpack32 where they are used.
 __device__ __forceinline__ void load_bias_q(const __nv_bfloat16* bias, int N, int col0,
-                                            uint4* q) {
+                                            uint4 (&q)[4]) {
   if (bias && col0 + 32 <= N && (N & 7) == 0) {
     const uint4* src = (const uint4*)(bias + col0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
     return;
   }
-  __nv_bfloat16 h[32];
+  const unsigned short* b16 = (const unsigned short*)bias;
+  uint32_t w[16];
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
-    h[j] = (bias && col0 + j < N) ? bias[col0 + j] : __float2bfloat16_rn(0.f);
+  for (int k = 0; k < 16; ++k) {
+    const int c = col0 + 2 * k;
+    const uint32_t lo = (bias && c < N) ? b16[c] : 0u;
+    const uint32_t hi = (bias && c + 1 < N) ? b16[c + 1] : 0u;
+    w[k] = lo | (hi << 16);
+  }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = *(const uint4*)(h + 8 * i);
+  for (int i = 0; i < 4; ++i) q[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-// 32 bf16 values at p (16-byte aligned) widened to fp32.
-__device__ __forceinline__ void unpack32(const uint4* q, float* out) {
+// 32 bf16 values (four 16-byte words) widened to fp32.
+__device__ __forceinline__ void unpack32(const uint4 (&q)[4], float (&out)[32]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t u[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __nv_bfloat162 h2 = *(const __nv_bfloat162*)&u[k];
-      out[i * 8 + 2 * k] = __low2float(h2);
-      out[i * 8 + 2 * k + 1] = __high2float(h2);
-    }
+    out[i * 8 + 0] = ptx::bf16lo(q[i].x); out[i * 8 + 1] = ptx::bf16hi(q[i].x);
+    out[i * 8 + 2] = ptx::bf16lo(q[i].y); out[i * 8 + 3] = ptx::bf16hi(q[i].y);
+    out[i * 8 + 4] = ptx::bf16lo(q[i].z); out[i * 8 + 5] = ptx::bf16hi(q[i].z);
+    out[i * 8 + 6] = ptx::bf16lo(q[i].w); out[i * 8 + 7] = ptx::bf16hi(q[i].w);
   }
 }
 
@@ -188,7 +190,7 @@ __device__ __forceinline__ void unpack32(const uint4* q, float* out) {
 // to global memory at rows base_row .. +31, columns col0 .. +31 (ld elements
 // per row), through the warp's staging area: each store instruction then
 // covers 8 consecutive rows' 64-byte pieces instead of 32 scattered rows.
-__device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4* q,
+__device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4 (&q)[4],
                                                 __nv_bfloat16* gbase, long long ld,
                                                 bool row_ok_mask_all) {
   const int lane = threadIdx.x & 31;
@@ -208,7 +210,7 @@ __device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4*
 // base_row .. +31, loaded with 8 rows per instruction and redistributed
 // through the staging area.
 __device__ __forceinline__ void load_rows_bf16(unsigned char* stg, const __nv_bfloat16* gbase,
-                                               long long ld, uint4* q) {
+                                               long long ld, uint4 (&q)[4]) {
   const int lane = threadIdx.x & 31;
   uint4 x[4];
 #pragma unroll
@@ -228,14 +230,8 @@ __device__ __forceinline__ void load_rows_bf16(unsigned char* stg, const __nv_bf
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* d) {
-  __nv_bfloat162 q0 = __floats2bfloat162_rn(d[0], d[1]);
-  __nv_bfloat162 q1 = __floats2bfloat162_rn(d[2], d[3]);
-  __nv_bfloat162 q2 = __floats2bfloat162_rn(d[4], d[5]);
-  __nv_bfloat162 q3 = __floats2bfloat162_rn(d[6], d[7]);
-  uint4 pk;
-  pk.x = *(uint32_t*)&q0; pk.y = *(uint32_t*)&q1;
-  pk.z = *(uint32_t*)&q2; pk.w = *(uint32_t*)&q3;
-  return pk;
+  return make_uint4(ptx::pack_bf16x2(d[0], d[1]), ptx::pack_bf16x2(d[2], d[3]),
+                    ptx::pack_bf16x2(d[4], d[5]), ptx::pack_bf16x2(d[6], d[7]));
 }
 
 // Select v[j] for a runtime j in [0,32) without local memory.
@@ -289,9 +285,10 @@ __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const
   const int jl = st.lab - col0;
   if (jl >= 0 && jl < 32) st.h_lab = pick32(v, jl);
   if (keep) {
-    for (int j = 0; j < nv; j += 2) {
-      if (j + 1 < nv) *(__nv_bfloat162*)(keep + j) = __floats2bfloat162_rn(v[j], v[j + 1]);
-      else keep[j] = __float2bfloat16_rn(v[j]);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      if (j + 1 < nv) *(uint32_t*)(keep + j) = ptx::pack_bf16x2(v[j], v[j + 1]);
+      else if (j < nv) keep[j] = __float2bfloat16_rn(v[j]);
     }
   }
 }
@@ -384,7 +381,9 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       store_rows_bf16((unsigned char*)wscr, q, gbase, p.N, true);
     } else {
       __nv_bfloat16* dst = gbase + (long long)lane * p.N;
-      for (int j = 0; j < nv; ++j) dst[j] = __float2bfloat16_rn(d[j]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nv) dst[j] = __float2bfloat16_rn(d[j]);
     }
   }
 }
@@ -489,15 +488,19 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                   ptx::tma_load_2d_mc(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j,
                                       kb * BK, kMask);
             }
-            issued[stage] = (int)phase;
+#pragma unroll
+            for (int k = 0; k < 6; ++k)
+              if (k == stage) issued[k] = (int)phase;
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
         }
       }
       // Wind-down: every fill this thread issued must have landed before the
       // CTA may exit (normally all of them were consumed already).
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] >= 0 && !ptx::mbar_wait(&full[s], (uint32_t)issued[s], WAIT_NS))
+#pragma unroll
+      for (int s = 0; s < 6; ++s)
+        if (s < STAGES && issued[s] >= 0 &&
+            !ptx::mbar_wait(&full[s], (uint32_t)issued[s], WAIT_NS))
           report_timeout(p, abort_flag);
     }
   } else if (warp == 1) {
@@ -605,11 +608,11 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           if (USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
           float bb[32];
           if (USE_BIAS) unpack32(bq, bb);
-          if (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
+          if constexpr (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
             const long long grow = (long long)w.m * BM + row;
             if (grow < p.M && col0 < p.N) {
               float* dst = p.C + grow * p.ldc + col0;
-              if (EPI == EPI_STORE) {
+              if constexpr (EPI == EPI_STORE) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] += bb[j];
                 if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
@@ -617,53 +620,60 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                   for (int j = 0; j < 32; j += 4)
                     *(float4*)(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                 } else {
-                  for (int j = 0; j < 32 && col0 + j < p.N; ++j) dst[j] = v[j];
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) dst[j] = v[j];
                 }
               } else if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
                   ptx::red_add_v4(dst + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
               } else {
-                for (int j = 0; j < 32 && col0 + j < p.N; ++j) ptx::red_add_f32(dst + j, v[j]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < p.N) ptx::red_add_f32(dst + j, v[j]);
               }
             }
-          } else if (EPI == EPI_LSE) {
+          } else if constexpr (EPI == EPI_LSE) {
             lse_chunk(ls, p, rc, v, bb, col0,
                       p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
-          } else if (EPI == EPI_DH) {
+          } else if constexpr (EPI == EPI_DH) {
             dh_chunk(ds, p, rc, v, bb, col0, (long long)w.m * BM + sub * 32, wscr,
                      w.m < p.ch.ntiles);
-          } else if (EPI == EPI_DA) {
+          } else if constexpr (EPI == EPI_DA) {
             // da = dz (1 - z^2) on the thread's own row, then 16-column halves
             // of the warp's 32 x 32 block are transposed through the warp's
             // scratch (lane = column c, row half h) and summed over the tile's
             // u (into dA[b,t]) and t (into dLr[b,u]).
-            float da[32];
+            // (da is formed in place in v)
             if (tr.exists && col0 + 32 <= p.N && (p.N & 7) == 0) {
               uint4 zq[4];
               load_rows_bf16((unsigned char*)wscr,
                              p.Zin + ((long long)w.m * BM + sub * 32) * p.N + col0, p.N, zq);
-              float z[32];
-              unpack32(zq, z);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) da[j] = rc.valid ? v[j] * (1.f - z[j] * z[j]) : 0.f;
-            } else if (rc.valid) {
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t zw[4] = {zq[i].x, zq[i].y, zq[i].z, zq[i].w};
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float z = (col0 + j < p.N)
-                                    ? bf(p.Zin, ((long long)w.m * BM + row) * p.N + col0 + j) : 0.f;
-                da[j] = (col0 + j < p.N) ? v[j] * (1.f - z * z) : 0.f;
+                for (int k = 0; k < 4; ++k) {
+                  const float z0 = ptx::bf16lo(zw[k]), z1 = ptx::bf16hi(zw[k]);
+                  v[8 * i + 2 * k] = rc.valid ? v[8 * i + 2 * k] * (1.f - z0 * z0) : 0.f;
+                  v[8 * i + 2 * k + 1] = rc.valid ? v[8 * i + 2 * k + 1] * (1.f - z1 * z1) : 0.f;
+                }
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) da[j] = 0.f;
+              for (int j = 0; j < 32; ++j) {
+                const bool ok = rc.valid && col0 + j < p.N;
+                const float z = ok ? bf(p.Zin, ((long long)w.m * BM + row) * p.N + col0 + j) : 0.f;
+                v[j] = ok ? v[j] * (1.f - z * z) : 0.f;
+              }
             }
             const int cc = lane & 15, h = lane >> 4;
             const int tw = tr.t0 + sub * 4;   // rows r of this warp: t = tw + r/8, u = u0 + r%8
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = da[half * 16 + j];
+              for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = v[half * 16 + j];
               __syncwarp();
               // this lane: column col0 + half*16 + cc, rows h*16 .. h*16+15
               // (t = tw + 2h and tw + 2h + 1, u = u0 .. u0+7)
@@ -783,12 +793,11 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
       const float4 a0 = a[0], a1 = a[1], l0 = l[0], l1 = l[1];
       // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
       using ptx::tanh_approx;
-      __nv_bfloat162 q0 = __floats2bfloat162_rn(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
-      __nv_bfloat162 q1 = __floats2bfloat162_rn(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
-      __nv_bfloat162 q2 = __floats2bfloat162_rn(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
-      __nv_bfloat162 q3 = __floats2bfloat162_rn(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
-      out.x = *(uint32_t*)&q0; out.y = *(uint32_t*)&q1;
-      out.z = *(uint32_t*)&q2; out.w = *(uint32_t*)&q3;
+      using ptx::pack_bf16x2;
+      out.x = pack_bf16x2(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
+      out.y = pack_bf16x2(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
+      out.z = pack_bf16x2(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
+      out.w = pack_bf16x2(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
     }
     *(uint4*)(Z + (row0 + i) * H + k8) = out;
   }

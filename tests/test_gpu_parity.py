@@ -87,9 +87,12 @@ def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
     untiled = run_gpu(inp, mode="untiled")
     for r in runs[1:] + [untiled]:
         np.testing.assert_array_equal(r["loss"], runs[0]["loss"])
+    # bf16: dA is rounded to bf16 before the encoder GEMMs, so an fp32 atomic-order
+    # difference can flip a rounding there
+    tol_tiles = 1e-5 if dtype == "f32" else 1e-3
     for r in runs[1:]:
         for k in GRAD_KEYS:
-            assert rel_l2(r[k], runs[0][k]) < 1e-5, k
+            assert rel_l2(r[k], runs[0][k]) < tol_tiles, k
     tol_untiled = 1e-5 if dtype == "f32" else 1e-2
     for k in GRAD_KEYS:
         assert rel_l2(untiled[k], runs[0][k]) < tol_untiled, k

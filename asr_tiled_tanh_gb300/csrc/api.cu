@@ -81,6 +81,9 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   p->s_lnPD = put(4 * ncell);
   p->s_alpha = put(4 * ncell);
   p->s_beta = put(4 * ncell);
+  // the joint projections are kept for the backward (tiled mode recomputes z from them)
+  p->s_pA = put(4 * B * T * H);
+  p->s_pL = put(4 * B * U1 * H);
   if (d->mode == RNNT_UNTILED) {
     p->s_z = put(rows * H * p->zelem);
     p->s_h = put(rows * V * p->helem);
@@ -88,8 +91,6 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   p->s_total = o;
 
   o = 0;
-  p->w_pA = put(4 * B * T * H);
-  p->w_pL = put(4 * B * U1 * H);
   p->w_dA = put(4 * B * T * H);
   p->w_dLr = put(4 * B * U1 * H);
   if (d->mode == RNNT_TILED) {
@@ -290,8 +291,8 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
   const Shape sh = shape_of(p);
   SavedView sv = saved_view(p, saved);
   char* w = (char*)ws;
-  float* pA = (float*)(w + p.w_pA);
-  float* pL = (float*)(w + p.w_pL);
+  float* pA = (float*)((char*)saved + p.s_pA);
+  float* pL = (float*)((char*)saved + p.s_pL);
 
   LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
   if (p.B == 0) return RNNT_OK;
@@ -337,8 +338,8 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
   cudaStream_t st = (cudaStream_t)stream;
   SavedView sv = saved_view(p, saved);
   char* w = (char*)ws;
-  float* pA = (float*)(w + p.w_pA);
-  float* pL = (float*)(w + p.w_pL);
+  const float* pA = (const float*)((char*)saved + p.s_pA);  // written by rnnt_fwd
+  const float* pL = (const float*)((char*)saved + p.s_pL);
   float* dA = (float*)(w + p.w_dA);
   float* dLr = (float*)(w + p.w_dLr);
   int32_t* Teff = (int32_t*)(w + p.w_len);
@@ -370,10 +371,6 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
   LAUNCH("eff_lengths", launch_eff_lengths(shape_of(p), sv, T_len, U_len, Teff, Ueff, st));
 
   rnnt_status s;
-  if (!untiled) {
-    s = projections(p, hA, hL, pr, pA, pL, st);
-    if (s != RNNT_OK) return s;
-  }
   void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
 

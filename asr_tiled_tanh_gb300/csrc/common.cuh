@@ -42,9 +42,10 @@ struct Plan {
   long long chunk_rows;     // = chunk_tiles * TILE
   int zelem, helem;         // bytes per element of the z and score buffers
   // saved layout
-  size_t s_status, s_prefix, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_z, s_h, s_total;
+  size_t s_status, s_prefix, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_pA, s_pL, s_z, s_h,
+      s_total;
   // workspace layout
-  size_t w_pA, w_pL, w_dA, w_dLr, w_z, w_h, w_dz, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
+  size_t w_dA, w_dLr, w_z, w_h, w_dz, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
       w_total;
 };
 

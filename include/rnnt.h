@@ -111,19 +111,22 @@ typedef struct {
 } rnnt_saved_offsets;
 
 /* Bytes of the `saved` buffer that rnnt_fwd fills and rnnt_bwd reads:
- * 20 B per lattice position [B,T,U1] plus small headers, and in untiled mode
- * the kept z and scores.  Returns 0 if dims are invalid. */
+ * 20 B per lattice position [B,T,U1], the joint projections W^A hA + b^Z
+ * [B,T,H] and W^L hL [B,U1,H] in fp32 (kept so that the backward rebuilds z
+ * without redoing them), small headers, and in untiled mode the kept z and
+ * scores.  Returns 0 if dims are invalid. */
 size_t rnnt_saved_bytes(const rnnt_dims* dims);
 
 /* Fill *out with the layout of `saved` for dims.  Returns RNNT_OK or
  * RNNT_ERR_INVALID_ARG. */
 rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out);
 
-/* Bytes of the scratch buffer `ws` that rnnt_fwd and rnnt_bwd need: the joint
- * projections W^A hA + b^Z [B,T,H] and W^L hL [B,U1,H] (fp32), the tile
- * buffers (tile_cells x (H + V) elements in tiled mode), and the fp32
- * gradient accumulators of the joint pre-activations.  Returns 0 if dims are
- * invalid.  The buffer needs no initialisation and 256-byte alignment. */
+/* Bytes of the scratch buffer `ws` that rnnt_fwd and rnnt_bwd need: the tile
+ * buffers (tile_cells x (H + V) elements in tiled mode), the fp32 gradient
+ * accumulators of the joint pre-activations [B,T,H] and [B,U1,H], and their
+ * bf16 copies for the encoder-side products.  Returns 0 if dims are invalid.
+ * The buffer needs no initialisation (its contents are not carried from
+ * rnnt_fwd to rnnt_bwd) and 256-byte alignment. */
 size_t rnnt_workspace_bytes(const rnnt_dims* dims);
 
 /* Forward pass.  Inputs: hA [B,T,HA], hL [B,U1,HL], params, labels [B,U1]

@@ -322,11 +322,13 @@ k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restr
 // ---------------------------------------------------------------------------
 // The same recursion with the log-probabilities streamed through shared
 // memory: rows of the sample's lattice are copied (cp.async) in windows of 32
-// into a ring of ceil(U1/32) + 2 window slots, one window ahead of the
-// wavefront, so the diagonal loop reads only shared memory.  The front at
-// diagonal d spans rows [max(0, d - U_b), min(d, T_b - 1)], at most
-// ceil(U1/32) + 1 windows.  One warp per block: alpha (blockIdx.y == 0) or
-// beta (blockIdx.y == 1) of sample blockIdx.x.
+// rows into a circular buffer of R rows (R a power of two, at least
+// ceil(U1/32) + 2 windows), one window ahead of the wavefront, so the diagonal
+// loop reads only shared memory.  The front at diagonal d spans rows
+// [max(0, d - U_b), min(d, T_b - 1)], at most ceil(U1/32) + 1 windows.
+// Lane l owns the NJ consecutive label positions u = NJ*l + j, so a diagonal
+// needs a single shuffle (for j = 0 with alpha, j = NJ-1 with beta).
+// One warp per block: alpha (blockIdx.y == 0) or beta (blockIdx.y == 1).
 constexpr int AB_W = 32;
 
 __device__ __forceinline__ void cp_async4(float* dst, const float* src) {
@@ -346,8 +348,8 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int NJ, bool FAST>
 __global__ void __launch_bounds__(32)
 k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
-                  SavedView sv, float* __restrict__ loss, int nslots) {
-  extern __shared__ float ring[];  // nslots x [lpb | lpl] x AB_W x U1
+                  SavedView sv, float* __restrict__ loss, int R) {
+  extern __shared__ float ring[];  // [lpb | lpl] x R rows x U1
   const int b = blockIdx.x;
   const bool is_beta = blockIdx.y != 0;
   const int lane = threadIdx.x;
@@ -359,55 +361,54 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
   const float* __restrict__ LPL = sv.lpl + base;
   float* __restrict__ OUT = (is_beta ? sv.beta : sv.alpha) + base;
   const int ndiag = Tb + Ub;
-  const int slot_floats = 2 * AB_W * U1;
+  const int plane = R * U1;
+  const int rmask = R - 1;
   const int nwin = (Tb + AB_W - 1) / AB_W;
 
   auto load_window = [&](int w) {  // rows [w*32, w*32+32) of lpb and lpl
-    float* dst = ring + (w % nslots) * slot_floats;
     const int r0 = w * AB_W, r1 = min(Tb, r0 + AB_W);
     const int n = (r1 - r0) * U1;
+    float* dst = ring + (r0 & rmask) * U1;
     const float* gb = LPB + (size_t)r0 * U1;
     const float* gl = LPL + (size_t)r0 * U1;
     for (int i = lane; i < n; i += 32) {
       cp_async4(dst + i, gb + i);
-      cp_async4(dst + AB_W * U1 + i, gl + i);
+      cp_async4(dst + plane + i, gl + i);
     }
     cp_async_commit();
   };
-  // windows are loaded in the order the wavefront needs them
-  int next_win, ready;   // next window to load; last window known complete
+  int next_win, ready;  // next window to load; window known complete
   if (!is_beta) {
     load_window(0);
     if (nwin > 1) load_window(1); else cp_async_commit();
     next_win = 2;
-    cp_async_wait<1>();
     ready = 0;
   } else {
     load_window(nwin - 1);
     if (nwin > 1) load_window(nwin - 2); else cp_async_commit();
     next_win = nwin - 3;
-    cp_async_wait<1>();
     ready = nwin - 1;
   }
+  cp_async_wait<1>();
   __syncwarp();
 
   float own[NJ], send[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
+  const int u0 = NJ * lane;
 
   for (int s = 0; s < ndiag; ++s) {
     const int d = is_beta ? ndiag - 1 - s : s;
-    // keep the windows of rows [lo, hi] resident, one more in flight
     if (!is_beta) {
-      const int hi = min(d, Tb - 1) / AB_W;
-      if (hi > ready) {            // entering window `hi`: it was loaded one ahead
+      const int hi = min(d, Tb - 1) >> 5;
+      if (hi > ready) {  // entering window `hi`, loaded one ahead
         if (next_win < nwin) { load_window(next_win); ++next_win; } else cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();
         ready = hi;
       }
     } else {
-      const int lo = max(0, d - Ub) / AB_W;
+      const int lo = max(0, d - Ub) >> 5;
       if (lo < ready) {
         if (next_win >= 0) { load_window(next_win); --next_win; } else cp_async_commit();
         cp_async_wait<1>();
@@ -415,39 +416,35 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
         ready = lo;
       }
     }
+    // neighbours from the previous diagonal
     float nb[NJ];
+    if (!is_beta) {
+      const float x = __shfl_up_sync(0xffffffffu, send[NJ - 1], 1);
+      nb[0] = lane == 0 ? -INFINITY : x;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (!is_beta) {
-        const float x = __shfl_up_sync(0xffffffffu, send[j], 1);
-        const float y = __shfl_sync(0xffffffffu, j > 0 ? send[j - 1] : -INFINITY, 31);
-        nb[j] = lane == 0 ? y : x;
-      } else {
-        const float x = __shfl_down_sync(0xffffffffu, send[j], 1);
-        const float y = __shfl_sync(0xffffffffu, j + 1 < NJ ? send[j + 1] : -INFINITY, 0);
-        nb[j] = lane == 31 ? y : x;
-      }
+      for (int j = 1; j < NJ; ++j) nb[j] = send[j - 1];
+    } else {
+      const float x = __shfl_down_sync(0xffffffffu, send[0], 1);
+      nb[NJ - 1] = lane == 31 ? -INFINITY : x;
+#pragma unroll
+      for (int j = 0; j < NJ - 1; ++j) nb[j] = send[j + 1];
     }
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int u = lane + 32 * j, t = d - u;
+      const int u = u0 + j, t = d - u;
       const bool in = u <= Ub && t >= 0 && t < Tb;
-      float lb = -INFINITY, ll = -INFINITY;
-      if (in) {
-        const float* w = ring + ((t / AB_W) % nslots) * slot_floats + (t % AB_W) * U1 + u;
-        lb = w[0];
-        ll = w[AB_W * U1];
+      const int off = (t & rmask) * U1 + min(u, U1 - 1);  // always inside the ring
+      const float lb = in ? ring[off] : -INFINITY;
+      const float ll = in ? ring[off + plane] : -INFINITY;
+      float val;
+      if (!is_beta) {
+        val = (s == 0) ? 0.f : lae<FAST>(own[j], nb[j]);
+      } else {
+        const float from_t = (t + 1 < Tb) ? own[j] : (u == Ub ? 0.f : -INFINITY);
+        val = lae<FAST>(from_t + lb, nb[j] + ll);
       }
-      float val = -INFINITY;
-      if (in) {
-        if (!is_beta) {
-          val = (s == 0) ? 0.f : lae<FAST>(own[j], nb[j]);
-        } else {
-          const float from_t = (t + 1 < Tb) ? own[j] : (u == Ub ? 0.f : -INFINITY);
-          val = lae<FAST>(from_t + lb, nb[j] + ll);
-        }
-        OUT[(size_t)t * U1 + u] = val;
-      }
+      val = in ? val : -INFINITY;
+      if (in) OUT[(size_t)t * U1 + u] = val;
       if (!is_beta) {
         own[j] = val + lb;
         send[j] = val + ll;
@@ -461,7 +458,7 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
   if (!is_beta) {
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      if (lane + 32 * j == Ub) {
+      if (u0 + j == Ub) {
         sv.lnP[b] = own[j];
         loss[b] = -own[j];
       }
@@ -485,16 +482,16 @@ static cudaError_t launch_ab(const Shape& sh, const int32_t* T_len, const int32_
 
 template <int NJ, bool FAST>
 static cudaError_t launch_ab_smem(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
-                                  SavedView sv, float* loss, int nslots, size_t smem,
+                                  SavedView sv, float* loss, int R, size_t smem,
                                   cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_alpha_beta_smem<NJ, FAST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_alpha_beta_smem<NJ, FAST><<<dim3(sh.B, 2), 32, smem, s>>>(sh, T_len, U_len, sv, loss, nslots);
+  k_alpha_beta_smem<NJ, FAST><<<dim3(sh.B, 2), 32, smem, s>>>(sh, T_len, U_len, sv, loss, R);
   return cudaGetLastError();
 }
 
@@ -502,19 +499,20 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
                               SavedView sv, float* loss, bool fast, cudaStream_t s) {
   if (sh.B == 0) return cudaSuccess;
   if (sh.U1 > 1024) return cudaErrorInvalidValue;
-  // shared-memory ring when it fits in 200 KiB, else the register-prefetch kernel
-  const int nslots = (int)cdiv(sh.U1, AB_W) + 2;
-  const size_t smem = (size_t)nslots * 2 * AB_W * sh.U1 * sizeof(float);
-  if (smem <= 200 * 1024) {
-    const int nj = (int)cdiv(sh.U1, 32);
+  // shared-memory ring when it fits in 220 KiB, else the register-prefetch kernel
+  int R = AB_W;
+  while (R < ((int)cdiv(sh.U1, AB_W) + 2) * AB_W) R *= 2;
+  const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float);
+  const int nj = (int)cdiv(sh.U1, 32);
+  if (smem <= 220 * 1024 && nj <= 4) {
     if (fast) {
-      if (nj <= 1) return launch_ab_smem<1, true>(sh, T_len, U_len, sv, loss, nslots, smem, s);
-      if (nj <= 2) return launch_ab_smem<2, true>(sh, T_len, U_len, sv, loss, nslots, smem, s);
-      return launch_ab_smem<4, true>(sh, T_len, U_len, sv, loss, nslots, smem, s);
+      if (nj <= 1) return launch_ab_smem<1, true>(sh, T_len, U_len, sv, loss, R, smem, s);
+      if (nj <= 2) return launch_ab_smem<2, true>(sh, T_len, U_len, sv, loss, R, smem, s);
+      return launch_ab_smem<4, true>(sh, T_len, U_len, sv, loss, R, smem, s);
     }
-    if (nj <= 1) return launch_ab_smem<1, false>(sh, T_len, U_len, sv, loss, nslots, smem, s);
-    if (nj <= 2) return launch_ab_smem<2, false>(sh, T_len, U_len, sv, loss, nslots, smem, s);
-    return launch_ab_smem<4, false>(sh, T_len, U_len, sv, loss, nslots, smem, s);
+    if (nj <= 1) return launch_ab_smem<1, false>(sh, T_len, U_len, sv, loss, R, smem, s);
+    if (nj <= 2) return launch_ab_smem<2, false>(sh, T_len, U_len, sv, loss, R, smem, s);
+    return launch_ab_smem<4, false>(sh, T_len, U_len, sv, loss, R, smem, s);
   }
   return fast ? launch_ab<true>(sh, T_len, U_len, sv, loss, s)
               : launch_ab<false>(sh, T_len, U_len, sv, loss, s);

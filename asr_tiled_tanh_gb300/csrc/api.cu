@@ -58,9 +58,9 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
     if (d->tile_cells > 0) {
       ct = cdiv(d->tile_cells, TILE);
     } else {
-      // default: at most 512 MiB of tile buffers, in whole waves of 152 tiles
+      // default: at most 2 GiB of tile buffers, in whole waves of 152 tiles
       const long long per_tile = (long long)TILE * (H * p->zelem + V * p->helem);
-      ct = (512LL << 20) / per_tile;
+      ct = (2048LL << 20) / per_tile;
       ct = ct / 152 * 152;
       if (ct < 152) ct = 152;
     }

@@ -57,6 +57,7 @@ struct TcParams {
   int units;             // including the padding units of a ragged last cluster group
   int m_groups;          // M tiles in groups of the cluster size
   int row_complete;      // a unit is one M tile with all of its N tiles, in order
+  int n_split;           // row-complete units: N tiles split into this many units (1 for LSE)
   float* C;              // STORE / ATOMIC output, row-major with ldc
   long long ldc;
   const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
@@ -99,7 +100,12 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
   const int r = u % CL;
   int rest = u / CL;
   if (p.row_complete) {
-    w.m = rest * CL + r; w.n0 = 0; w.n1 = p.n_tiles; w.kb0 = 0; w.kb1 = p.kb_total;
+    const int ns = p.n_split > 1 ? p.n_split : 1;
+    const int per = (p.n_tiles + ns - 1) / ns;
+    const int sp = rest % ns;
+    w.m = (rest / ns) * CL + r;
+    w.n0 = sp * per; w.n1 = min(p.n_tiles, w.n0 + per);
+    w.kb0 = 0; w.kb1 = (w.n1 > w.n0) ? p.kb_total : 0;
   } else {
     const int ks = rest % p.k_splits;
     rest /= p.k_splits;
@@ -206,6 +212,31 @@ __device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4 
   __syncwarp();
 }
 
+// Split form of load_rows_bf16: issue the coalesced global loads early, and
+// redistribute through the staging area when the values are needed.
+__device__ __forceinline__ void issue_rows_bf16(const __nv_bfloat16* gbase, long long ld,
+                                                uint4 (&x)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), piece = lane & 3;
+    x[i] = __ldg((const uint4*)(gbase + (long long)r * ld + piece * 8));
+  }
+}
+__device__ __forceinline__ void finish_rows_bf16(unsigned char* stg, const uint4 (&x)[4],
+                                                 uint4 (&q)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), piece = lane & 3;
+    *(uint4*)(stg + r * STAGE_PITCH + piece * 16) = x[i];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = *(const uint4*)(stg + lane * STAGE_PITCH + i * 16);
+  __syncwarp();
+}
+
 // The reverse: each lane gets its own row's 32 bf16 (64 bytes) of rows
 // base_row .. +31, loaded with 8 rows per instruction and redistributed
 // through the staging area.
@@ -267,17 +298,27 @@ __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const
                                           __nv_bfloat16* keep) {
   if (!rc.valid) return;
   const int nv = min(32, p.N - col0);
-  float cm = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    v[j] += bb[j];
-    cm = (j < nv) ? fmaxf(cm, v[j]) : cm;
+  for (int j = 0; j < 32; ++j) v[j] += bb[j];
+  if (nv < 32) {  // columns past V take no part in the sum
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (j < nv) ? v[j] : -INFINITY;
   }
+  float cm = v[0];
+#pragma unroll
+  for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
   const float nm = fmaxf(st.run_max, cm);
   float s = st.run_sum * ptx::ex2((st.run_max - nm) * kLog2e);
   const float nmL = nm * kLog2e;
+  float s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) s += (j < nv) ? ptx::ex2(fmaf(v[j], kLog2e, -nmL)) : 0.f;
+  for (int j = 0; j < 32; j += 4) {
+    s += ptx::ex2(fmaf(v[j], kLog2e, -nmL));
+    s1 += ptx::ex2(fmaf(v[j + 1], kLog2e, -nmL));
+    s2 += ptx::ex2(fmaf(v[j + 2], kLog2e, -nmL));
+    s3 += ptx::ex2(fmaf(v[j + 3], kLog2e, -nmL));
+  }
+  s += (s1 + s2) + s3;
   st.run_sum = s;
   st.run_max = nm;
   const int jb = p.ch.sh.blank - col0;
@@ -341,13 +382,25 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   const int nv = min(32, p.N - col0);
   float d[32];
   if (rc.valid) {
+    // g (pb + pl) softmax_v for every column; the blank and label terms are
+    // applied only to the (at most two) columns they belong to
     const float nl = st.lnPD * kLog2e;
+    const float gg = st.g * st.gam;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float x = st.gam * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -nl));
-      if (col0 + j == p.ch.sh.blank) x -= st.pb;
-      if (col0 + j == st.lab) x -= st.pl;
-      d[j] = (j < nv) ? st.g * x : 0.f;
+    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -nl));
+    const int jb = p.ch.sh.blank - col0;   // uniform over the warp
+    if (jb >= 0 && jb < 32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) d[j] = (j == jb) ? d[j] - st.g * st.pb : d[j];
+    }
+    const int jl = st.lab - col0;
+    if (jl >= 0 && jl < 32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) d[j] = (j == jl) ? d[j] - st.g * st.pl : d[j];
+    }
+    if (nv < 32) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) d[j] = (j < nv) ? d[j] : 0.f;
     }
   } else {
 #pragma unroll
@@ -597,6 +650,12 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         constexpr bool USE_BIAS = (EPI == EPI_STORE || EPI == EPI_LSE || EPI == EPI_DH);
         uint4 bq[4];
         if (USE_BIAS) load_bias_q(p.bias, p.N, n * BN + hf * 32, bq);
+        // dz epilogue: z rows of the current chunk, loaded one chunk ahead
+        const bool z_vec = (EPI == EPI_DA) && tr.exists && (p.N & 7) == 0;
+        const __nv_bfloat16* zrow = p.Zin + ((long long)w.m * BM + sub * 32) * p.N;
+        uint4 zx[4];
+        if (EPI == EPI_DA && z_vec && n * BN + hf * 32 + 32 <= p.N)
+          issue_rows_bf16(zrow + n * BN + hf * 32, p.N, zx);
         ptx::tmem_ld_wait();
         ptx::reg_fence32(v);
 #pragma unroll 1
@@ -606,6 +665,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           const int col0 = n * BN + c * 32;
           uint4 bqn[4];
           if (USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
+
           float bb[32];
           if (USE_BIAS) unpack32(bq, bb);
           if constexpr (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
@@ -646,10 +706,11 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // scratch (lane = column c, row half h) and summed over the tile's
             // u (into dA[b,t]) and t (into dLr[b,u]).
             // (da is formed in place in v)
-            if (tr.exists && col0 + 32 <= p.N && (p.N & 7) == 0) {
+            if (z_vec && col0 + 32 <= p.N) {
               uint4 zq[4];
-              load_rows_bf16((unsigned char*)wscr,
-                             p.Zin + ((long long)w.m * BM + sub * 32) * p.N + col0, p.N, zq);
+              finish_rows_bf16((unsigned char*)wscr, zx, zq);
+              // the next chunk's z is in flight while this one is processed
+              if (more && col0 + 96 <= p.N) issue_rows_bf16(zrow + col0 + 64, p.N, zx);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint32_t zw[4] = {zq[i].x, zq[i].y, zq[i].z, zq[i].w};
@@ -720,6 +781,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
               for (int i = 0; i < 4; ++i) bq[i] = bqn[i];
             }
+
           }
         }
         ptx::tc_fence_before();
@@ -972,7 +1034,10 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   if (p.k_splits < 1) p.k_splits = 1;
   p.kb_per_split = (int)cdiv(p.kb_total, p.k_splits);
   p.k_splits = (int)cdiv(p.kb_total, p.kb_per_split);
-  const int groups = p.row_complete ? p.m_groups : p.m_groups * p.n_tiles * p.k_splits;
+  if (p.n_split < 1 || !p.row_complete) p.n_split = 1;
+  if (p.n_split > p.n_tiles) p.n_split = p.n_tiles;
+  const int groups =
+      p.row_complete ? p.m_groups * p.n_split : p.m_groups * p.n_tiles * p.k_splits;
   p.units = groups * CL;
   if (groups <= 0 || g.K <= 0) return cudaSuccess;
   const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
@@ -1186,6 +1251,10 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.grad_loss = grad_loss;
       tp.Hout = Hs;
       tp.dbO = dbO;
+      // fewer than ~4 waves of tiles: split each tile's V range over several
+      // units so that the last wave is not mostly idle
+      tp.n_split = (int)std::max<long long>(1, std::min<long long>(
+                       4, cdiv(4LL * num_sms(), std::max<long long>(1, p.chunk_tiles))));
       tp.status = sv.status;
       if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {

@@ -900,17 +900,60 @@ k_dh_rows_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float* __restr
   }
 }
 
-// out[n] += sum over rows of a bf16 [R][N] matrix.
+int g_num_sms = 0;
+
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+// out[n] += sum over rows of a bf16 [R][N] matrix (N % 8 == 0).  A block is
+// 8 row groups x 32 threads; each thread sums 8 consecutive columns (one
+// 16-byte load per row), so a warp reads 512 contiguous bytes of a row.
 __global__ void __launch_bounds__(256)
 k_colsum_bf16(const __nv_bfloat16* __restrict__ X, long long R, int N, float* __restrict__ out,
               long long rows_per) {
-  const int n = blockIdx.x * 256 + threadIdx.x;
-  if (n >= N) return;
+  __shared__ float part[8][256];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int c0 = (blockIdx.x * 32 + lane) * 8;
   const long long r0 = (long long)blockIdx.y * rows_per;
   const long long r1 = min(R, r0 + rows_per);
-  float s = 0.f;
-  for (long long r = r0; r < r1; ++r) s += __bfloat162float(X[r * N + n]);
-  atomicAdd(out + n, s);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c0 < N) {
+    for (long long r = r0 + grp; r < r1; r += 8) {
+      const uint4 q = __ldg((const uint4*)(X + r * N + c0));
+      acc[0] += ptx::bf16lo(q.x); acc[1] += ptx::bf16hi(q.x);
+      acc[2] += ptx::bf16lo(q.y); acc[3] += ptx::bf16hi(q.y);
+      acc[4] += ptx::bf16lo(q.z); acc[5] += ptx::bf16hi(q.z);
+      acc[6] += ptx::bf16lo(q.w); acc[7] += ptx::bf16hi(q.w);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) part[grp][lane * 8 + k] = acc[k];
+  __syncthreads();
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  if (c < N) {
+    float sum = 0.f;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) sum += part[g][threadIdx.x];
+    if (sum != 0.f) atomicAdd(out + c, sum);
+  }
+}
+
+cudaError_t launch_colsum_bf16(const __nv_bfloat16* X, long long R, int N, float* out,
+                               cudaStream_t s) {
+  if (R <= 0 || N <= 0) return cudaSuccess;
+  const int strips = (int)cdiv(N, 256);
+  long long slabs = std::max<long long>(1, (long long)num_sms() * 4 / strips);
+  long long rows_per = cdiv(R, slabs);
+  if (cdiv(R, rows_per) > 65535) rows_per = cdiv(R, 65535);
+  k_colsum_bf16<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per);
+  return cudaGetLastError();
 }
 
 // bf16 copy of an fp32 [R][N] matrix.
@@ -933,18 +976,6 @@ __global__ void k_mask_rows_bf16(const __nv_bfloat16* __restrict__ x,
     const int b = (int)(row / P), q = (int)(row % P);
     y[i] = (q < len[b]) ? x[i] : __float2bfloat16_rn(0.f);
   }
-}
-
-int g_num_sms = 0;
-
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  return g_num_sms;
 }
 
 int elementwise_grid(size_t n) {
@@ -1119,12 +1150,21 @@ int pick_bn(int N, long long M = 1LL << 40) {
   return w256 <= w128 ? 256 : 128;
 }
 
-// Split K so that the units fill the SMs once, each with >= 8 K blocks.
+// Split K into s ranges (>= 8 K blocks each) so that units_mn * s CTAs fill
+// whole waves of SMs; a small penalty per split keeps the atomics down.
 int pick_splits(int units_mn, int K) {
   const int kb = (int)cdiv(K, BK);
-  int want = (num_sms() + units_mn - 1) / units_mn;
-  want = std::min(want, std::max(1, kb / 8));
-  return std::max(1, want);
+  const int smax = std::max(1, kb / 8);
+  int best = 1;
+  double best_score = -1.0;
+  for (int sp = 1; sp <= smax && sp <= 64; ++sp) {
+    const long long units = (long long)units_mn * sp;
+    const long long waves = cdiv(units, num_sms());
+    const double eff = (double)units / (double)(waves * num_sms());
+    const double score = eff - 0.004 * sp;
+    if (score > best_score + 1e-9) { best_score = score; best = sp; }
+  }
+  return best;
 }
 
 // Cluster size of the lattice GEMMs (scores, dh, dz, dW^O).
@@ -1250,7 +1290,6 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.ch = c;
       tp.grad_loss = grad_loss;
       tp.Hout = Hs;
-      tp.dbO = dbO;
       // fewer than ~4 waves of tiles: split each tile's V range over several
       // units so that the last wave is not mostly idle
       tp.n_split = (int)std::max<long long>(1, std::min<long long>(
@@ -1285,13 +1324,9 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.status = sv.status;
       if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
-    if (dbO && untiled) {  // the tiled path sums dh inside the dh epilogue
+    if (dbO) {  // db^O += sum over the chunk's positions of dh (rows outside are 0)
       ProfScope ps("tc_colsum_dh", s);
-      long long rows_per = 512;
-      if (cdiv(rows, rows_per) > 65535) rows_per = cdiv(rows, 65535);
-      dim3 grid((unsigned)cdiv(p.V, 256), (unsigned)cdiv(rows, rows_per));
-      k_colsum_bf16<<<grid, 256, 0, s>>>(Hs, rows, p.V, dbO, rows_per);
-      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
   }
   return RNNT_OK;

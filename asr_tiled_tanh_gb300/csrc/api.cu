@@ -74,6 +74,7 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   auto put = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   p->s_status = put(sizeof(SavedHeader));
   p->s_prefix = put(4 * (B + 1));
+  p->s_tiles = put(16 * (size_t)(p->max_tiles ? p->max_tiles : 1));
   p->s_lnP = put(4 * (B ? B : 1));
   const size_t ncell = B * T * U1;
   p->s_lpb = put(4 * ncell);
@@ -117,6 +118,7 @@ SavedView saved_view(const Plan& p, void* saved) {
   v.status = &hdr->status;
   v.total_tiles = &hdr->total_tiles;
   v.prefix = (int32_t*)(s + p.s_prefix);
+  v.tiles = (int4*)(s + p.s_tiles);
   v.lnP = (float*)(s + p.s_lnP);
   v.lpb = (float*)(s + p.s_lpb);
   v.lpl = (float*)(s + p.s_lpl);
@@ -222,6 +224,7 @@ rnnt_status check_common(const rnnt_dims* dims, const void* hA, const void* hL,
   if (p->B > 0 && (!hA || !hL || !labels || !T_len || !U_len)) return RNNT_ERR_INVALID_ARG;
   if (!pr->WA || !pr->WL || !pr->WO) return RNNT_ERR_INVALID_ARG;
   if (p->U1 > 1024) return RNNT_ERR_UNSUPPORTED_SHAPE;  // one thread per label position
+  if (p->T > 65535) return RNNT_ERR_UNSUPPORTED_SHAPE;  // tile table packs T_b in 16 bits
   if (p->tc) {
     rnnt_status s = tc_check_shape(*p);
     if (s != RNNT_OK) return s;
@@ -296,6 +299,7 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
 
   LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
   if (p.B == 0) return RNNT_OK;
+  LAUNCH("tile_table", launch_tile_table(sh, T_len, U_len, sv, st));
   const size_t ncell = (size_t)p.B * p.T * p.U1;
   // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
   (void)ncell;

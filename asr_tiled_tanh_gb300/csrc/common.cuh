@@ -42,7 +42,7 @@ struct Plan {
   long long chunk_rows;     // = chunk_tiles * TILE
   int zelem, helem;         // bytes per element of the z and score buffers
   // saved layout
-  size_t s_status, s_prefix, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_pA, s_pL, s_z, s_h,
+  size_t s_status, s_prefix, s_tiles, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_pA, s_pL, s_z, s_h,
       s_total;
   // workspace layout
   size_t w_dA, w_dLr, w_z, w_h, w_dz, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
@@ -61,6 +61,7 @@ struct SavedView {
   int32_t* status;
   int32_t* total_tiles;
   int32_t* prefix;  // [B+1]
+  int4* tiles;      // [max tiles]: (b, t0, u0, T_b | U_b << 16) of every actual tile
   float* lnP;       // [B]
   float *lpb, *lpl, *lnPD, *alpha, *beta;
 };

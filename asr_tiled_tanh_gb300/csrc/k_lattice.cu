@@ -103,13 +103,17 @@ __device__ inline int sample_tiles(const Shape& sh, const int32_t* __restrict__ 
     *bad |= status_bit(RNNT_ERR_LENGTH_RANGE);
     return 0;
   }
+  // no early exit, so the label loads of a sample are all in flight together
   const int32_t* lab = labels + (size_t)b * sh.U1;
+  bool ok = true;
+#pragma unroll 8
   for (int u = 1; u <= Ub; ++u) {
-    const int y = lab[u];
-    if (y < 0 || y >= sh.V) {
-      *bad |= status_bit(RNNT_ERR_LABEL_RANGE);
-      return 0;
-    }
+    const int y = __ldg(lab + u);
+    ok &= (y >= 0) & (y < sh.V);
+  }
+  if (!ok) {
+    *bad |= status_bit(RNNT_ERR_LABEL_RANGE);
+    return 0;
   }
   return (int)(cdiv(Tb, TT) * cdiv(Ub + 1, TU));
 }
@@ -171,6 +175,26 @@ k_index(Shape sh, const int32_t* __restrict__ labels, const int32_t* __restrict_
 cudaError_t launch_index(const Shape& sh, const int32_t* labels, const int32_t* T_len,
                          const int32_t* U_len, SavedView sv, float* loss, cudaStream_t s) {
   k_index<<<1, IDX_THREADS, 0, s>>>(sh, labels, T_len, U_len, sv, loss);
+  return cudaGetLastError();
+}
+
+// One block per sample: tile j of sample b (row-major over its t and u blocks)
+// is entry prefix[b] + j of the table.
+__global__ void k_tile_table(Shape sh, const int32_t* __restrict__ T_len,
+                             const int32_t* __restrict__ U_len, SavedView sv) {
+  const int b = blockIdx.x;
+  const int first = sv.prefix[b], n = sv.prefix[b + 1] - first;
+  if (n <= 0) return;
+  const int Tb = T_len[b], Ub = U_len[b];
+  const int ntu = (int)cdiv(Ub + 1, TU);
+  for (int j = threadIdx.x; j < n; j += blockDim.x)
+    sv.tiles[first + j] = make_int4(b, (j / ntu) * TT, (j % ntu) * TU, Tb | (Ub << 16));
+}
+
+cudaError_t launch_tile_table(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                              SavedView sv, cudaStream_t s) {
+  if (sh.B == 0) return cudaSuccess;
+  k_tile_table<<<sh.B, 128, 0, s>>>(sh, T_len, U_len, sv);
   return cudaGetLastError();
 }
 

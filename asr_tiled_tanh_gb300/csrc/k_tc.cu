@@ -134,9 +134,9 @@ __device__ __forceinline__ TileRef tile_ref(const ChunkArgs& c, int m) {
   TileRef r{};
   const long long g = c.first_tile + m;
   if (m >= c.ntiles || g >= *c.sv.total_tiles) return r;
-  TileCoord tc = decode_tile(c.sv.prefix, c.T_len, c.U_len, c.sh.B, g);
+  const int4 e = __ldg(c.sv.tiles + g);  // (b, t0, u0, T_b | U_b << 16)
   r.exists = true;
-  r.b = tc.b; r.t0 = tc.t0; r.u0 = tc.u0; r.Tb = tc.Tb; r.Ub = tc.Ub;
+  r.b = e.x; r.t0 = e.y; r.u0 = e.z; r.Tb = e.w & 0xffff; r.Ub = e.w >> 16;
   return r;
 }
 
@@ -945,6 +945,50 @@ k_colsum_bf16(const __nv_bfloat16* __restrict__ X, long long R, int N, float* __
   }
 }
 
+// out[n] += sum over rows of an fp32 [R][N] matrix (N % 4 == 0); same layout
+// as k_colsum_bf16 with 4 columns (one 16-byte load) per thread.
+__global__ void __launch_bounds__(256)
+k_colsum_f32v(const float* __restrict__ X, long long R, int N, float* __restrict__ out,
+              long long rows_per) {
+  __shared__ float part[8][128];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int c0 = (blockIdx.x * 32 + lane) * 4;
+  const long long r0 = (long long)blockIdx.y * rows_per;
+  const long long r1 = min(R, r0 + rows_per);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c0 < N) {
+    for (long long r = r0 + grp; r < r1; r += 8) {
+      const float4 q = __ldg((const float4*)(X + r * N + c0));
+      acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+    }
+  }
+  part[grp][lane * 4 + 0] = acc.x;
+  part[grp][lane * 4 + 1] = acc.y;
+  part[grp][lane * 4 + 2] = acc.z;
+  part[grp][lane * 4 + 3] = acc.w;
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int c = blockIdx.x * 128 + threadIdx.x;
+    if (c < N) {
+      float sum = 0.f;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) sum += part[g][threadIdx.x];
+      if (sum != 0.f) atomicAdd(out + c, sum);
+    }
+  }
+}
+
+cudaError_t launch_colsum_f32v(const float* X, long long R, int N, float* out, cudaStream_t s) {
+  if (R <= 0 || N <= 0) return cudaSuccess;
+  if (N % 4 != 0) return launch_colsum(X, R, N, N, out, s);
+  const int strips = (int)cdiv(N, 128);
+  long long slabs = std::max<long long>(1, (long long)num_sms() * 4 / strips);
+  long long rows_per = cdiv(R, slabs);
+  if (cdiv(R, rows_per) > 65535) rows_per = cdiv(R, 65535);
+  k_colsum_f32v<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_colsum_bf16(const __nv_bfloat16* X, long long R, int N, float* out,
                                cudaStream_t s) {
   if (R <= 0 || N <= 0) return cudaSuccess;
@@ -1301,6 +1345,10 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       k_dh_rows_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, Hs, grad_loss);
       if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
     }
+    if (dbO) {  // (right after dh is written, while it is warm in L2) db^O += sum over the chunk's positions of dh (rows outside are 0)
+      ProfScope ps("tc_colsum_dh", s);
+      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    }
     {  // dz = dh W^O, da = dz (1 - z^2) reduced into dA and dLr
       ProfScope ps("tc_bwd_dz", s);
       GemmDesc g{Hs, 0, pr->WO, 1, rows, p.H, p.V};
@@ -1323,10 +1371,6 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.ldc = p.H;
       tp.status = sv.status;
       if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
-    }
-    if (dbO) {  // db^O += sum over the chunk's positions of dh (rows outside are 0)
-      ProfScope ps("tc_colsum_dh", s);
-      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
   }
   return RNNT_OK;
@@ -1391,8 +1435,8 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.ldc = p.HL;
     if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
-  if (dbZ) {
-    if (launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, s) != cudaSuccess)
+  if (dbZ) {  // db^Z = sum of dA over frames (= sum of da over every position)
+    if (launch_colsum_f32v(dA, (long long)p.B * p.T, p.H, dbZ, s) != cudaSuccess)
       return RNNT_ERR_CUDA;
   }
   return RNNT_OK;

@@ -18,6 +18,9 @@ cudaError_t launch_zero_many(const ZeroList& z, cudaStream_t s);
 // status word, mark rejected samples (loss = lnP = NaN).
 cudaError_t launch_index(const Shape& sh, const int32_t* labels, const int32_t* T_len,
                          const int32_t* U_len, SavedView sv, float* loss, cudaStream_t s);
+// Table of every actual tile's coordinates (saved.tiles), from the prefix sum.
+cudaError_t launch_tile_table(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                              SavedView sv, cudaStream_t s);
 // alpha/beta wavefronts over every sample's lattice; writes lnP and loss.
 // fast: approximate ex2/lg2 in logaddexp (bf16 path); else expf/log1pf.
 cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32_t* U_len,

@@ -101,6 +101,7 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   if (!p->tc) {
     p->w_dz = put(4 * rows * H);
   } else {
+    p->w_post = put(16 * rows);
     p->w_dA16 = put(2 * B * T * H);
     p->w_dLr16 = put(2 * B * U1 * H);
     p->w_hAm = put(2 * B * T * HA);
@@ -380,7 +381,7 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
 
   if (p.tc) {
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          dA, dLr, dWO, dbO, st);
+                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), st);
     if (s != RNNT_OK) return s;
     s = tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ, st);
     return s;

@@ -45,7 +45,7 @@ struct Plan {
   size_t s_status, s_prefix, s_tiles, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_pA, s_pL, s_z, s_h,
       s_total;
   // workspace layout
-  size_t w_dA, w_dLr, w_z, w_h, w_dz, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
+  size_t w_dA, w_dLr, w_z, w_h, w_dz, w_post, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
       w_total;
 };
 

@@ -421,6 +421,7 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
   for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
   const int u0 = NJ * lane;
 
+#pragma unroll 2
   for (int s = 0; s < ndiag; ++s) {
     const int d = is_beta ? ndiag - 1 - s : s;
     if (!is_beta) {

@@ -68,6 +68,7 @@ struct TcParams {
   float* dA;
   float* dLr;
   float* dbO;            // DH: column sums of dh accumulated here (may be NULL)
+  const float4* post;    // DH: per-row records (g pb, g pl, lnPD log2 e, label bits)
   int32_t* status;
 };
 
@@ -347,29 +348,18 @@ __device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p
 
 // f^W_4 (Eq. 10): dh_v = g ((pb + pl) softmax_v - pb [v = blank] - pl [v = label]).
 struct DhState {
-  float pb, pl, gam, lnPD, g;
+  float gpb, gpl, nl;  // g pb, g pl, lnPD * log2(e)
   int lab;
 };
 
-__device__ __forceinline__ void dh_init(DhState& st, const TcParams& p, const RowCell& rc) {
-  st.pb = st.pl = st.gam = st.lnPD = 0.f;
-  st.g = 1.f;
-  st.lab = -1;
-  if (!rc.valid) return;
-  const SavedView& sv = p.ch.sv;
-  const int U1 = p.ch.sh.U1;
-  const size_t cell = ((size_t)rc.b * p.ch.sh.T + rc.t) * U1 + rc.u;
-  const float lnP = sv.lnP[rc.b];
-  const float a = sv.alpha[cell];
-  float bn;
-  if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
-  else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
-  st.pb = __expf(a + sv.lpb[cell] + bn - lnP);
-  st.pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
-  st.gam = st.pb + st.pl;
-  st.lnPD = sv.lnPD[cell];
-  st.g = p.grad_loss ? p.grad_loss[rc.b] : 1.f;
-  st.lab = (rc.u < rc.Ub) ? p.ch.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
+// The row's record, precomputed by k_posteriors (see there for the formulas).
+__device__ __forceinline__ DhState dh_state(const float4 q) {
+  DhState st;
+  st.gpb = q.x;
+  st.gpl = q.y;
+  st.nl = q.z;
+  st.lab = __float_as_int(q.w);
+  return st;
 }
 
 // dh of 32 columns; the warp's 32 rows are written as bf16 to rows
@@ -384,19 +374,18 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   if (rc.valid) {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
-    const float nl = st.lnPD * kLog2e;
-    const float gg = st.g * st.gam;
+    const float gg = st.gpb + st.gpl;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -nl));
+    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -st.nl));
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
     if (jb >= 0 && jb < 32) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) d[j] = (j == jb) ? d[j] - st.g * st.pb : d[j];
+      for (int j = 0; j < 32; ++j) d[j] = (j == jb) ? d[j] - st.gpb : d[j];
     }
     const int jl = st.lab - col0;
     if (jl >= 0 && jl < 32) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) d[j] = (j == jl) ? d[j] - st.g * st.pl : d[j];
+      for (int j = 0; j < 32; ++j) d[j] = (j == jl) ? d[j] - st.gpl : d[j];
     }
     if (nv < 32) {
 #pragma unroll
@@ -620,8 +609,20 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     constexpr int NCH = BN / 32;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // dh epilogue: the row's record of the next unit is loaded one unit ahead
+    float4 post_next = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+    if (EPI == EPI_DH && cluster_id * CL < p.units) {
+      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank);
+      if (w0.m < p.ch.ntiles) post_next = __ldg(p.post + (long long)w0.m * BM + row);
+    }
     for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
       const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
+      const float4 post_cur = post_next;
+      if (EPI == EPI_DH && (gi + n_clusters) * CL < p.units) {
+        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank);
+        post_next = (wn.m < p.ch.ntiles) ? __ldg(p.post + (long long)wn.m * BM + row)
+                                         : make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+      }
       if (w.kb1 <= w.kb0) continue;
       const int uidx = gi / n_clusters;   // this CTA's unit counter
       // per-unit state of the lattice epilogues
@@ -634,7 +635,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         rc = row_of(tr, row);
       }
       if (EPI == EPI_LSE) lse_init(ls, p, rc);
-      if (EPI == EPI_DH) dh_init(ds, p, rc);
+      if (EPI == EPI_DH) ds = dh_state(post_cur);
       bool ok = true;
       for (int n = w.n0; n < w.n1; ++n) {
         if (*abort_flag || !ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
@@ -845,6 +846,7 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
   const int H8 = H / 8;
   const int r0 = blockIdx.y * (TILE / 4);
   const long long row0 = (long long)blockIdx.x * TILE;
+#pragma unroll 4
   for (int e = threadIdx.x; e < (TILE / 4) * H8; e += blockDim.x) {
     const int i = r0 + e / H8, k8 = (e % H8) * 8;
     const RowCell rc = row_of(tr, i);
@@ -863,6 +865,35 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
     }
     *(uint4*)(Z + (row0 + i) * H + k8) = out;
   }
+}
+
+// Per-row records for the dh epilogue (f^W_4, Eq. 10): with the posteriors
+// pb = exp(alpha + lpb + beta(t+1,u) - lnP) and pl = exp(alpha + lpl +
+// beta(t,u+1) - lnP) (beta(T_b,U_b) := 0, beta(T_b,u<U_b) := -inf, pl = 0 on
+// row U_b) and g = grad_loss[b], the record of a lattice position is
+// (g pb, g pl, lnPD log2(e), label id as bits); rows outside the lattice get
+// (0, 0, +inf, -1).  One thread per row of the chunk.
+__global__ void __launch_bounds__(128)
+k_posteriors(ChunkArgs c, const float* __restrict__ grad_loss, float4* __restrict__ post) {
+  const TileRef tr = tile_ref(c, blockIdx.x);
+  const RowCell rc = row_of(tr, threadIdx.x);
+  float4 rec = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+  if (rc.valid) {
+    const SavedView& sv = c.sv;
+    const int U1 = c.sh.U1;
+    const size_t cell = ((size_t)rc.b * c.sh.T + rc.t) * U1 + rc.u;
+    const float lnP = sv.lnP[rc.b];
+    const float a = sv.alpha[cell];
+    float bn;
+    if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
+    else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
+    const float pb = __expf(a + sv.lpb[cell] + bn - lnP);
+    const float pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
+    const float g = grad_loss ? grad_loss[rc.b] : 1.f;
+    const int lab = (rc.u < rc.Ub) ? c.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
+    rec = make_float4(g * pb, g * pl, sv.lnPD[cell] * kLog2e, __int_as_float(lab));
+  }
+  post[(long long)blockIdx.x * TILE + threadIdx.x] = rec;
 }
 
 // dh from kept bf16 scores, in place (untiled mode; no recompute).
@@ -1310,7 +1341,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Zv,
                               void* Hv, bool untiled, float* dA, float* dLr, float* dWO,
-                              float* dbO, cudaStream_t s) {
+                              float* dbO, float4* post, cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
   long long nch = 0;
@@ -1325,6 +1356,11 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
         k_build_z_bf16<<<dim3((unsigned)c.ntiles, 4), 256, 0, s>>>(c, pA, pL, Z);
         if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
       }
+      {
+        ProfScope ps("tc_posteriors", s);
+        k_posteriors<<<(unsigned)c.ntiles, TILE, 0, s>>>(c, grad_loss, post);
+        if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      }
       // recompute the tile's scores and overwrite them with dh
       ProfScope ps("tc_bwd_dh", s);
       GemmDesc g{Z, 0, pr->WO, 0, rows, p.V, p.H};
@@ -1334,6 +1370,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.ch = c;
       tp.grad_loss = grad_loss;
       tp.Hout = Hs;
+      tp.post = post;
       // fewer than ~4 waves of tiles: split each tile's V range over several
       // units so that the last wave is not mostly idle
       tp.n_split = (int)std::max<long long>(1, std::min<long long>(

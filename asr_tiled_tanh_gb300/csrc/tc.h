@@ -18,12 +18,13 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                              const float* pA, const float* pL, void* Z, void* Hkeep,
                              cudaStream_t s);
-// Backward over every tile: dA, dLr (accumulated), dW^O, db^O.
+// Backward over every tile: dA, dLr (accumulated), dW^O, db^O.  post: the
+// per-row posterior records of one chunk (chunk_rows float4, tiled mode).
 rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Z,
                               void* Hs, bool untiled, float* dA, float* dLr, float* dWO,
-                              float* dbO, cudaStream_t s);
+                              float* dbO, float4* post, cudaStream_t s);
 // dh^A, dW^A, dh^L, dW^L, db^Z from dA and dLr.
 rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
                              const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,

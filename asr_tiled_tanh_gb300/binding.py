@@ -99,6 +99,9 @@ def load(build_if_missing: bool = False):
     lib.rnnt_testing_gemm_bf16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                            ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    lib.rnnt_testing_gemm_timeout.restype = ctypes.c_int
+    lib.rnnt_testing_gemm_timeout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
+                                              P, ctypes.c_ulonglong, P]
     _lib = lib
     return lib
 
@@ -209,6 +212,13 @@ def rnnt_testing_gemm_bf16(A, a_mn, B, b_mn, C, M, N, K, accumulate=0, k_splits=
     _check(load().rnnt_testing_gemm_bf16(M, N, K, _p(A), a_mn, _p(B), b_mn, _p(C), accumulate,
                                          k_splits, bn, cluster, _stream(stream)),
            "rnnt_testing_gemm_bf16")
+
+
+def rnnt_testing_gemm_timeout(A, B, C, status, M, N, K, wait_ns, stream=None):
+    """The GEMM with a stage that is never filled (include/rnnt_testing.h)."""
+    _check(load().rnnt_testing_gemm_timeout(M, N, K, _p(A), _p(B), _p(C), _p(status),
+                                            int(wait_ns), _stream(stream)),
+           "rnnt_testing_gemm_timeout")
 
 
 # --- convenience: buffers owned by torch -------------------------------------

@@ -70,6 +70,8 @@ struct TcParams {
   float* dbO;            // DH: column sums of dh accumulated here (may be NULL)
   const float4* post;    // DH: per-row records (g pb, g pl, lnPD log2 e, label bits)
   int32_t* status;
+  unsigned long long wait_ns;  // limit of every mbarrier wait (0: WAIT_NS)
+  int skip_first_fill;         // test hook: the producer never fills the first stage
 };
 
 template <int BN>
@@ -367,16 +369,16 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
 // dbO is given, the rows are also summed per column through the warp's
 // scratch and added to dbO.  bb: the 32 bias values.  All lanes take part.
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
-                                         const float* v, const float* bb, int col0,
+                                         float (&d)[32], const float* bb, int col0,
                                          long long wrow0, float* wscr, bool write) {
+  // d holds the chunk's scores on entry and dh on exit
   const int nv = min(32, p.N - col0);
-  float d[32];
   if (rc.valid) {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
     const float gg = st.gpb + st.gpl;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(v[j] + bb[j], kLog2e, -st.nl));
+    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(d[j] + bb[j], kLog2e, -st.nl));
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
     if (jb >= 0 && jb < 32) {
 #pragma unroll
@@ -441,6 +443,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0;
   constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
   const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
+  const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
   constexpr int STAGES = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -493,15 +496,22 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       int stage = 0;
       uint32_t phase = 0;
       int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
+      bool first_fill = true;
       for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
         const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!ptx::mbar_wait(&empty[stage], phase ^ 1, WAIT_NS)) {
+            if (!ptx::mbar_wait(&empty[stage], phase ^ 1, wait_ns)) {
               report_timeout(p, abort_flag);
               break;
             }
+            if (p.skip_first_fill && first_fill) {  // test hook: leave this stage empty
+              first_fill = false;
+              if (++stage == STAGES) { stage = 0; phase ^= 1; }
+              continue;
+            }
+            first_fill = false;
             ptx::mbar_arrive_expect_tx(&full[stage], C::STAGE);
             unsigned char* a = sA + stage * C::A_BYTES;
             unsigned char* b = sB + stage * C::B_BYTES;
@@ -542,7 +552,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 #pragma unroll
       for (int s = 0; s < 6; ++s)
         if (s < STAGES && issued[s] >= 0 &&
-            !ptx::mbar_wait(&full[s], (uint32_t)issued[s], WAIT_NS))
+            !ptx::mbar_wait(&full[s], (uint32_t)issued[s], wait_ns))
           report_timeout(p, abort_flag);
     }
   } else if (warp == 1) {
@@ -557,7 +567,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
-          if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, WAIT_NS)) {
+          if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, wait_ns)) {
             report_timeout(p, abort_flag);
             break;
           }
@@ -565,7 +575,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           const uint32_t d_tmem = tmem_base + acc * BN;
           bool ok = true;
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!ptx::mbar_wait(&full[stage], phase, WAIT_NS)) {
+            if (!ptx::mbar_wait(&full[stage], phase, wait_ns)) {
               report_timeout(p, abort_flag);
               ok = false;
               break;
@@ -594,7 +604,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       }
       // all issued MMAs complete before TMEM is released
       ptx::mma_commit(done_bar);
-      if (!ptx::mbar_wait(done_bar, 0, WAIT_NS)) report_timeout(p, abort_flag);
+      if (!ptx::mbar_wait(done_bar, 0, wait_ns)) report_timeout(p, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -638,7 +648,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       if (EPI == EPI_DH) ds = dh_state(post_cur);
       bool ok = true;
       for (int n = w.n0; n < w.n1; ++n) {
-        if (*abort_flag || !ptx::mbar_wait(&acc_full[acc], acc_phase, WAIT_NS)) {
+        if (*abort_flag || !ptx::mbar_wait(&acc_full[acc], acc_phase, wait_ns)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
@@ -799,7 +809,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           cb[2] = ls.h_blank;
           cb[3] = ls.h_lab;
           ptx::mbar_arrive(&comb_bar[uidx & 1]);
-        } else if (ptx::mbar_wait(&comb_bar[uidx & 1], (uint32_t)(uidx >> 1) & 1u, WAIT_NS)) {
+        } else if (ptx::mbar_wait(&comb_bar[uidx & 1], (uint32_t)(uidx >> 1) & 1u, wait_ns)) {
           const float m1 = cb[0], s1 = cb[1];
           const float nm = fmaxf(ls.run_max, m1);
           float sum = 0.f;
@@ -1480,6 +1490,28 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
 }
 
 }  // namespace rnnt
+
+// ===========================================================================
+// Test hook (include/rnnt_testing.h): the GEMM with its first pipeline stage
+// never filled, so the MMA thread's bounded wait runs out.
+extern "C" rnnt_status rnnt_testing_gemm_timeout(int M, int N, int K, const void* A,
+                                                 const void* B, float* C, int32_t* status,
+                                                 unsigned long long wait_ns, void* stream) {
+  using namespace rnnt;
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C || !status || wait_ns == 0)
+    return RNNT_ERR_INVALID_ARG;
+  if (K % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
+  if (!encode_fn()) return RNNT_ERR_CUDA;
+  GemmDesc g{A, 0, B, 0, M, N, K};
+  TcParams tp{};
+  tp.C = C;
+  tp.ldc = N;
+  tp.status = status;
+  tp.wait_ns = wait_ns;
+  tp.skip_first_fill = 1;
+  cudaError_t e = launch_gemm<EPI_STORE>(g, tp, 128, 1, (cudaStream_t)stream);
+  return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
+}
 
 // ===========================================================================
 // Test hook (include/rnnt_testing.h): one raw GEMM through the same kernel.

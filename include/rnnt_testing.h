@@ -27,6 +27,17 @@ rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A, int a_mn,
                                    int b_mn, float* C, int accumulate, int k_splits, int bn,
                                    int cluster, void* stream);
 
+/* Failure-detection hook: the same GEMM (A [M,K], B [N,K], both K-major,
+ * C = A B^T) with the first pipeline stage never filled, so the kernel's
+ * bounded mbarrier waits run out after `wait_ns` nanoseconds each.  The
+ * kernel then sets bit RNNT_ERR_TIMEOUT in the device int32 `*status`, stops
+ * issuing work, waits (bounded) for the loads it did issue, frees its TMEM
+ * and returns; nothing traps and the CUDA context stays usable.  C is left
+ * undefined.  Asynchronous on `stream`. */
+rnnt_status rnnt_testing_gemm_timeout(int M, int N, int K, const void* A, const void* B,
+                                      float* C, int32_t* status, unsigned long long wait_ns,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

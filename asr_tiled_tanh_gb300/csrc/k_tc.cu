@@ -1434,6 +1434,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
   const size_t nA = (size_t)p.B * p.T * p.H, nL = (size_t)p.B * p.U1 * p.H;
   {
     ProfScope ps("tc_enc_prep", s);
+    ps.set_kernels(2 + (dWA ? 1 : 0) + (dWL ? 1 : 0));
     k_f32_to_bf16<<<elementwise_grid(nA), 256, 0, s>>>(dA, dA16, nA);
     k_f32_to_bf16<<<elementwise_grid(nL), 256, 0, s>>>(dLr, dLr16, nL);
     if (dWA) {
@@ -1449,6 +1450,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
   }
   ProfScope ps("tc_enc_grads", s);
+  ps.set_kernels((dhA ? 1 : 0) + (dhL ? 1 : 0) + (dWA ? 1 : 0) + (dWL ? 1 : 0) + (dbZ ? 1 : 0));
   const int MA = p.B * p.T, ML = p.B * p.U1;
   if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
     GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};

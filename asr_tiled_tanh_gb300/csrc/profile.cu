@@ -12,7 +12,8 @@ struct Session {
   int capacity = 0;
   int used = 0;
   std::vector<cudaEvent_t> ev;       // 2 per launch
-  std::vector<const char*> name;     // per launch
+  std::vector<const char*> name;     // per bracket
+  std::vector<int> kernels;          // kernel launches inside each bracket
 };
 Session g_sess;
 struct Entry {
@@ -29,7 +30,12 @@ ProfScope::ProfScope(const char* name, cudaStream_t s) : slot_(-1), s_(s) {
   if (!g_sess.open || g_sess.used >= g_sess.capacity) return;
   slot_ = g_sess.used++;
   g_sess.name[slot_] = name;
+  g_sess.kernels[slot_] = 1;
   cudaEventRecord(g_sess.ev[2 * slot_], s);
+}
+
+void ProfScope::set_kernels(int n) {
+  if (slot_ >= 0) g_sess.kernels[slot_] = n;
 }
 
 ProfScope::~ProfScope() {
@@ -46,6 +52,7 @@ rnnt_status rnnt_profile_start(int capacity) {
   if (capacity < 1 || g_sess.open) return RNNT_ERR_INVALID_ARG;
   g_sess.ev.assign(2 * (size_t)capacity, nullptr);
   g_sess.name.assign(capacity, nullptr);
+  g_sess.kernels.assign(capacity, 1);
   for (auto& e : g_sess.ev) {
     if (cudaEventCreate(&e) != cudaSuccess) {
       for (auto& f : g_sess.ev)
@@ -76,16 +83,17 @@ int rnnt_profile_stop(void) {
     for (auto& e : g_last) {
       if (std::strcmp(e.name, g_sess.name[i]) == 0) {
         e.ms += ms;
-        e.launches += 1;
+        e.launches += g_sess.kernels[i];
         found = true;
         break;
       }
     }
-    if (!found) g_last.push_back(Entry{g_sess.name[i], (double)ms, 1});
+    if (!found) g_last.push_back(Entry{g_sess.name[i], (double)ms, g_sess.kernels[i]});
   }
   for (auto& e : g_sess.ev) cudaEventDestroy(e);
   g_sess.ev.clear();
   g_sess.name.clear();
+  g_sess.kernels.clear();
   if (rc != 0) {
     g_last.clear();
     return -1;

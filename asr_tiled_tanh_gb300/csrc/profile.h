@@ -12,6 +12,8 @@ class ProfScope {
  public:
   ProfScope(const char* name, cudaStream_t s);
   ~ProfScope();
+  // number of kernel launches the bracket holds (1 unless set)
+  void set_kernels(int n);
   ProfScope(const ProfScope&) = delete;
   ProfScope& operator=(const ProfScope&) = delete;
 

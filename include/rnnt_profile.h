@@ -2,10 +2,11 @@
  * rnnt_profile.h -- per-kernel timing of librnnt_gb300, for measurement tools.
  *
  * Not part of the method (the pages define no instrumentation): while a
- * profiling session is open, every kernel launch the library makes through
- * rnnt_fwd / rnnt_bwd is bracketed by a pair of CUDA events recorded on the
- * launch's own stream, so the device time of each kernel can be summed by
- * name after the fact.  Recording an event is asynchronous; nothing is
+ * profiling session is open, every step of the path that rnnt_fwd / rnnt_bwd
+ * run is bracketed by a pair of CUDA events recorded on the step's own
+ * stream, so the device time of each step can be summed by name after the
+ * fact.  A bracket holds one kernel launch, except the encoder-gradient
+ * steps (tc_enc_prep, tc_enc_grads), which hold up to four and five.  Recording an event is asynchronous; nothing is
  * synchronized until rnnt_profile_stop.  Sessions are process-wide and not
  * thread-safe.  Events are created by rnnt_profile_start (no device memory
  * is allocated for them) and destroyed by rnnt_profile_stop.
@@ -19,8 +20,8 @@
 extern "C" {
 #endif
 
-/* Open a session able to record `capacity` launches (further launches are
- * counted but not timed).  RNNT_ERR_INVALID_ARG if capacity < 1 or a session
+/* Open a session able to record `capacity` brackets (further ones are not
+ * recorded).  RNNT_ERR_INVALID_ARG if capacity < 1 or a session
  * is already open; RNNT_ERR_CUDA if the events cannot be created. */
 rnnt_status rnnt_profile_start(int capacity);
 
@@ -30,8 +31,8 @@ rnnt_status rnnt_profile_start(int capacity);
 int rnnt_profile_stop(void);
 
 /* Entry i (0 <= i < the count rnnt_profile_stop returned) of the last
- * closed session: kernel name (static string), total milliseconds and the
- * number of timed launches.  RNNT_ERR_INVALID_ARG if i is out of range. */
+ * closed session: step name (static string), total milliseconds and the
+ * number of kernel launches its brackets held.  RNNT_ERR_INVALID_ARG if i is out of range. */
 rnnt_status rnnt_profile_entry(int i, const char** name, double* total_ms, int* launches);
 
 #ifdef __cplusplus

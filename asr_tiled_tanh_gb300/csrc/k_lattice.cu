@@ -242,6 +242,22 @@ __device__ __forceinline__ float lae(float a, float b) {
   return m + log1pf(expf(d));
 }
 
+// log-add-exp of the shared-memory kernel: on the fast path its arguments
+// are base-2 logarithms (both -inf: min - max is NaN, clamped to -126, and
+// the result is max = -inf).
+template <bool FAST>
+__device__ __forceinline__ float lae_k(float a, float b) {
+  if (FAST) {
+    const float m = fmaxf(a, b);
+    const float d = fmaxf(fminf(a, b) - m, -126.f);
+    float e, l;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(d));
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + e));
+    return m + l;
+  }
+  return lae<false>(a, b);
+}
+
 template <int NJ, int PF, bool FAST>
 __global__ void __launch_bounds__(64)
 k_alpha_beta(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
@@ -416,17 +432,18 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
   cp_async_wait<1>();
   __syncwarp();
 
-  float own[NJ], send[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
+  // The fast path runs the recursion on base-2 logarithms: inputs are scaled
+  // by log2 e as they are read, results by ln 2 as they are stored, so the
+  // log-add-exp on the dependency chain is max + lg2(1 + 2^(min - max)).
+  constexpr float kIn = FAST ? 1.4426950408889634f : 1.f;
+  constexpr float kOut = FAST ? 0.6931471805599453f : 1.f;
   const int u0 = NJ * lane;
-
-#pragma unroll 2
-  for (int s = 0; s < ndiag; ++s) {
-    const int d = is_beta ? ndiag - 1 - s : s;
+  // window bookkeeping for diagonal d: the window holding its last (alpha)
+  // or first (beta) row is complete, the one after it is in flight
+  auto need = [&](int d) {
     if (!is_beta) {
       const int hi = min(d, Tb - 1) >> 5;
-      if (hi > ready) {  // entering window `hi`, loaded one ahead
+      if (hi > ready) {
         if (next_win < nwin) { load_window(next_win); ++next_win; } else cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();
@@ -440,6 +457,37 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
         __syncwarp();
         ready = lo;
       }
+    }
+  };
+  // the (scaled) blank and label log-probs of this lane's positions on
+  // diagonal d; -inf off the lattice
+  auto fetch = [&](int d, float (&lb)[NJ], float (&ll)[NJ]) {
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int u = u0 + j, t = d - u;
+      const bool in = u <= Ub && t >= 0 && t < Tb;
+      const int off = (t & rmask) * U1 + min(u, U1 - 1);  // always inside the ring
+      lb[j] = in ? ring[off] * kIn : -INFINITY;
+      ll[j] = in ? ring[off + plane] * kIn : -INFINITY;
+    }
+  };
+
+  float own[NJ], send[NJ], lbn[NJ], lln[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
+  fetch(is_beta ? ndiag - 1 : 0, lbn, lln);
+
+#pragma unroll 2
+  for (int s = 0; s < ndiag; ++s) {
+    const int d = is_beta ? ndiag - 1 - s : s;
+    float lb[NJ], ll[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) { lb[j] = lbn[j]; ll[j] = lln[j]; }
+    // the next diagonal's inputs are read while this one is computed
+    if (s + 1 < ndiag) {
+      const int dn = is_beta ? d - 1 : d + 1;
+      need(dn);
+      fetch(dn, lbn, lln);
     }
     // neighbours from the previous diagonal
     float nb[NJ];
@@ -458,21 +506,18 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
     for (int j = 0; j < NJ; ++j) {
       const int u = u0 + j, t = d - u;
       const bool in = u <= Ub && t >= 0 && t < Tb;
-      const int off = (t & rmask) * U1 + min(u, U1 - 1);  // always inside the ring
-      const float lb = in ? ring[off] : -INFINITY;
-      const float ll = in ? ring[off + plane] : -INFINITY;
       float val;
       if (!is_beta) {
-        val = (s == 0) ? 0.f : lae<FAST>(own[j], nb[j]);
+        val = (s == 0) ? 0.f : lae_k<FAST>(own[j], nb[j]);
       } else {
         const float from_t = (t + 1 < Tb) ? own[j] : (u == Ub ? 0.f : -INFINITY);
-        val = lae<FAST>(from_t + lb, nb[j] + ll);
+        val = lae_k<FAST>(from_t + lb[j], nb[j] + ll[j]);
       }
       val = in ? val : -INFINITY;
-      if (in) OUT[(size_t)t * U1 + u] = val;
+      if (in) OUT[(size_t)t * U1 + u] = val * kOut;
       if (!is_beta) {
-        own[j] = val + lb;
-        send[j] = val + ll;
+        own[j] = val + lb[j];
+        send[j] = val + ll[j];
       } else {
         own[j] = val;
         send[j] = val;
@@ -484,13 +529,12 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       if (u0 + j == Ub) {
-        sv.lnP[b] = own[j];
-        loss[b] = -own[j];
+        sv.lnP[b] = own[j] * kOut;
+        loss[b] = -own[j] * kOut;
       }
     }
   }
 }
-
 template <bool FAST>
 static cudaError_t launch_ab(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
                              SavedView sv, float* loss, cudaStream_t s) {

@@ -364,13 +364,56 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
   return st;
 }
 
-// dh of 32 columns; the warp's 32 rows are written as bf16 to rows
-// wrow0 .. +31 of the dh buffer (0 for positions outside the lattice); when
-// dbO is given, the rows are also summed per column through the warp's
-// scratch and added to dbO.  bb: the 32 bias values.  All lanes take part.
+// Column sums of the warp's 32 x 32 block (lane = row, d = its 32 columns)
+// added to dst[col0 ..]: the block is halved five times across lanes (lane
+// bit 4 keeps columns 16..31, bit 3 the upper 8 of those, ...), so that 36
+// shuffles leave lanes 4k..4k+3 all holding the sums of columns 4k..4k+3;
+// lane 4k adds them with one vector reduction.  Columns >= N are skipped (N
+// is a multiple of 8).  dst must be 16-byte aligned.
+__device__ __forceinline__ void colsum32_red(const float (&d)[32], float* dst, int col0, int N) {
+  const int lane = threadIdx.x & 31;
+  float e[16];
+  const bool u16 = (lane & 16) != 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float send = u16 ? d[j] : d[j + 16];
+    const float keep = u16 ? d[j + 16] : d[j];
+    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  const bool u8 = (lane & 8) != 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float send = u8 ? e[j] : e[j + 8];
+    const float keep = u8 ? e[j + 8] : e[j];
+    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const bool u4 = (lane & 4) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float send = u4 ? e[j] : e[j + 4];
+    const float keep = u4 ? e[j + 4] : e[j];
+    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    e[j] += __shfl_xor_sync(0xffffffffu, e[j], 1);
+    e[j] += __shfl_xor_sync(0xffffffffu, e[j], 2);
+  }
+  const int c = col0 + (lane & 28);
+  if ((lane & 3) == 0 && c < N) ptx::red_add_v4(dst + c, e[0], e[1], e[2], e[3]);
+}
+
+// dh of 32 columns (Eq. 10: softmax times the position's occupancy minus the
+// blank / label posteriors).  The warp's 32 rows are written as bf16 to rows
+// wrow0 .. +31 of the dh buffer by a TMA store from the warp's staging area
+// (32 rows x 64 bytes, 64-byte swizzle: lane r writes its 16-byte piece j at
+// piece j ^ ((r >> 1) & 3), which spreads every 8 lanes over all 32 banks);
+// rows outside the lattice are 0.  When dbO is given, the block's column sums
+// are added to it.  bb: the 32 bias values.  All lanes take part.
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
                                          float (&d)[32], const float* bb, int col0,
-                                         long long wrow0, float* wscr, bool write) {
+                                         long long wrow0, unsigned char* stg,
+                                         const CUtensorMap* tmC, bool write) {
   // d holds the chunk's scores on entry and dh on exit
   const int nv = min(32, p.N - col0);
   if (rc.valid) {
@@ -398,36 +441,22 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
     for (int j = 0; j < 32; ++j) d[j] = 0.f;
   }
   const int lane = threadIdx.x & 31;
-  if (p.dbO) {
-    // column sums of the warp's 32 rows, 16 columns at a time through the
-    // warp's scratch: lane = (column c, row half h)
-    const int c = lane & 15, h = lane >> 4;
+  if (p.dbO) colsum32_red(d, p.dbO, col0, p.N);
+  if (write && col0 < p.N) {  // (no store box starts past the last column)
+    uint4 q[4];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int i = 0; i < 4; ++i) q[i] = pack8_bf16(d + 8 * i);
+    // the previous store from this staging area has been read out
+    if (lane == 0) ptx::bulk_wait_read();
+    __syncwarp();
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = d[half * 16 + j];
-      __syncwarp();
-      float cs = 0.f;
-#pragma unroll
-      for (int r = 0; r < 16; ++r) cs += wscr[(h * 16 + r) * 17 + c];
-      cs += __shfl_xor_sync(0xffffffffu, cs, 16);
-      const int col = col0 + half * 16 + c;
-      if (h == 0 && col < p.N && cs != 0.f) ptx::red_add_f32(p.dbO + col, cs);
-      __syncwarp();
-    }
-  }
-  if (write) {
-    __nv_bfloat16* gbase = p.Hout + wrow0 * p.N + col0;
-    if (nv == 32 && (p.N & 7) == 0) {
-      uint4 q[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = pack8_bf16(d + 8 * i);
-      store_rows_bf16((unsigned char*)wscr, q, gbase, p.N, true);
-    } else {
-      __nv_bfloat16* dst = gbase + (long long)lane * p.N;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nv) dst[j] = __float2bfloat16_rn(d[j]);
+    for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * 64 + ((i ^ sw) << 4)) = q[i];
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmC, stg, col0, (int)wrow0);
+      ptx::bulk_commit();
     }
   }
 }
@@ -435,7 +464,7 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
 template <int BN, int A_MN, int B_MN, int EPI, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-          const TcParams p) {
+          const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using C = Cfg<BN>;
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
   static_assert(!B_MN || BN / 64 >= CL, "each CTA of a cluster loads whole 64-column B boxes");
@@ -709,8 +738,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             lse_chunk(ls, p, rc, v, bb, col0,
                       p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
           } else if constexpr (EPI == EPI_DH) {
-            dh_chunk(ds, p, rc, v, bb, col0, (long long)w.m * BM + sub * 32, wscr,
-                     w.m < p.ch.ntiles);
+            dh_chunk(ds, p, rc, v, bb, col0, (long long)w.m * BM + sub * 32,
+                     (unsigned char*)wscr, &tmC, w.m < p.ch.ntiles);
           } else if constexpr (EPI == EPI_DA) {
             // da = dz (1 - z^2) on the thread's own row, then 16-column halves
             // of the warp's 32 x 32 block are transposed through the warp's
@@ -827,6 +856,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
       }
     }
+    // the dh stores issued by this warp are complete before the CTA ends
+    if (EPI == EPI_DH && lane == 0) ptx::bulk_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -844,36 +875,48 @@ namespace rnnt {
 namespace {
 
 // z rows of a chunk in bf16: tanh(pA[b,t] + pL[b,u]) (joint network, Eq. 3-4),
-// 0 on rows outside the lattice.  One block per tile, 8 consecutive h per thread.
+// 0 on rows outside the lattice.  One block per tile; a thread item is one
+// frame t of the tile and 8 consecutive h: the frame's pA values are loaded
+// once and combined with the tile's 8 label positions (their pL rows stay in
+// L1 for the whole block), so L2 serves 48 KB of projections per 128 KB tile
+// of z (H = 512) instead of 512 KB.
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
-  // block (x = tile, y = quarter of its 128 rows)
   __shared__ TileRef tr;
   if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
   __syncthreads();
   const int H = c.sh.H;
   const int H8 = H / 8;
-  const int r0 = blockIdx.y * (TILE / 4);
   const long long row0 = (long long)blockIdx.x * TILE;
-#pragma unroll 4
-  for (int e = threadIdx.x; e < (TILE / 4) * H8; e += blockDim.x) {
-    const int i = r0 + e / H8, k8 = (e % H8) * 8;
-    const RowCell rc = row_of(tr, i);
-    uint4 out = make_uint4(0, 0, 0, 0);
-    if (rc.valid) {
-      const float4* a = (const float4*)(pA + ((size_t)rc.b * c.sh.T + rc.t) * H + k8);
-      const float4* l = (const float4*)(pL + ((size_t)rc.b * c.sh.U1 + rc.u) * H + k8);
-      const float4 a0 = a[0], a1 = a[1], l0 = l[0], l1 = l[1];
-      // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
-      using ptx::tanh_approx;
-      using ptx::pack_bf16x2;
-      out.x = pack_bf16x2(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
-      out.y = pack_bf16x2(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
-      out.z = pack_bf16x2(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
-      out.w = pack_bf16x2(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
+  using ptx::pack_bf16x2;
+  using ptx::tanh_approx;
+  for (int e = threadIdx.x; e < TT * H8; e += blockDim.x) {
+    const int ti = e / H8, k8 = (e % H8) * 8;
+    const int t = tr.t0 + ti;
+    const bool t_ok = tr.exists && t < tr.Tb;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    if (t_ok) {
+      const float4* a = (const float4*)(pA + ((size_t)tr.b * c.sh.T + t) * H + k8);
+      a0 = a[0];
+      a1 = a[1];
     }
-    *(uint4*)(Z + (row0 + i) * H + k8) = out;
+    __nv_bfloat16* zrow = Z + (row0 + ti * TU) * H + k8;
+#pragma unroll
+    for (int ui = 0; ui < TU; ++ui) {
+      const int u = tr.u0 + ui;
+      uint4 out = make_uint4(0, 0, 0, 0);
+      if (t_ok && u <= tr.Ub) {
+        const float4* l = (const float4*)(pL + ((size_t)tr.b * c.sh.U1 + u) * H + k8);
+        const float4 l0 = l[0], l1 = l[1];
+        // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
+        out.x = pack_bf16x2(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
+        out.y = pack_bf16x2(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
+        out.z = pack_bf16x2(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
+        out.w = pack_bf16x2(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
+      }
+      *(uint4*)(zrow + (long long)ui * H) = out;
+    }
   }
 }
 
@@ -1099,6 +1142,21 @@ bool make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, 
   return r == CUDA_SUCCESS;
 }
 
+// Store map of a row-major bf16 matrix [rows][cols]: 32 x 32 boxes (one
+// epilogue warp's block), 64-byte swizzle.
+bool make_tmap_store32(CUtensorMap* m, const void* ptr, long long rows, long long cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // One GEMM: C-shaped problem M x N x K with A = [M][K] (a_mn = 0) or [K][M]
 // (a_mn = 1) and B = [N][K] (b_mn = 0) or [K][N] (b_mn = 1), all bf16.
 struct GemmDesc {
@@ -1118,6 +1176,10 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   const bool ok_b =
       BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN / CL);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+  // dh epilogue: the store map of the dh buffer [M][N]; the other epilogues
+  // never read the third map
+  CUtensorMap tc = ta;
+  if (EPI == EPI_DH && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
   static int max_clusters = -1;  // per instantiation
   if (max_clusters < 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1159,7 +1221,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
   const int grid_groups = std::min(groups, cap);
   if (CL == 1) {
-    kern<<<grid_groups, NTHREADS, C::SMEM, s>>>(ta, tb, p);
+    kern<<<grid_groups, NTHREADS, C::SMEM, s>>>(ta, tb, tc, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1174,7 +1236,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 
 // Cluster size used for a GEMM: CTAs of a cluster share B tiles over TMA
@@ -1331,7 +1393,7 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     {
       ProfScope ps("tc_build_z", s);
-      k_build_z_bf16<<<dim3((unsigned)c.ntiles, 4), 256, 0, s>>>(c, pA, pL, Z);
+      k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
       if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
     }
     ProfScope ps("tc_fwd_tiles", s);
@@ -1363,7 +1425,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
     if (!untiled) {
       {
         ProfScope ps("tc_build_z", s);
-        k_build_z_bf16<<<dim3((unsigned)c.ntiles, 4), 256, 0, s>>>(c, pA, pL, Z);
+        k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
         if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
       }
       {
@@ -1386,13 +1448,17 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.n_split = (int)std::max<long long>(1, std::min<long long>(
                        4, cdiv(4LL * num_sms(), std::max<long long>(1, p.chunk_tiles))));
       tp.status = sv.status;
+      // db^O: column sums of dh formed in the same epilogue (vector
+      // reductions need a 16-byte aligned db^O)
+      if (dbO && ((uintptr_t)dbO & 15) == 0) tp.dbO = dbO;
       if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
       ProfScope ps("tc_dh_kept", s);
       k_dh_rows_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, Hs, grad_loss);
       if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
     }
-    if (dbO) {  // (right after dh is written, while it is warm in L2) db^O += sum over the chunk's positions of dh (rows outside are 0)
+    if (dbO && (untiled || ((uintptr_t)dbO & 15) != 0)) {
+      // db^O += sum over the chunk's positions of dh (rows outside are 0)
       ProfScope ps("tc_colsum_dh", s);
       if (launch_colsum_bf16(Hs, rows, p.V, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }

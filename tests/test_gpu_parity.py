@@ -73,6 +73,28 @@ def test_bf16_ragged_shapes_with_biases():
     assert_parity(gpu, orc, inp)
 
 
+def test_unaligned_output_bias_gradient():
+    # db^O at an address that is not 16-byte aligned: the column sums of dh
+    # then take the separate pass instead of the dh epilogue's vector adds
+    inp = synthetic.custom(B=6, T=45, U=13, HA=64, HL=192, H=128, V=320, dtype="bf16", seed=7,
+                           t_frac=0.1, u_frac=0.0, bias_std=0.3)
+    dev = to_device(inp)
+    r = rn.Rnnt.for_inputs(inp)
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    r.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    g = r.alloc_grads()
+    backing = torch.zeros(inp.wl.V + 1, dtype=torch.float32, device="cuda")
+    g["dbO"] = backing[1:]
+    assert g["dbO"].data_ptr() % 16 != 0
+    r.bwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"], grads=g)
+    torch.cuda.synchronize()
+    orc = run_oracle(inp)
+    assert rel_l2(g["dbO"].cpu().numpy(), orc.grads["dbO"]) < 1e-2
+    aligned = run_gpu(inp, keep_saved=False)
+    assert rel_l2(aligned["dbO"], orc.grads["dbO"]) < 1e-2
+    assert rel_l2(g["dbO"].cpu().numpy(), aligned["dbO"]) < 1e-2
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
     # Flash RNN-T: tiled and untiled execution compute the same thing.  The

@@ -25,6 +25,7 @@
 
 #include "kernels.h"
 #include "profile.h"
+#include "streams.h"
 #include "tc.h"
 
 using namespace rnnt;
@@ -181,11 +182,11 @@ ChunkArgs chunk_args(const Plan& p, const SavedView& sv, long long k, const int3
 
 // Projections pA = hA W^A^T + b^Z [B*T,H] and pL = hL W^L^T [B*U1,H], fp32.
 rnnt_status projections(const Plan& p, const void* hA, const void* hL, const rnnt_params* pr,
-                        float* pA, float* pL, cudaStream_t st) {
+                        float* pA, float* pL, cudaStream_t st, cudaStream_t st_l) {
   const int bf = p.dtype == RNNT_BF16;
   if (p.tc) {
     RNNT_CHECK(tc_projection(p, hA, pr->WA, pr->bZ, p.B * p.T, p.HA, pA, st));
-    RNNT_CHECK(tc_projection(p, hL, pr->WL, nullptr, p.B * p.U1, p.HL, pL, st));
+    RNNT_CHECK(tc_projection(p, hL, pr->WL, nullptr, p.B * p.U1, p.HL, pL, st_l));
     return RNNT_OK;
   }
   SimtGemm g{};
@@ -283,10 +284,14 @@ const char* rnnt_status_string(rnnt_status s) {
   return "unknown status";
 }
 
-rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
-                     const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
-                     const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
-                     rnnt_stream stream) {
+}  // extern "C"
+
+// The forward pass; side_streams = false keeps every launch on `stream`
+// (the no-allocation entry point creates no streams).
+rnnt_status rnnt::fwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
+                          const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                          const int32_t* U_len, float* loss, void* saved, void* ws,
+                          size_t ws_bytes, rnnt_stream stream, bool side_streams) {
   Plan p;
   rnnt_status st0 = check_common(dims, hA, hL, pr, labels, T_len, U_len, saved, ws, ws_bytes, &p);
   if (st0 != RNNT_OK) return st0;
@@ -298,16 +303,21 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
   float* pA = (float*)((char*)saved + p.s_pA);
   float* pL = (float*)((char*)saved + p.s_pL);
 
-  LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
-  if (p.B == 0) return RNNT_OK;
-  LAUNCH("tile_table", launch_tile_table(sh, T_len, U_len, sv, st));
-  const size_t ncell = (size_t)p.B * p.T * p.U1;
-  // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
-  (void)ncell;
-  LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY,
-                                     (p.s_beta - p.s_lpb) / 4 + (size_t)p.B * p.T * p.U1, st));
-  rnnt_status s = projections(p, hA, hL, pr, pA, pL, st);
-  if (s != RNNT_OK) return s;
+  rnnt_status s;
+  {
+    // the two joint projections run beside the index, tile table and fill
+    // (they read only the inputs and write only pA, pL)
+    Fork fork(st, side_streams && p.tc && p.B > 0 ? 2 : 0);
+    LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
+    if (p.B == 0) return RNNT_OK;
+    s = projections(p, hA, hL, pr, pA, pL, fork.side(0), fork.side(1));
+    if (s != RNNT_OK) return s;
+    LAUNCH("tile_table", launch_tile_table(sh, T_len, U_len, sv, st));
+    // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
+    LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY,
+                                       (p.s_beta - p.s_lpb) / 4 + (size_t)p.B * p.T * p.U1, st));
+    RNNT_CHECK(fork.join());
+  }
 
   const bool untiled = p.mode == RNNT_UNTILED;
   void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
@@ -330,6 +340,16 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
   }
   LAUNCH("alpha_beta", launch_alpha_beta(sh, T_len, U_len, sv, loss, p.tc, st));
   return RNNT_OK;
+}
+
+extern "C" {
+
+rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
+                     rnnt_stream stream) {
+  return rnnt::fwd_impl(dims, hA, hL, pr, labels, T_len, U_len, loss, saved, ws, ws_bytes,
+                        stream, true);
 }
 
 rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,

@@ -385,25 +385,24 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int NJ, bool FAST>
-__global__ void __launch_bounds__(32)
-k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
-                  SavedView sv, float* __restrict__ loss, int R) {
-  extern __shared__ float ring[];  // [lpb | lpl] x R rows x U1
-  const int b = blockIdx.x;
-  const bool is_beta = blockIdx.y != 0;
+// One direction of the recursion for one sample (one warp).  The per-lane
+// state advances by increments from one diagonal to the next: position j's
+// frame t, its row in the ring and its offset in the output array.
+template <int NJ, bool FAST, bool BETA>
+__device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int U1,
+                                        const float* __restrict__ LPB,
+                                        const float* __restrict__ LPL, float* __restrict__ OUT,
+                                        float* lnP, float* loss) {
   const int lane = threadIdx.x;
-  if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample
-  const int Tb = T_len[b], Ub = U_len[b];
-  const int U1 = sh.U1;
-  const size_t base = (size_t)b * sh.T * U1;
-  const float* __restrict__ LPB = sv.lpb + base;
-  const float* __restrict__ LPL = sv.lpl + base;
-  float* __restrict__ OUT = (is_beta ? sv.beta : sv.alpha) + base;
-  const int ndiag = Tb + Ub;
   const int plane = R * U1;
   const int rmask = R - 1;
   const int nwin = (Tb + AB_W - 1) / AB_W;
+  const int ndiag = Tb + Ub;
+  // The fast path runs the recursion on base-2 logarithms: inputs are scaled
+  // by log2 e as they are read, results by ln 2 as they are stored, so the
+  // log-add-exp on the dependency chain is max + lg2(1 + 2^(min - max)).
+  constexpr float kIn = FAST ? 1.4426950408889634f : 1.f;
+  constexpr float kOut = FAST ? 0.6931471805599453f : 1.f;
 
   auto load_window = [&](int w) {  // rows [w*32, w*32+32) of lpb and lpl
     const int r0 = w * AB_W, r1 = min(Tb, r0 + AB_W);
@@ -418,7 +417,7 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
     cp_async_commit();
   };
   int next_win, ready;  // next window to load; window known complete
-  if (!is_beta) {
+  if (!BETA) {
     load_window(0);
     if (nwin > 1) load_window(1); else cp_async_commit();
     next_win = 2;
@@ -432,18 +431,28 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
   cp_async_wait<1>();
   __syncwarp();
 
-  // The fast path runs the recursion on base-2 logarithms: inputs are scaled
-  // by log2 e as they are read, results by ln 2 as they are stored, so the
-  // log-add-exp on the dependency chain is max + lg2(1 + 2^(min - max)).
-  constexpr float kIn = FAST ? 1.4426950408889634f : 1.f;
-  constexpr float kOut = FAST ? 0.6931471805599453f : 1.f;
   const int u0 = NJ * lane;
-  // window bookkeeping for diagonal d: the window holding its last (alpha)
-  // or first (beta) row is complete, the one after it is in flight
-  auto need = [&](int d) {
-    if (!is_beta) {
+  const int d0 = BETA ? ndiag - 1 : 0;
+  int t[NJ], ri[NJ], oo[NJ];
+  bool uok[NJ], ulast[NJ];
+  float own[NJ], send[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int u = u0 + j;
+    uok[j] = u <= Ub;
+    ulast[j] = u == Ub;
+    t[j] = d0 - u;
+    ri[j] = (t[j] & rmask) * U1 + min(u, U1 - 1);  // always inside the ring
+    oo[j] = t[j] * U1 + u;
+    own[j] = send[j] = -INFINITY;
+  }
+
+#pragma unroll 2
+  for (int s = 0; s < ndiag; ++s) {
+    const int d = BETA ? ndiag - 1 - s : s;
+    if (!BETA) {
       const int hi = min(d, Tb - 1) >> 5;
-      if (hi > ready) {
+      if (hi > ready) {  // entering window `hi`, loaded one ahead
         if (next_win < nwin) { load_window(next_win); ++next_win; } else cp_async_commit();
         cp_async_wait<1>();
         __syncwarp();
@@ -458,40 +467,9 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
         ready = lo;
       }
     }
-  };
-  // the (scaled) blank and label log-probs of this lane's positions on
-  // diagonal d; -inf off the lattice
-  auto fetch = [&](int d, float (&lb)[NJ], float (&ll)[NJ]) {
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int u = u0 + j, t = d - u;
-      const bool in = u <= Ub && t >= 0 && t < Tb;
-      const int off = (t & rmask) * U1 + min(u, U1 - 1);  // always inside the ring
-      lb[j] = in ? ring[off] * kIn : -INFINITY;
-      ll[j] = in ? ring[off + plane] * kIn : -INFINITY;
-    }
-  };
-
-  float own[NJ], send[NJ], lbn[NJ], lln[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) own[j] = send[j] = -INFINITY;
-  fetch(is_beta ? ndiag - 1 : 0, lbn, lln);
-
-#pragma unroll 2
-  for (int s = 0; s < ndiag; ++s) {
-    const int d = is_beta ? ndiag - 1 - s : s;
-    float lb[NJ], ll[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) { lb[j] = lbn[j]; ll[j] = lln[j]; }
-    // the next diagonal's inputs are read while this one is computed
-    if (s + 1 < ndiag) {
-      const int dn = is_beta ? d - 1 : d + 1;
-      need(dn);
-      fetch(dn, lbn, lln);
-    }
     // neighbours from the previous diagonal
     float nb[NJ];
-    if (!is_beta) {
+    if (!BETA) {
       const float x = __shfl_up_sync(0xffffffffu, send[NJ - 1], 1);
       nb[0] = lane == 0 ? -INFINITY : x;
 #pragma unroll
@@ -504,37 +482,65 @@ k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __
     }
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      const int u = u0 + j, t = d - u;
-      const bool in = u <= Ub && t >= 0 && t < Tb;
+      const bool in = uok[j] && (unsigned)t[j] < (unsigned)Tb;
+      const float lb = in ? ring[ri[j]] * kIn : -INFINITY;
+      const float ll = in ? ring[ri[j] + plane] * kIn : -INFINITY;
       float val;
-      if (!is_beta) {
+      if (!BETA) {
         val = (s == 0) ? 0.f : lae_k<FAST>(own[j], nb[j]);
       } else {
-        const float from_t = (t + 1 < Tb) ? own[j] : (u == Ub ? 0.f : -INFINITY);
-        val = lae_k<FAST>(from_t + lb[j], nb[j] + ll[j]);
+        const float from_t = (t[j] + 1 < Tb) ? own[j] : (ulast[j] ? 0.f : -INFINITY);
+        val = lae_k<FAST>(from_t + lb, nb[j] + ll);
       }
       val = in ? val : -INFINITY;
-      if (in) OUT[(size_t)t * U1 + u] = val * kOut;
-      if (!is_beta) {
-        own[j] = val + lb[j];
-        send[j] = val + ll[j];
+      if (in) OUT[oo[j]] = val * kOut;
+      if (!BETA) {
+        own[j] = val + lb;   // alpha + lpb: the blank move to (t+1, u)
+        send[j] = val + ll;  // alpha + lpl: the label move to (t, u+1)
+        ++t[j];
+        ri[j] += U1;
+        if (ri[j] >= plane) ri[j] -= plane;
+        oo[j] += U1;
       } else {
         own[j] = val;
         send[j] = val;
+        --t[j];
+        ri[j] -= U1;
+        if (ri[j] < 0) ri[j] += plane;
+        oo[j] -= U1;
       }
     }
   }
   cp_async_wait<0>();
-  if (!is_beta) {
+  if (!BETA) {
+    // ln P = alpha(T_b-1, U_b) + lpb(T_b-1, U_b): the own value at u = U_b
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      if (u0 + j == Ub) {
-        sv.lnP[b] = own[j] * kOut;
-        loss[b] = -own[j] * kOut;
+      if (ulast[j]) {
+        *lnP = own[j] * kOut;
+        *loss = -own[j] * kOut;
       }
     }
   }
 }
+
+template <int NJ, bool FAST>
+__global__ void __launch_bounds__(32)
+k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
+                  SavedView sv, float* __restrict__ loss, int R) {
+  extern __shared__ float ring[];  // [lpb | lpl] x R rows x U1
+  const int b = blockIdx.x;
+  if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample
+  const int Tb = T_len[b], Ub = U_len[b];
+  const size_t base = (size_t)b * sh.T * sh.U1;
+  if (blockIdx.y == 0)
+    ab_walk<NJ, FAST, false>(ring, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                             sv.alpha + base, sv.lnP + b, loss + b);
+  else
+    ab_walk<NJ, FAST, true>(ring, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                            sv.beta + base, nullptr, nullptr);
+}
+
 template <bool FAST>
 static cudaError_t launch_ab(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
                              SavedView sv, float* loss, cudaStream_t s) {

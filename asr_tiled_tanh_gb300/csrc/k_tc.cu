@@ -27,6 +27,7 @@
 
 #include "kernels.h"
 #include "profile.h"
+#include "streams.h"
 #include "ptx.cuh"
 #include "tc.h"
 #include "../../include/rnnt_testing.h"
@@ -1498,40 +1499,31 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
   __nv_bfloat16* hAm = (__nv_bfloat16*)(ws + p.w_hAm);
   __nv_bfloat16* hLm = (__nv_bfloat16*)(ws + p.w_hLm);
   const size_t nA = (size_t)p.B * p.T * p.H, nL = (size_t)p.B * p.U1 * p.H;
+  // Two phases of independent launches, each spread over side streams: the
+  // bf16 operands, then the four encoder-side GEMMs and db^Z.
   {
     ProfScope ps("tc_enc_prep", s);
     ps.set_kernels(2 + (dWA ? 1 : 0) + (dWL ? 1 : 0));
+    Fork fork(s, 3);
     k_f32_to_bf16<<<elementwise_grid(nA), 256, 0, s>>>(dA, dA16, nA);
-    k_f32_to_bf16<<<elementwise_grid(nL), 256, 0, s>>>(dLr, dLr16, nL);
+    k_f32_to_bf16<<<elementwise_grid(nL), 256, 0, fork.side(0)>>>(dLr, dLr16, nL);
     if (dWA) {
       const size_t n = (size_t)p.B * p.T * p.HA;
-      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, s>>>((const __nv_bfloat16*)hA, hAm, p.B,
-                                                           p.T, p.HA, Teff);
+      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, fork.side(1)>>>(
+          (const __nv_bfloat16*)hA, hAm, p.B, p.T, p.HA, Teff);
     }
     if (dWL) {
       const size_t n = (size_t)p.B * p.U1 * p.HL;
-      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, s>>>((const __nv_bfloat16*)hL, hLm, p.B,
-                                                           p.U1, p.HL, Ueff);
+      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, fork.side(2)>>>(
+          (const __nv_bfloat16*)hL, hLm, p.B, p.U1, p.HL, Ueff);
     }
     if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
   }
   ProfScope ps("tc_enc_grads", s);
   ps.set_kernels((dhA ? 1 : 0) + (dhL ? 1 : 0) + (dWA ? 1 : 0) + (dWL ? 1 : 0) + (dbZ ? 1 : 0));
+  Fork fork(s, 3);
   const int MA = p.B * p.T, ML = p.B * p.U1;
-  if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
-    GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};
-    TcParams tp{};
-    tp.C = dhA;
-    tp.ldc = p.HA;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), 1, s) != cudaSuccess) return RNNT_ERR_CUDA;
-  }
-  if (dhL) {
-    GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
-    TcParams tp{};
-    tp.C = dhL;
-    tp.ldc = p.HL;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), 1, s) != cudaSuccess) return RNNT_ERR_CUDA;
-  }
   if (dWA) {  // dW^A = dA^T hA: A = dA16 as [K=MA][M=H], B = hAm as [K=MA][N=HA]
     GemmDesc g{dA16, 1, hAm, 1, p.H, p.HA, MA};
     TcParams tp{};
@@ -1541,6 +1533,22 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.ldc = p.HA;
     if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
+  if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
+    GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};
+    TcParams tp{};
+    tp.C = dhA;
+    tp.ldc = p.HA;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), 1, fork.side(0)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+  }
+  if (dhL) {
+    GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
+    TcParams tp{};
+    tp.C = dhL;
+    tp.ldc = p.HL;
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), 1, fork.side(1)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+  }
   if (dWL) {
     GemmDesc g{dLr16, 1, hLm, 1, p.H, p.HL, ML};
     TcParams tp{};
@@ -1548,12 +1556,14 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HL, bn)), ML);
     tp.C = dWL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
-  }
-  if (dbZ) {  // db^Z = sum of dA over frames (= sum of da over every position)
-    if (launch_colsum_f32v(dA, (long long)p.B * p.T, p.H, dbZ, s) != cudaSuccess)
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, fork.side(2)) != cudaSuccess)
       return RNNT_ERR_CUDA;
   }
+  if (dbZ) {  // db^Z = sum of dA over frames (= sum of da over every position)
+    if (launch_colsum_f32v(dA, (long long)p.B * p.T, p.H, dbZ, fork.side(1)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+  }
+  if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
   return RNNT_OK;
 }
 

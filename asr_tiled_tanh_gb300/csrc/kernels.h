@@ -69,4 +69,12 @@ cudaError_t launch_da_reduce(const ChunkArgs& c, const float* dZ, const void* Z,
 cudaError_t launch_colsum(const float* X, long long R, int N, long long ld, float* out,
                           cudaStream_t s);
 
+// ---- the forward pass behind rnnt_fwd (api.cu) ----------------------------
+// side_streams: run the independent launches on side streams (false: every
+// launch on `stream`, and no stream is ever created).
+rnnt_status fwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
+                     const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                     const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
+                     rnnt_stream stream, bool side_streams);
+
 }  // namespace rnnt

@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "../../include/rnnt.h"
+#include "kernels.h"
 #include <cuda_runtime.h>
 
 namespace {
@@ -56,6 +57,7 @@ extern "C" rnnt_status rnnt_fwd_noalloc(const rnnt_dims* dims, const void* hA, c
   if (s != RNNT_OK) return s;
   // The forward overwrites every scratch byte it reads, so nothing left over
   // from an earlier call has to be cleared first.
-  return rnnt_fwd(dims, hA, hL, params, labels, T_len, U_len, loss, saved, ws, kScratchBytes,
-                  stream);
+  // (all on `stream`: the plain forward's side streams are not created here)
+  return rnnt::fwd_impl(dims, hA, hL, params, labels, T_len, U_len, loss, saved, ws,
+                        kScratchBytes, stream, false);
 }

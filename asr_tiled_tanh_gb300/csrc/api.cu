@@ -383,7 +383,8 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
     LAUNCH("zero", launch_zero_many(z0, st));
     return RNNT_OK;
   }
-  {
+  // zero the accumulated outputs (one launch) and clamp the lengths
+  auto prepare = [&](cudaStream_t st) -> rnnt_status {
     ZeroList z{};
     void* ps[7] = {dWO, dbO, dbZ, dA, dLr, dWA, dWL};
     size_t bs[7] = {sizeof(float) * (size_t)p.V * p.H, sizeof(float) * (size_t)p.V,
@@ -392,21 +393,26 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                     sizeof(float) * (size_t)p.H * p.HL};
     for (int i = 0; i < 7; ++i) { z.p[z.n] = ps[i]; z.bytes[z.n] = bs[i]; ++z.n; }
     LAUNCH("zero", launch_zero_many(z, st));
-  }
-  LAUNCH("eff_lengths", launch_eff_lengths(shape_of(p), sv, T_len, U_len, Teff, Ueff, st));
+    LAUNCH("eff_lengths", launch_eff_lengths(shape_of(p), sv, T_len, U_len, Teff, Ueff, st));
+    return RNNT_OK;
+  };
 
   rnnt_status s;
   void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
 
   if (p.tc) {
+    // (the preparation runs beside the first chunk's z rebuild)
+    const PreLaunch pre = prepare;
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), st);
+                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, st);
     if (s != RNNT_OK) return s;
     s = tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ, st);
     return s;
   }
 
+  s = prepare(st);
+  if (s != RNNT_OK) return s;
   long long nch = 0;
   s = chunk_count(p, sv, st, &nch);
   if (s != RNNT_OK) return s;

@@ -38,9 +38,7 @@ namespace {
 
 constexpr int BM = 128;              // rows per tile (TMEM lanes)
 constexpr int BK = 64;               // K per stage: one 128-byte swizzle atom of bf16
-constexpr int NTHREADS = 320;
-constexpr int EPI_WARP0 = 2;         // first of 8 epilogue warps (two per TMEM lane quarter)
-constexpr int EPI_THREADS = 256;
+constexpr int EPI_WARP0 = 2;         // first epilogue warp
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait, then give up
 constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
 
@@ -75,13 +73,30 @@ struct TcParams {
   int skip_first_fill;         // test hook: the producer never fills the first stage
 };
 
-template <int BN>
+// Epilogue warps of a kernel, four per TMEM lane quarter for the scores
+// (LSE) epilogue and three for the dh epilogue, whose per-element work would
+// otherwise hold the MMAs back (the dh epilogue needs the 128 registers a
+// thread gets in a 448-thread block; LSE fits the 96 of a 576-thread one);
+// two per quarter for the others.
+template <int EPI>
+constexpr int epi_warps() {
+  return EPI == EPI_LSE ? 16 : (EPI == EPI_DH ? 12 : 8);
+}
+
+template <int BN, int EPI>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int EPI_SCRATCH = 8 * WSCR_BYTES;     // per epilogue warp staging area
-  static constexpr int COMB_BYTES = 2 * 128 * 4 * 4;     // LSE halves, double-buffered
+  static constexpr int EW = epi_warps<EPI>();
+  static constexpr int PARTS = EW / 4;                   // warps per TMEM lane quarter
+  static constexpr int THREADS = 64 + 32 * EW;
+  // per epilogue warp staging area: none for LSE, a 32 x 64 B TMA-store box
+  // for dh, transposes / row staging for the others
+  static constexpr int WSCR = EPI == EPI_LSE ? 0 : (EPI == EPI_DH ? 2048 : WSCR_BYTES);
+  static constexpr int EPI_SCRATCH = EW * WSCR;
+  // LSE: partials of the other parts of each row, double-buffered
+  static constexpr int COMB_BYTES = EPI == EPI_LSE ? 2 * (PARTS - 1) * 128 * 4 * 4 : 0;
   static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_RAW =
       (SMEM_LIMIT - 1024 - EPI_SCRATCH - COMB_BYTES - BAR_BYTES) / STAGE;
@@ -111,10 +126,13 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     w.n0 = sp * per; w.n1 = min(p.n_tiles, w.n0 + per);
     w.kb0 = 0; w.kb1 = (w.n1 > w.n0) ? p.kb_total : 0;
   } else {
-    const int ks = rest % p.k_splits;
-    rest /= p.k_splits;
+    // N fastest, then M, then the K split: the clusters working at the same
+    // time share K ranges, so each K block of A and B is fetched from DRAM
+    // about once and served to the other units from L2
     const int n = rest % p.n_tiles;
-    const int mg = rest / p.n_tiles;
+    rest /= p.n_tiles;
+    const int mg = rest % p.m_groups;
+    const int ks = rest / p.m_groups;
     w.m = mg * CL + r;
     w.n0 = n; w.n1 = n + 1;
     w.kb0 = ks * p.kb_per_split;
@@ -410,9 +428,9 @@ __device__ __forceinline__ void colsum32_red(const float (&d)[32], float* dst, i
 // (32 rows x 64 bytes, 64-byte swizzle: lane r writes its 16-byte piece j at
 // piece j ^ ((r >> 1) & 3), which spreads every 8 lanes over all 32 banks);
 // rows outside the lattice are 0.  When dbO is given, the block's column sums
-// are added to it.  bb: the 32 bias values.  All lanes take part.
+// are added to it.  bq: the 32 bias values (packed bf16).  All lanes take part.
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
-                                         float (&d)[32], const float* bb, int col0,
+                                         float (&d)[32], const uint4 (&bq)[4], int col0,
                                          long long wrow0, unsigned char* stg,
                                          const CUtensorMap* tmC, bool write) {
   // d holds the chunk's scores on entry and dh on exit
@@ -422,7 +440,16 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
     // applied only to the (at most two) columns they belong to
     const float gg = st.gpb + st.gpl;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = gg * ptx::ex2(fmaf(d[j] + bb[j], kLog2e, -st.nl));
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w[4] = {bq[i].x, bq[i].y, bq[i].z, bq[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float& d0 = d[8 * i + 2 * k];
+        float& d1 = d[8 * i + 2 * k + 1];
+        d0 = gg * ptx::ex2(fmaf(d0 + ptx::bf16lo(w[k]), kLog2e, -st.nl));
+        d1 = gg * ptx::ex2(fmaf(d1 + ptx::bf16hi(w[k]), kLog2e, -st.nl));
+      }
+    }
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
     if (jb >= 0 && jb < 32) {
 #pragma unroll
@@ -442,7 +469,6 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
     for (int j = 0; j < 32; ++j) d[j] = 0.f;
   }
   const int lane = threadIdx.x & 31;
-  if (p.dbO) colsum32_red(d, p.dbO, col0, p.N);
   if (write && col0 < p.N) {  // (no store box starts past the last column)
     uint4 q[4];
 #pragma unroll
@@ -460,13 +486,15 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       ptx::bulk_commit();
     }
   }
+  // (after the store, so that the packed copy is no longer live)
+  if (p.dbO) colsum32_red(d, p.dbO, col0, p.N);
 }
 
 template <int BN, int A_MN, int B_MN, int EPI, int CL>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<BN, EPI>::THREADS, 1)
 k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
   static_assert(!B_MN || BN / 64 >= CL, "each CTA of a cluster loads whole 64-column B boxes");
   // CTAs of a cluster share each B stage: CTA r loads slice r and multicasts it
@@ -487,7 +515,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   uint64_t* acc_full = bars + 2 * STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
-  uint64_t* comb_bar = done_bar + 1;  // [2]: the second half's LSE partials are in `comb`
+  uint64_t* comb_bar = done_bar + 1;  // [2]: the other parts' LSE partials are in `comb`
   uint32_t* tmem_holder = (uint32_t*)(comb_bar + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
@@ -499,8 +527,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
-      ptx::mbar_init(&acc_empty[a], EPI_THREADS);
-      ptx::mbar_init(&comb_bar[a], 128);
+      ptx::mbar_init(&acc_empty[a], 32 * C::EW);
+      ptx::mbar_init(&comb_bar[a], 128 * (C::PARTS - 1 > 0 ? C::PARTS - 1 : 1));
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -638,14 +666,16 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps: warp w drains TMEM lane quarter (w & 3) and, of each
-    // accumulator's 32-column chunks, the even ones (first four warps) or the
-    // odd ones (last four).  The next chunk's tcgen05.ld is in flight while
-    // the current one is processed.
+    // EW warps: warp w drains TMEM lane quarter (w & 3) and, of each
+    // accumulator's 32-column chunks, those with c % PARTS == its part.  With
+    // two parts the next chunk's tcgen05.ld is in flight while the current one
+    // is processed; with more, the other warps of the quarter cover it.
+    constexpr int PARTS = C::PARTS;
+    constexpr bool DB = PARTS == 2;              // double-buffered TMEM loads
     const int sub = warp & 3;                    // TMEM lane quarter of this warp
-    const int hf = (warp - EPI_WARP0) >> 2;      // which chunks: c % 2 == hf
+    const int hf = (warp - EPI_WARP0) >> 2;      // part: chunks c % PARTS == hf
     const int row = sub * 32 + lane;             // accumulator row owned by this thread
-    float* wscr = (float*)((unsigned char*)scratch + (warp - EPI_WARP0) * WSCR_BYTES);
+    float* wscr = (float*)((unsigned char*)scratch + (warp - EPI_WARP0) * C::WSCR);
     constexpr int NCH = BN / 32;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -685,7 +715,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(sub * 32) << 16);
-        float v[32], vn[32];
+        float v[32], vn[DB ? 32 : 1];
         ptx::tmem_ld32(tbase + hf * 32, v);
         // bias values of the current chunk; the next chunk's are loaded early
         constexpr bool USE_BIAS = (EPI == EPI_STORE || EPI == EPI_LSE || EPI == EPI_DH);
@@ -700,15 +730,17 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         ptx::tmem_ld_wait();
         ptx::reg_fence32(v);
 #pragma unroll 1
-        for (int c = hf; c < NCH; c += 2) {
-          const bool more = c + 2 < NCH;
-          if (more) ptx::tmem_ld32(tbase + (c + 2) * 32, vn);
+        for (int c = hf; c < NCH; c += PARTS) {
+          const bool more = c + PARTS < NCH;
+          if constexpr (DB) {
+            if (more) ptx::tmem_ld32(tbase + (c + 2) * 32, vn);
+          }
           const int col0 = n * BN + c * 32;
           uint4 bqn[4];
-          if (USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
+          if (DB && USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
 
           float bb[32];
-          if (USE_BIAS) unpack32(bq, bb);
+          if (USE_BIAS && EPI != EPI_DH) unpack32(bq, bb);
           if constexpr (EPI == EPI_STORE || EPI == EPI_ATOMIC) {
             const long long grow = (long long)w.m * BM + row;
             if (grow < p.M && col0 < p.N) {
@@ -739,7 +771,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             lse_chunk(ls, p, rc, v, bb, col0,
                       p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
           } else if constexpr (EPI == EPI_DH) {
-            dh_chunk(ds, p, rc, v, bb, col0, (long long)w.m * BM + sub * 32,
+            dh_chunk(ds, p, rc, v, bq, col0, (long long)w.m * BM + sub * 32,
                      (unsigned char*)wscr, &tmC, w.m < p.ch.ntiles);
           } else if constexpr (EPI == EPI_DA) {
             // da = dz (1 - z^2) on the thread's own row, then 16-column halves
@@ -814,15 +846,21 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
           }
           if (more) {
-            ptx::tmem_ld_wait();
-            ptx::reg_fence32(vn);
+            if constexpr (DB) {
+              ptx::tmem_ld_wait();
+              ptx::reg_fence32(vn);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = vn[j];
-            if (USE_BIAS) {
+              for (int j = 0; j < 32; ++j) v[j] = vn[j];
+              if (USE_BIAS) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) bq[i] = bqn[i];
+                for (int i = 0; i < 4; ++i) bq[i] = bqn[i];
+              }
+            } else {
+              ptx::tmem_ld32(tbase + (c + PARTS) * 32, v);
+              if (USE_BIAS) load_bias_q(p.bias, p.N, col0 + 32 * PARTS, bq);
+              ptx::tmem_ld_wait();
+              ptx::reg_fence32(v);
             }
-
           }
         }
         ptx::tc_fence_before();
@@ -830,27 +868,36 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
       if (EPI == EPI_LSE && ok) {
-        // combine the two column halves of each row: the second half hands
-        // its partial (max, sum, blank score, label score) to the first
-        float* cb = comb + (uidx & 1) * 128 * 4 + row * 4;
-        if (hf == 1) {
-          cb[0] = ls.run_max;
-          cb[1] = ls.run_sum;
-          cb[2] = ls.h_blank;
-          cb[3] = ls.h_lab;
+        // combine the column parts of each row: parts 1.. hand their partial
+        // (max, sum, blank score, label score) to part 0
+        float* cb = comb + ((uidx & 1) * (PARTS - 1)) * 128 * 4;
+        if (hf > 0) {
+          float* mine = cb + ((hf - 1) * 128 + row) * 4;
+          mine[0] = ls.run_max;
+          mine[1] = ls.run_sum;
+          mine[2] = ls.h_blank;
+          mine[3] = ls.h_lab;
           ptx::mbar_arrive(&comb_bar[uidx & 1]);
         } else if (ptx::mbar_wait(&comb_bar[uidx & 1], (uint32_t)(uidx >> 1) & 1u, wait_ns)) {
-          const float m1 = cb[0], s1 = cb[1];
-          const float nm = fmaxf(ls.run_max, m1);
+          float nm = ls.run_max;
+#pragma unroll
+          for (int q = 1; q < PARTS; ++q) nm = fmaxf(nm, cb[((q - 1) * 128 + row) * 4]);
           float sum = 0.f;
           if (ls.run_max != -INFINITY) sum += ls.run_sum * ptx::ex2((ls.run_max - nm) * kLog2e);
-          if (m1 != -INFINITY) sum += s1 * ptx::ex2((m1 - nm) * kLog2e);
+#pragma unroll
+          for (int q = 1; q < PARTS; ++q) {
+            const float* o = cb + ((q - 1) * 128 + row) * 4;
+            if (o[0] != -INFINITY) sum += o[1] * ptx::ex2((o[0] - nm) * kLog2e);
+          }
           ls.run_max = nm;
           ls.run_sum = sum;
-          // each score column lives in exactly one half: take it from there
-          const int bchunk = (p.ch.sh.blank % BN) / 32;
-          if ((bchunk & 1) == 1) ls.h_blank = cb[2];
-          if (ls.lab >= 0 && (((ls.lab % BN) / 32) & 1) == 1) ls.h_lab = cb[3];
+          // each score column lives in exactly one part: take it from there
+          const int bpart = ((p.ch.sh.blank % BN) / 32) % PARTS;
+          if (bpart != 0) ls.h_blank = cb[((bpart - 1) * 128 + row) * 4 + 2];
+          if (ls.lab >= 0) {
+            const int lpart = ((ls.lab % BN) / 32) % PARTS;
+            if (lpart != 0) ls.h_lab = cb[((lpart - 1) * 128 + row) * 4 + 3];
+          }
           lse_finish(ls, p, rc);
         } else {
           report_timeout(p, abort_flag);
@@ -1170,7 +1217,7 @@ struct GemmDesc {
 
 template <int BN, int AMN, int BMN, int EPI, int CL>
 cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   auto kern = k_tc_gemm<BN, AMN, BMN, EPI, CL>;
   CUtensorMap ta, tb;
   const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64) : make_tmap(&ta, g.A, g.M, g.K, BM);
@@ -1195,7 +1242,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.gridDim = dim3(CL * 64);
-      cfg.blockDim = dim3(NTHREADS);
+      cfg.blockDim = dim3(C::THREADS);
       cfg.dynamicSmemBytes = C::SMEM;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
@@ -1222,7 +1269,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
   const int grid_groups = std::min(groups, cap);
   if (CL == 1) {
-    kern<<<grid_groups, NTHREADS, C::SMEM, s>>>(ta, tb, tc, p);
+    kern<<<grid_groups, C::THREADS, C::SMEM, s>>>(ta, tb, tc, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1232,7 +1279,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(grid_groups * CL);
-  cfg.blockDim = dim3(NTHREADS);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -1414,25 +1461,40 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Zv,
                               void* Hv, bool untiled, float* dA, float* dLr, float* dWO,
-                              float* dbO, float4* post, cudaStream_t s) {
+                              float* dbO, float4* post, const PreLaunch* pre,
+                              cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
   long long nch = 0;
   rnnt_status st = chunk_total(p, sv, s, &nch);
   if (st != RNNT_OK) return st;
   const int rows = (int)p.chunk_rows;
+  if (pre && (untiled || nch == 0)) {
+    st = (*pre)(s);
+    if (st != RNNT_OK) return st;
+  }
   for (long long k = 0; k < nch; ++k) {
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     if (!untiled) {
       {
-        ProfScope ps("tc_build_z", s);
-        k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
-        if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
-      }
-      {
-        ProfScope ps("tc_posteriors", s);
-        k_posteriors<<<(unsigned)c.ntiles, TILE, 0, s>>>(c, grad_loss, post);
-        if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+        // the z rebuild, the posterior records and (first chunk) the caller's
+        // preparatory launches are independent of one another
+        Fork fork(s, 2);
+        if (k == 0 && pre) {
+          st = (*pre)(fork.side(1));
+          if (st != RNNT_OK) return st;
+        }
+        {
+          ProfScope ps("tc_posteriors", fork.side(0));
+          k_posteriors<<<(unsigned)c.ntiles, TILE, 0, fork.side(0)>>>(c, grad_loss, post);
+          if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+        }
+        {
+          ProfScope ps("tc_build_z", s);
+          k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+          if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+        }
+        if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
       }
       // recompute the tile's scores and overwrite them with dh
       ProfScope ps("tc_bwd_dh", s);

@@ -43,6 +43,7 @@ constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait, then give up
 constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
 
 enum { EPI_STORE = 0, EPI_ATOMIC = 1, EPI_LSE = 2, EPI_DH = 3, EPI_DA = 4 };
+enum { TILES_NONE = 0, TILES_ON_M = 1, TILES_ON_K = 2 };
 
 // Per-epilogue-warp shared scratch: either 32 rows x 16 fp32 (+1 pad) for
 // column transposes, or 32 rows x 32 bf16 at an 80-byte pitch for staging
@@ -69,6 +70,11 @@ struct TcParams {
   float* dbO;            // DH: column sums of dh accumulated here (may be NULL)
   const float4* post;    // DH: per-row records (g pb, g pl, lnPD log2 e, label bits)
   int32_t* status;
+  // Lattice GEMMs: which axis runs over the chunk's tiles (TILES_ON_M: M
+  // tiles are lattice tiles; TILES_ON_K: K runs over the tiles' rows), so
+  // that units past the batch's last tile (the host sizes the chunk by an
+  // upper bound) are skipped; TILES_NONE for the other GEMMs.
+  int tiles_on;
   unsigned long long wait_ns;  // limit of every mbarrier wait (0: WAIT_NS)
   int skip_first_fill;         // test hook: the producer never fills the first stage
 };
@@ -114,7 +120,7 @@ struct Unit {
 // B tiles at the same time.  M tiles past the matrix are padding: their A
 // loads are zero-filled and their epilogues write nothing.
 template <int CL>
-__device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
+__device__ __forceinline__ Unit unit_of(const TcParams& p, int u, int kb_lim) {
   Unit w;
   const int r = u % CL;
   int rest = u / CL;
@@ -136,7 +142,7 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
     w.m = mg * CL + r;
     w.n0 = n; w.n1 = n + 1;
     w.kb0 = ks * p.kb_per_split;
-    w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
+    w.kb1 = min(kb_lim, w.kb0 + p.kb_per_split);
   }
   return w;
 }
@@ -166,6 +172,14 @@ struct RowCell {
   bool valid;   // inside its sample's lattice
   int b, t, u, Tb, Ub;
 };
+
+// Whether tile m of a chunk is read by any GEMM: the actual tiles, and the
+// padding tiles that complete the last cluster group (up to 4 CTAs) - the
+// chunk itself is sized by an upper bound, and the GEMMs skip the rest.
+__device__ __forceinline__ bool tile_in_use(const ChunkArgs& c, int m) {
+  const long long have = (long long)*c.sv.total_tiles - c.first_tile;
+  return m < ((have + 3) / 4) * 4;
+}
 
 __device__ __forceinline__ RowCell row_of(const TileRef& tr, int row) {
   RowCell r{};
@@ -369,7 +383,8 @@ __device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p
 
 // f^W_4 (Eq. 10): dh_v = g ((pb + pl) softmax_v - pb [v = blank] - pl [v = label]).
 struct DhState {
-  float gpb, gpl, nl;  // g pb, g pl, lnPD * log2(e)
+  float gpb, gpl;  // g pb, g pl
+  float lgn;       // log2(g (pb + pl)) - lnPD log2(e): g (pb+pl) softmax_v = 2^(h_v log2 e + lgn)
   int lab;
 };
 
@@ -378,48 +393,10 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
   DhState st;
   st.gpb = q.x;
   st.gpl = q.y;
-  st.nl = q.z;
+  const float gg = q.x + q.y;
+  st.lgn = gg > 0.f ? ptx::lg2(gg) - q.z : -INFINITY;
   st.lab = __float_as_int(q.w);
   return st;
-}
-
-// Column sums of the warp's 32 x 32 block (lane = row, d = its 32 columns)
-// added to dst[col0 ..]: the block is halved five times across lanes (lane
-// bit 4 keeps columns 16..31, bit 3 the upper 8 of those, ...), so that 36
-// shuffles leave lanes 4k..4k+3 all holding the sums of columns 4k..4k+3;
-// lane 4k adds them with one vector reduction.  Columns >= N are skipped (N
-// is a multiple of 8).  dst must be 16-byte aligned.
-__device__ __forceinline__ void colsum32_red(const float (&d)[32], float* dst, int col0, int N) {
-  const int lane = threadIdx.x & 31;
-  float e[16];
-  const bool u16 = (lane & 16) != 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float send = u16 ? d[j] : d[j + 16];
-    const float keep = u16 ? d[j + 16] : d[j];
-    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  const bool u8 = (lane & 8) != 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float send = u8 ? e[j] : e[j + 8];
-    const float keep = u8 ? e[j + 8] : e[j];
-    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  const bool u4 = (lane & 4) != 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float send = u4 ? e[j] : e[j + 4];
-    const float keep = u4 ? e[j + 4] : e[j];
-    e[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    e[j] += __shfl_xor_sync(0xffffffffu, e[j], 1);
-    e[j] += __shfl_xor_sync(0xffffffffu, e[j], 2);
-  }
-  const int c = col0 + (lane & 28);
-  if ((lane & 3) == 0 && c < N) ptx::red_add_v4(dst + c, e[0], e[1], e[2], e[3]);
 }
 
 // dh of 32 columns (Eq. 10: softmax times the position's occupancy minus the
@@ -428,7 +405,10 @@ __device__ __forceinline__ void colsum32_red(const float (&d)[32], float* dst, i
 // (32 rows x 64 bytes, 64-byte swizzle: lane r writes its 16-byte piece j at
 // piece j ^ ((r >> 1) & 3), which spreads every 8 lanes over all 32 banks);
 // rows outside the lattice are 0.  When dbO is given, the block's column sums
-// are added to it.  bq: the 32 bias values (packed bf16).  All lanes take part.
+// (of the bf16 values, read back from the staging area: lane k + 16 h sums
+// columns 2k, 2k+1 over rows 16h .. 16h+15, rows of the two halves taken in
+// opposite parity so that the reads hit distinct banks) are added to it.
+// bq: the 32 bias values (packed bf16).  All lanes take part.
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
                                          float (&d)[32], const uint4 (&bq)[4], int col0,
                                          long long wrow0, unsigned char* stg,
@@ -438,7 +418,6 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   if (rc.valid) {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
-    const float gg = st.gpb + st.gpl;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t w[4] = {bq[i].x, bq[i].y, bq[i].z, bq[i].w};
@@ -446,8 +425,8 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       for (int k = 0; k < 4; ++k) {
         float& d0 = d[8 * i + 2 * k];
         float& d1 = d[8 * i + 2 * k + 1];
-        d0 = gg * ptx::ex2(fmaf(d0 + ptx::bf16lo(w[k]), kLog2e, -st.nl));
-        d1 = gg * ptx::ex2(fmaf(d1 + ptx::bf16hi(w[k]), kLog2e, -st.nl));
+        d0 = ptx::ex2(fmaf(d0 + ptx::bf16lo(w[k]), kLog2e, st.lgn));
+        d1 = ptx::ex2(fmaf(d1 + ptx::bf16hi(w[k]), kLog2e, st.lgn));
       }
     }
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
@@ -485,9 +464,34 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       ptx::tma_store_2d(tmC, stg, col0, (int)wrow0);
       ptx::bulk_commit();
     }
+    if (p.dbO) {
+      // row 16h + 2q + (e ^ h): its 16-byte piece k/4 sits at (k/4 ^ (q & 3))
+      const int k = lane & 15, h = lane >> 4;
+      const uint32_t a0 = ptx::smem_u32(stg) + 1024 * h + (k & 3) * 4;
+      uint32_t ad[2][4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ad[e][q] = a0 + 64 * (e ^ h) + (((k >> 2) ^ q) << 4);
+      float s0 = 0.f, s1 = 0.f;
+      auto add = [&](uint32_t w) {
+        s0 += ptx::bf16lo(w);
+        s1 += ptx::bf16hi(w);
+      };
+      // q = 0..7: rows 2q, 2q+1 of the half; q & 3 selects the address, q / 4 the offset
+      add(ptx::lds32<0>(ad[0][0]));   add(ptx::lds32<0>(ad[1][0]));
+      add(ptx::lds32<128>(ad[0][1])); add(ptx::lds32<128>(ad[1][1]));
+      add(ptx::lds32<256>(ad[0][2])); add(ptx::lds32<256>(ad[1][2]));
+      add(ptx::lds32<384>(ad[0][3])); add(ptx::lds32<384>(ad[1][3]));
+      add(ptx::lds32<512>(ad[0][0])); add(ptx::lds32<512>(ad[1][0]));
+      add(ptx::lds32<640>(ad[0][1])); add(ptx::lds32<640>(ad[1][1]));
+      add(ptx::lds32<768>(ad[0][2])); add(ptx::lds32<768>(ad[1][2]));
+      add(ptx::lds32<896>(ad[0][3])); add(ptx::lds32<896>(ad[1][3]));
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+      if (h == 0 && col0 + 2 * k < p.N) ptx::red_add_v2(p.dbO + col0 + 2 * k, s0, s1);
+    }
   }
-  // (after the store, so that the packed copy is no longer live)
-  if (p.dbO) colsum32_red(d, p.dbO, col0, p.N);
 }
 
 template <int BN, int A_MN, int B_MN, int EPI, int CL>
@@ -503,6 +507,22 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
   constexpr int STAGES = C::STAGES;
+  // units that hold actual lattice tiles: a prefix of the unit order (M
+  // groups, resp. K splits, are the slow index), read from the tile count
+  int units = p.units, kb_lim = p.kb_total;
+  if (p.tiles_on != TILES_NONE) {
+    const long long have = max(0LL, min(p.ch.ntiles, (long long)*p.ch.sv.total_tiles -
+                                                         p.ch.first_tile));
+    if (p.tiles_on == TILES_ON_M) {
+      const int groups = (int)((have + CL - 1) / CL);
+      // (row-complete: the V split is the fast index; otherwise N, with no K split)
+      units = min(units, groups * (p.row_complete ? max(1, p.n_split) : p.n_tiles) * CL);
+    } else {
+      kb_lim = (int)min((long long)p.kb_total, have * (BM / BK));
+      const int splits = (kb_lim + p.kb_per_split - 1) / p.kb_per_split;
+      units = min(units, splits * p.m_groups * p.n_tiles * CL);
+    }
+  }
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
@@ -555,8 +575,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       uint32_t phase = 0;
       int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
       bool first_fill = true;
-      for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
+      for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -621,8 +641,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
+      for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, wait_ns)) {
@@ -681,15 +701,15 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint32_t acc_phase = 0;
     // dh epilogue: the row's record of the next unit is loaded one unit ahead
     float4 post_next = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
-    if (EPI == EPI_DH && cluster_id * CL < p.units) {
-      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank);
+    if (EPI == EPI_DH && cluster_id * CL < units) {
+      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank, kb_lim);
       if (w0.m < p.ch.ntiles) post_next = __ldg(p.post + (long long)w0.m * BM + row);
     }
-    for (int gi = cluster_id; gi * CL < p.units && !*abort_flag; gi += n_clusters) {
-      const Unit w = unit_of<CL>(p, gi * CL + (int)crank);
+    for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
+      const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
       const float4 post_cur = post_next;
-      if (EPI == EPI_DH && (gi + n_clusters) * CL < p.units) {
-        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank);
+      if (EPI == EPI_DH && (gi + n_clusters) * CL < units) {
+        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank, kb_lim);
         post_next = (wn.m < p.ch.ntiles) ? __ldg(p.post + (long long)wn.m * BM + row)
                                          : make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
       }
@@ -931,6 +951,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
+  if (!tile_in_use(c, blockIdx.x)) return;
   __shared__ TileRef tr;
   if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
   __syncthreads();
@@ -976,6 +997,7 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
 // (0, 0, +inf, -1).  One thread per row of the chunk.
 __global__ void __launch_bounds__(128)
 k_posteriors(ChunkArgs c, const float* __restrict__ grad_loss, float4* __restrict__ post) {
+  if (!tile_in_use(c, blockIdx.x)) return;
   const TileRef tr = tile_ref(c, blockIdx.x);
   const RowCell rc = row_of(tr, threadIdx.x);
   float4 rec = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
@@ -1049,10 +1071,12 @@ int num_sms() {
 // 16-byte load per row), so a warp reads 512 contiguous bytes of a row.
 __global__ void __launch_bounds__(256)
 k_colsum_bf16(const __nv_bfloat16* __restrict__ X, long long R, int N, float* __restrict__ out,
-              long long rows_per) {
+              long long rows_per, const int32_t* __restrict__ tiles_total, long long first_tile) {
   __shared__ float part[8][256];
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
   const int c0 = (blockIdx.x * 32 + lane) * 8;
+  // rows of tiles past the batch's last one hold nothing
+  if (tiles_total) R = min(R, max(0LL, ((long long)*tiles_total - first_tile) * TILE));
   const long long r0 = (long long)blockIdx.y * rows_per;
   const long long r1 = min(R, r0 + rows_per);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -1122,13 +1146,15 @@ cudaError_t launch_colsum_f32v(const float* X, long long R, int N, float* out, c
 }
 
 cudaError_t launch_colsum_bf16(const __nv_bfloat16* X, long long R, int N, float* out,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int32_t* tiles_total = nullptr,
+                               long long first_tile = 0) {
   if (R <= 0 || N <= 0) return cudaSuccess;
   const int strips = (int)cdiv(N, 256);
   long long slabs = std::max<long long>(1, (long long)num_sms() * 4 / strips);
   long long rows_per = cdiv(R, slabs);
   if (cdiv(R, rows_per) > 65535) rows_per = cdiv(R, 65535);
-  k_colsum_bf16<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per);
+  k_colsum_bf16<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per,
+                                                                          tiles_total, first_tile);
   return cudaGetLastError();
 }
 
@@ -1452,6 +1478,7 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     tp.ch = c;
     tp.Hout = (__nv_bfloat16*)Hkeep;
     tp.status = sv.status;
+    tp.tiles_on = TILES_ON_M;
     if (launch_gemm<EPI_LSE>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   return RNNT_OK;
@@ -1514,6 +1541,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       // db^O: column sums of dh formed in the same epilogue (vector
       // reductions need a 16-byte aligned db^O)
       if (dbO && ((uintptr_t)dbO & 15) == 0) tp.dbO = dbO;
+      tp.tiles_on = TILES_ON_M;
       if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
       ProfScope ps("tc_dh_kept", s);
@@ -1523,7 +1551,8 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
     if (dbO && (untiled || ((uintptr_t)dbO & 15) != 0)) {
       // db^O += sum over the chunk's positions of dh (rows outside are 0)
       ProfScope ps("tc_colsum_dh", s);
-      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s, sv.total_tiles, c.first_tile) != cudaSuccess)
+        return RNNT_ERR_CUDA;
     }
     {  // dz = dh W^O, da = dz (1 - z^2) reduced into dA and dLr
       ProfScope ps("tc_bwd_dz", s);
@@ -1534,6 +1563,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.dA = dA;
       tp.dLr = dLr;
       tp.status = sv.status;
+      tp.tiles_on = TILES_ON_M;
       if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), kClusterLattice, s) != cudaSuccess)
         return RNNT_ERR_CUDA;
     }
@@ -1546,6 +1576,8 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.C = dWO;
       tp.ldc = p.H;
       tp.status = sv.status;
+      tp.ch = c;
+      tp.tiles_on = TILES_ON_K;
       if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
   }

@@ -305,17 +305,21 @@ rnnt_status rnnt::fwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
 
   rnnt_status s;
   {
-    // the two joint projections run beside the index, tile table and fill
-    // (they read only the inputs and write only pA, pL)
-    Fork fork(st, side_streams && p.tc && p.B > 0 ? 2 : 0);
+    // the two joint projections (they read only the inputs and write only
+    // pA, pL) and the -inf fill of the saved arrays run beside the index and
+    // tile table
+    Fork fork(st, side_streams && p.tc && p.B > 0 ? 3 : 0);
     LAUNCH("index", launch_index(sh, labels, T_len, U_len, sv, loss, st));
     if (p.B == 0) return RNNT_OK;
     s = projections(p, hA, hL, pr, pA, pL, fork.side(0), fork.side(1));
     if (s != RNNT_OK) return s;
+    {
+      // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
+      cudaStream_t st = fork.side(2);
+      LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY,
+                                         (p.s_beta - p.s_lpb) / 4 + (size_t)p.B * p.T * p.U1, st));
+    }
     LAUNCH("tile_table", launch_tile_table(sh, T_len, U_len, sv, st));
-    // lpb, lpl, lnPD, alpha, beta are consecutive (with alignment gaps): one fill
-    LAUNCH("fill_f32", launch_fill_f32(sv.lpb, -INFINITY,
-                                       (p.s_beta - p.s_lpb) / 4 + (size_t)p.B * p.T * p.U1, st));
     RNNT_CHECK(fork.join());
   }
 

@@ -94,47 +94,50 @@ cudaError_t launch_zero_many(const ZeroList& z, cudaStream_t s) {
 // [0,V).  labels[b,0] (the prepended blank) is never read.
 constexpr int IDX_THREADS = 1024;
 
-// Tiles of sample b, or 0 (and a status bit in *bad) if it is rejected.
-__device__ inline int sample_tiles(const Shape& sh, const int32_t* __restrict__ labels,
-                                   const int32_t* __restrict__ T_len,
-                                   const int32_t* __restrict__ U_len, int b, int* bad) {
-  const int Tb = T_len[b], Ub = U_len[b];
-  if (Tb < 1 || Tb > sh.T || Ub < 0 || Ub > sh.U1 - 1) {
-    *bad |= status_bit(RNNT_ERR_LENGTH_RANGE);
-    return 0;
-  }
-  // no early exit, so the label loads of a sample are all in flight together
-  const int32_t* lab = labels + (size_t)b * sh.U1;
-  bool ok = true;
-#pragma unroll 8
-  for (int u = 1; u <= Ub; ++u) {
-    const int y = __ldg(lab + u);
-    ok &= (y >= 0) & (y < sh.V);
-  }
-  if (!ok) {
-    *bad |= status_bit(RNNT_ERR_LABEL_RANGE);
-    return 0;
-  }
-  return (int)(cdiv(Tb, TT) * cdiv(Ub + 1, TU));
+// Validation bits of sample b's lengths (0 if they are in range).
+__device__ __forceinline__ int length_bits(const Shape& sh, int Tb, int Ub) {
+  return (Tb < 1 || Tb > sh.T || Ub < 0 || Ub > sh.U1 - 1) ? status_bit(RNNT_ERR_LENGTH_RANGE)
+                                                              : 0;
 }
 
+// One block.  prefix[] first holds each sample's validation bits, then its
+// tile count, then its exclusive prefix: (1) lengths, one thread per sample;
+// (2) every label of every sample with valid lengths, all threads over the
+// flattened [B, U+1] array (coalesced; a bad label ORs a bit into its
+// sample's word); (3) tile counts (0 for a rejected sample, whose loss and
+// ln P become NaN); (4) block scan.
 __global__ void __launch_bounds__(IDX_THREADS)
 k_index(Shape sh, const int32_t* __restrict__ labels, const int32_t* __restrict__ T_len,
         const int32_t* __restrict__ U_len, SavedView sv, float* __restrict__ loss) {
   __shared__ int warp_sum[IDX_THREADS / 32];
   __shared__ int bad_bits;
-  const int B = sh.B;
+  const int B = sh.B, U1 = sh.U1;
+  if (threadIdx.x == 0) bad_bits = 0;
+  for (int b = threadIdx.x; b < B; b += IDX_THREADS)
+    sv.prefix[b] = length_bits(sh, T_len[b], U_len[b]);
+  __syncthreads();
+  const long long nl = (long long)B * U1;
+  for (long long i = threadIdx.x; i < nl; i += IDX_THREADS) {
+    const int b = (int)(i / U1), u = (int)(i % U1);
+    if (u == 0 || u > U_len[b]) continue;  // the prepended blank, or past U_b
+    const int y = __ldg(labels + i);
+    if ((y < 0) | (y >= sh.V)) atomicOr(&sv.prefix[b], status_bit(RNNT_ERR_LABEL_RANGE));
+  }
+  __syncthreads();
   const int per = (int)cdiv(B, IDX_THREADS);
   const int b0 = min(B, (int)threadIdx.x * per), b1 = min(B, b0 + per);
-  if (threadIdx.x == 0) bad_bits = 0;
-  __syncthreads();
   int local = 0, bad = 0;
   for (int b = b0; b < b1; ++b) {
-    const int n = sample_tiles(sh, labels, T_len, U_len, b, &bad);
-    if (n == 0) {
+    const int bits = sv.prefix[b];
+    int n = 0;
+    if (bits) {
+      bad |= bits;
       loss[b] = NAN;
       sv.lnP[b] = NAN;
+    } else {
+      n = (int)(cdiv(T_len[b], TT) * cdiv(U_len[b] + 1, TU));
     }
+    sv.prefix[b] = n;
     local += n;
   }
   // block exclusive scan of `local`
@@ -160,10 +163,10 @@ k_index(Shape sh, const int32_t* __restrict__ labels, const int32_t* __restrict_
   }
   __syncthreads();
   int run = warp_sum[w] + incl - local;
-  int dummy = 0;
   for (int b = b0; b < b1; ++b) {
+    const int n = sv.prefix[b];
     sv.prefix[b] = run;
-    run += sample_tiles(sh, labels, T_len, U_len, b, &dummy);
+    run += n;
   }
   if (threadIdx.x == IDX_THREADS - 1) {
     sv.prefix[B] = run;
@@ -388,12 +391,12 @@ __device__ __forceinline__ void cp_async_wait() {
 // One direction of the recursion for one sample (one warp).  The per-lane
 // state advances by increments from one diagonal to the next: position j's
 // frame t, its row in the ring and its offset in the output array.
-template <int NJ, bool FAST, bool BETA>
-__device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int U1,
+template <int NJ, bool FAST, bool BETA, int W>
+__device__ __forceinline__ void ab_walk(float* ring, float* xch, int R, int Tb, int Ub, int U1,
                                         const float* __restrict__ LPB,
                                         const float* __restrict__ LPL, float* __restrict__ OUT,
                                         float* lnP, float* loss) {
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int plane = R * U1;
   const int rmask = R - 1;
   const int nwin = (Tb + AB_W - 1) / AB_W;
@@ -410,11 +413,16 @@ __device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int 
     float* dst = ring + (r0 & rmask) * U1;
     const float* gb = LPB + (size_t)r0 * U1;
     const float* gl = LPL + (size_t)r0 * U1;
-    for (int i = lane; i < n; i += 32) {
+    for (int i = threadIdx.x; i < n; i += 32 * W) {
       cp_async4(dst + i, gb + i);
       cp_async4(dst + plane + i, gl + i);
     }
     cp_async_commit();
+  };
+  // every thread's copies of a window are complete, and seen by all warps
+  auto window_sync = [&]() {
+    cp_async_wait<1>();
+    if (W > 1) __syncthreads(); else __syncwarp();
   };
   int next_win, ready;  // next window to load; window known complete
   if (!BETA) {
@@ -428,10 +436,9 @@ __device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int 
     next_win = nwin - 3;
     ready = nwin - 1;
   }
-  cp_async_wait<1>();
-  __syncwarp();
+  window_sync();
 
-  const int u0 = NJ * lane;
+  const int u0 = NJ * (warp * 32 + lane);
   const int d0 = BETA ? ndiag - 1 : 0;
   int t[NJ], ri[NJ], oo[NJ];
   bool uok[NJ], ulast[NJ];
@@ -454,29 +461,30 @@ __device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int 
       const int hi = min(d, Tb - 1) >> 5;
       if (hi > ready) {  // entering window `hi`, loaded one ahead
         if (next_win < nwin) { load_window(next_win); ++next_win; } else cp_async_commit();
-        cp_async_wait<1>();
-        __syncwarp();
+        window_sync();
         ready = hi;
       }
     } else {
       const int lo = max(0, d - Ub) >> 5;
       if (lo < ready) {
         if (next_win >= 0) { load_window(next_win); --next_win; } else cp_async_commit();
-        cp_async_wait<1>();
-        __syncwarp();
+        window_sync();
         ready = lo;
       }
     }
-    // neighbours from the previous diagonal
+    // neighbours from the previous diagonal: a shuffle within the warp, the
+    // neighbouring warp's edge value through shared memory (written at the
+    // end of the previous diagonal, before the barrier)
     float nb[NJ];
+    const float* xin = xch + ((s + 1) & 1) * W;
     if (!BETA) {
       const float x = __shfl_up_sync(0xffffffffu, send[NJ - 1], 1);
-      nb[0] = lane == 0 ? -INFINITY : x;
+      nb[0] = lane > 0 ? x : ((W > 1 && warp > 0 && s > 0) ? xin[warp - 1] : -INFINITY);
 #pragma unroll
       for (int j = 1; j < NJ; ++j) nb[j] = send[j - 1];
     } else {
       const float x = __shfl_down_sync(0xffffffffu, send[0], 1);
-      nb[NJ - 1] = lane == 31 ? -INFINITY : x;
+      nb[NJ - 1] = lane < 31 ? x : ((W > 1 && warp < W - 1 && s > 0) ? xin[warp + 1] : -INFINITY);
 #pragma unroll
       for (int j = 0; j < NJ - 1; ++j) nb[j] = send[j + 1];
     }
@@ -510,6 +518,13 @@ __device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int 
         oo[j] -= U1;
       }
     }
+    if (W > 1) {
+      // the warp's edge value for its neighbour warp on the next diagonal
+      float* xout = xch + (s & 1) * W;
+      if (!BETA && lane == 31) xout[warp] = send[NJ - 1];
+      if (BETA && lane == 0) xout[warp] = send[0];
+      __syncthreads();
+    }
   }
   cp_async_wait<0>();
   if (!BETA) {
@@ -524,21 +539,26 @@ __device__ __forceinline__ void ab_walk(float* ring, int R, int Tb, int Ub, int 
   }
 }
 
-template <int NJ, bool FAST>
-__global__ void __launch_bounds__(32)
+// W warps per block split the label positions of one sample (lane l of warp
+// w owns u = NJ (32 w + l) ..); with W > 1 the warps meet at a barrier once
+// per diagonal.  Several warps pay off when there are few samples (the
+// recursion is latency-bound, and the GPU otherwise runs 2B warps).
+template <int NJ, bool FAST, int W>
+__global__ void __launch_bounds__(32 * W)
 k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
                   SavedView sv, float* __restrict__ loss, int R) {
-  extern __shared__ float ring[];  // [lpb | lpl] x R rows x U1
+  extern __shared__ float ring[];  // [lpb | lpl] x R rows x U1, then 2 x W exchange slots
+  float* xch = ring + 2 * (size_t)R * sh.U1;
   const int b = blockIdx.x;
-  if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample
+  if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample (uniform over the block)
   const int Tb = T_len[b], Ub = U_len[b];
   const size_t base = (size_t)b * sh.T * sh.U1;
   if (blockIdx.y == 0)
-    ab_walk<NJ, FAST, false>(ring, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
-                             sv.alpha + base, sv.lnP + b, loss + b);
+    ab_walk<NJ, FAST, false, W>(ring, xch, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                                sv.alpha + base, sv.lnP + b, loss + b);
   else
-    ab_walk<NJ, FAST, true>(ring, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
-                            sv.beta + base, nullptr, nullptr);
+    ab_walk<NJ, FAST, true, W>(ring, xch, R, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                               sv.beta + base, nullptr, nullptr);
 }
 
 template <bool FAST>
@@ -555,19 +575,46 @@ static cudaError_t launch_ab(const Shape& sh, const int32_t* T_len, const int32_
   return cudaGetLastError();
 }
 
-template <int NJ, bool FAST>
+template <int NJ, bool FAST, int W>
 static cudaError_t launch_ab_smem(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
                                   SavedView sv, float* loss, int R, size_t smem,
                                   cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_alpha_beta_smem<NJ, FAST>,
+    cudaError_t e = cudaFuncSetAttribute(k_alpha_beta_smem<NJ, FAST, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_alpha_beta_smem<NJ, FAST><<<dim3(sh.B, 2), 32, smem, s>>>(sh, T_len, U_len, sv, loss, R);
+  k_alpha_beta_smem<NJ, FAST, W><<<dim3(sh.B, 2), 32 * W, smem, s>>>(sh, T_len, U_len, sv, loss,
+                                                                       R);
   return cudaGetLastError();
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+template <bool FAST>
+static cudaError_t launch_ab_smem_nj(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                                     SavedView sv, float* loss, int R, size_t smem, int w,
+                                     cudaStream_t s) {
+  const int nj = (int)cdiv(sh.U1, 32 * w);
+  if (w == 4) return launch_ab_smem<1, FAST, 4>(sh, T_len, U_len, sv, loss, R, smem, s);
+  if (w == 2) {
+    if (nj <= 1) return launch_ab_smem<1, FAST, 2>(sh, T_len, U_len, sv, loss, R, smem, s);
+    return launch_ab_smem<2, FAST, 2>(sh, T_len, U_len, sv, loss, R, smem, s);
+  }
+  if (nj <= 1) return launch_ab_smem<1, FAST, 1>(sh, T_len, U_len, sv, loss, R, smem, s);
+  if (nj <= 2) return launch_ab_smem<2, FAST, 1>(sh, T_len, U_len, sv, loss, R, smem, s);
+  return launch_ab_smem<4, FAST, 1>(sh, T_len, U_len, sv, loss, R, smem, s);
 }
 
 cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
@@ -577,17 +624,15 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
   // shared-memory ring when it fits in 220 KiB, else the register-prefetch kernel
   int R = AB_W;
   while (R < ((int)cdiv(sh.U1, AB_W) + 2) * AB_W) R *= 2;
-  const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float);
+  const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float) + 2 * 4 * sizeof(float);
   const int nj = (int)cdiv(sh.U1, 32);
   if (smem <= 220 * 1024 && nj <= 4) {
-    if (fast) {
-      if (nj <= 1) return launch_ab_smem<1, true>(sh, T_len, U_len, sv, loss, R, smem, s);
-      if (nj <= 2) return launch_ab_smem<2, true>(sh, T_len, U_len, sv, loss, R, smem, s);
-      return launch_ab_smem<4, true>(sh, T_len, U_len, sv, loss, R, smem, s);
-    }
-    if (nj <= 1) return launch_ab_smem<1, false>(sh, T_len, U_len, sv, loss, R, smem, s);
-    if (nj <= 2) return launch_ab_smem<2, false>(sh, T_len, U_len, sv, loss, R, smem, s);
-    return launch_ab_smem<4, false>(sh, T_len, U_len, sv, loss, R, smem, s);
+    // warps per sample and direction: one label position per lane when the
+    // 2B recursions leave most SMs idle, else one warp (several positions each)
+    int w = 1;
+    if (nj > 1 && 2LL * sh.B * nj <= 2LL * sm_count()) w = nj <= 2 ? 2 : 4;
+    return fast ? launch_ab_smem_nj<true>(sh, T_len, U_len, sv, loss, R, smem, w, s)
+                : launch_ab_smem_nj<false>(sh, T_len, U_len, sv, loss, R, smem, w, s);
   }
   return fast ? launch_ab<true>(sh, T_len, U_len, sv, loss, s)
               : launch_ab<false>(sh, T_len, U_len, sv, loss, s);

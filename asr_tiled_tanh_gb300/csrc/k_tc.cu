@@ -228,28 +228,10 @@ __device__ __forceinline__ void unpack32(const uint4 (&q)[4], float (&out)[32]) 
   }
 }
 
-// The warp's 32 rows x 32 bf16 columns (lane = row, q = its 64 bytes) written
-// to global memory at rows base_row .. +31, columns col0 .. +31 (ld elements
-// per row), through the warp's staging area: each store instruction then
-// covers 8 consecutive rows' 64-byte pieces instead of 32 scattered rows.
-__device__ __forceinline__ void store_rows_bf16(unsigned char* stg, const uint4 (&q)[4],
-                                                __nv_bfloat16* gbase, long long ld,
-                                                bool row_ok_mask_all) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * STAGE_PITCH + i * 16) = q[i];
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i * 8 + (lane >> 2), piece = lane & 3;
-    const uint4 x = *(const uint4*)(stg + r * STAGE_PITCH + piece * 16);
-    if (row_ok_mask_all) *(uint4*)(gbase + (long long)r * ld + piece * 8) = x;
-  }
-  __syncwarp();
-}
-
-// Split form of load_rows_bf16: issue the coalesced global loads early, and
-// redistribute through the staging area when the values are needed.
+// The warp's 32 rows x 32 bf16 (columns col0 ..) of a row-major matrix, for
+// lane = row: issue_rows_bf16 starts coalesced loads (8 rows x 64 B per
+// instruction) early; finish_rows_bf16 redistributes them through the warp's
+// staging area (80-byte pitch) when the values are needed.
 __device__ __forceinline__ void issue_rows_bf16(const __nv_bfloat16* gbase, long long ld,
                                                 uint4 (&x)[4]) {
   const int lane = threadIdx.x & 31;
@@ -262,29 +244,6 @@ __device__ __forceinline__ void issue_rows_bf16(const __nv_bfloat16* gbase, long
 __device__ __forceinline__ void finish_rows_bf16(unsigned char* stg, const uint4 (&x)[4],
                                                  uint4 (&q)[4]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i * 8 + (lane >> 2), piece = lane & 3;
-    *(uint4*)(stg + r * STAGE_PITCH + piece * 16) = x[i];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = *(const uint4*)(stg + lane * STAGE_PITCH + i * 16);
-  __syncwarp();
-}
-
-// The reverse: each lane gets its own row's 32 bf16 (64 bytes) of rows
-// base_row .. +31, loaded with 8 rows per instruction and redistributed
-// through the staging area.
-__device__ __forceinline__ void load_rows_bf16(unsigned char* stg, const __nv_bfloat16* gbase,
-                                               long long ld, uint4 (&q)[4]) {
-  const int lane = threadIdx.x & 31;
-  uint4 x[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i * 8 + (lane >> 2), piece = lane & 3;
-    x[i] = __ldg((const uint4*)(gbase + (long long)r * ld + piece * 8));
-  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2), piece = lane & 3;
@@ -989,6 +948,12 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
   }
 }
 
+cudaError_t launch_build_z_bf16(const ChunkArgs& c, const float* pA, const float* pL,
+                                __nv_bfloat16* Z, cudaStream_t s) {
+  k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+  return cudaGetLastError();
+}
+
 // Per-row records for the dh epilogue (f^W_4, Eq. 10): with the posteriors
 // pb = exp(alpha + lpb + beta(t+1,u) - lnP) and pl = exp(alpha + lpl +
 // beta(t,u+1) - lnP) (beta(T_b,U_b) := 0, beta(T_b,u<U_b) := -inf, pl = 0 on
@@ -1467,8 +1432,7 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     {
       ProfScope ps("tc_build_z", s);
-      k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
-      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_build_z_bf16(c, pA, pL, Z, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
     ProfScope ps("tc_fwd_tiles", s);
     GemmDesc g{Z, 0, pr->WO, 0, (int)p.chunk_rows, p.V, p.H};
@@ -1518,8 +1482,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
         }
         {
           ProfScope ps("tc_build_z", s);
-          k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
-          if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+          if (launch_build_z_bf16(c, pA, pL, Z, s) != cudaSuccess) return RNNT_ERR_CUDA;
         }
         if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
       }

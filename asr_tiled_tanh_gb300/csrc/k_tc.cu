@@ -903,10 +903,11 @@ namespace {
 
 // z rows of a chunk in bf16: tanh(pA[b,t] + pL[b,u]) (joint network, Eq. 3-4),
 // 0 on rows outside the lattice.  One block per tile; a thread item is one
-// frame t of the tile and 8 consecutive h: the frame's pA values are loaded
+// frame t of the tile and 4 consecutive h: the frame's pA values are loaded
 // once and combined with the tile's 8 label positions (their pL rows stay in
 // L1 for the whole block), so L2 serves 48 KB of projections per 128 KB tile
-// of z (H = 512) instead of 512 KB.
+// of z (H = 512) instead of 512 KB.  Lanes take consecutive 16-byte pieces,
+// so every load instruction covers 512 contiguous bytes.
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
@@ -915,35 +916,28 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
   if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
   __syncthreads();
   const int H = c.sh.H;
-  const int H8 = H / 8;
+  const int H4 = H / 4;
   const long long row0 = (long long)blockIdx.x * TILE;
   using ptx::pack_bf16x2;
   using ptx::tanh_approx;
-  for (int e = threadIdx.x; e < TT * H8; e += blockDim.x) {
-    const int ti = e / H8, k8 = (e % H8) * 8;
+  for (int e = threadIdx.x; e < TT * H4; e += blockDim.x) {
+    const int ti = e / H4, k4 = (e % H4) * 4;
     const int t = tr.t0 + ti;
     const bool t_ok = tr.exists && t < tr.Tb;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    if (t_ok) {
-      const float4* a = (const float4*)(pA + ((size_t)tr.b * c.sh.T + t) * H + k8);
-      a0 = a[0];
-      a1 = a[1];
-    }
-    __nv_bfloat16* zrow = Z + (row0 + ti * TU) * H + k8;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t_ok) a = __ldg((const float4*)(pA + ((size_t)tr.b * c.sh.T + t) * H + k4));
+    __nv_bfloat16* zrow = Z + (row0 + ti * TU) * H + k4;
+    const float* lrow = pL + ((size_t)tr.b * c.sh.U1 + tr.u0) * H + k4;
 #pragma unroll
     for (int ui = 0; ui < TU; ++ui) {
-      const int u = tr.u0 + ui;
-      uint4 out = make_uint4(0, 0, 0, 0);
-      if (t_ok && u <= tr.Ub) {
-        const float4* l = (const float4*)(pL + ((size_t)tr.b * c.sh.U1 + u) * H + k8);
-        const float4 l0 = l[0], l1 = l[1];
+      uint2 out = make_uint2(0, 0);
+      if (t_ok && tr.u0 + ui <= tr.Ub) {
+        const float4 l = __ldg((const float4*)(lrow + (size_t)ui * H));
         // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
-        out.x = pack_bf16x2(tanh_approx(a0.x + l0.x), tanh_approx(a0.y + l0.y));
-        out.y = pack_bf16x2(tanh_approx(a0.z + l0.z), tanh_approx(a0.w + l0.w));
-        out.z = pack_bf16x2(tanh_approx(a1.x + l1.x), tanh_approx(a1.y + l1.y));
-        out.w = pack_bf16x2(tanh_approx(a1.z + l1.z), tanh_approx(a1.w + l1.w));
+        out.x = pack_bf16x2(tanh_approx(a.x + l.x), tanh_approx(a.y + l.y));
+        out.y = pack_bf16x2(tanh_approx(a.z + l.z), tanh_approx(a.w + l.w));
       }
-      *(uint4*)(zrow + (long long)ui * H) = out;
+      *(uint2*)(zrow + (long long)ui * H) = out;
     }
   }
 }
@@ -1353,8 +1347,12 @@ int pick_splits(int units_mn, int K) {
   return best;
 }
 
-// Cluster size of the lattice GEMMs (scores, dh, dz, dW^O).
-constexpr int kClusterLattice = 2;
+// Cluster size of the lattice GEMMs (scores, dh, dz, dW^O) and the
+// encoder-side weight gradients.  Measured on GB300: 2-CTA clusters sharing
+// B over multicast gave no gain (the kernels are not L2-bound) and pair the
+// CTAs' unit schedules, so single CTAs are used; the cluster path stays
+// available (and tested) for larger B tiles.
+constexpr int kClusterLattice = 1;
 
 #define TC_CHECK(expr)                                   \
   do {                                                   \

@@ -294,26 +294,32 @@ __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const
   if (!rc.valid) return;
   const int nv = min(32, p.N - col0);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] += bb[j];
+  for (int j = 0; j < 32; j += 2) {
+    const float2 x = __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bb[j], bb[j + 1]));
+    v[j] = x.x;
+    v[j + 1] = x.y;
+  }
   if (nv < 32) {  // columns past V take no part in the sum
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = (j < nv) ? v[j] : -INFINITY;
   }
-  float cm = v[0];
+  float cm = fmaxf(v[0], v[1]);
 #pragma unroll
-  for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
+  for (int j = 2; j < 32; j += 2) cm = ptx::max3(cm, v[j], v[j + 1]);
   const float nm = fmaxf(st.run_max, cm);
   float s = st.run_sum * ptx::ex2((st.run_max - nm) * kLog2e);
   const float nmL = nm * kLog2e;
-  float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  const float2 l2 = make_float2(kLog2e, kLog2e), m2 = make_float2(-nmL, -nmL);
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
-    s += ptx::ex2(fmaf(v[j], kLog2e, -nmL));
-    s1 += ptx::ex2(fmaf(v[j + 1], kLog2e, -nmL));
-    s2 += ptx::ex2(fmaf(v[j + 2], kLog2e, -nmL));
-    s3 += ptx::ex2(fmaf(v[j + 3], kLog2e, -nmL));
+    const float2 y0 = __ffma2_rn(make_float2(v[j], v[j + 1]), l2, m2);
+    const float2 y1 = __ffma2_rn(make_float2(v[j + 2], v[j + 3]), l2, m2);
+    a0 = __fadd2_rn(a0, make_float2(ptx::ex2(y0.x), ptx::ex2(y0.y)));
+    a1 = __fadd2_rn(a1, make_float2(ptx::ex2(y1.x), ptx::ex2(y1.y)));
   }
-  s += (s1 + s2) + s3;
+  a0 = __fadd2_rn(a0, a1);
+  s += a0.x + a0.y;
   st.run_sum = s;
   st.run_max = nm;
   const int jb = p.ch.sh.blank - col0;
@@ -377,6 +383,8 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   if (rc.valid) {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
+    // (pairs of columns through the packed fp32 add / fma)
+    const float2 l2 = make_float2(kLog2e, kLog2e), g2 = make_float2(st.lgn, st.lgn);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t w[4] = {bq[i].x, bq[i].y, bq[i].z, bq[i].w};
@@ -384,8 +392,11 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       for (int k = 0; k < 4; ++k) {
         float& d0 = d[8 * i + 2 * k];
         float& d1 = d[8 * i + 2 * k + 1];
-        d0 = ptx::ex2(fmaf(d0 + ptx::bf16lo(w[k]), kLog2e, st.lgn));
-        d1 = ptx::ex2(fmaf(d1 + ptx::bf16hi(w[k]), kLog2e, st.lgn));
+        const float2 x = __fadd2_rn(make_float2(d0, d1),
+                                    make_float2(ptx::bf16lo(w[k]), ptx::bf16hi(w[k])));
+        const float2 y = __ffma2_rn(x, l2, g2);
+        d0 = ptx::ex2(y.x);
+        d1 = ptx::ex2(y.y);
       }
     }
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
@@ -432,10 +443,9 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       for (int e = 0; e < 2; ++e)
 #pragma unroll
         for (int q = 0; q < 4; ++q) ad[e][q] = a0 + 64 * (e ^ h) + (((k >> 2) ^ q) << 4);
-      float s0 = 0.f, s1 = 0.f;
+      float2 acc = make_float2(0.f, 0.f);
       auto add = [&](uint32_t w) {
-        s0 += ptx::bf16lo(w);
-        s1 += ptx::bf16hi(w);
+        acc = __fadd2_rn(acc, make_float2(ptx::bf16lo(w), ptx::bf16hi(w)));
       };
       // q = 0..7: rows 2q, 2q+1 of the half; q & 3 selects the address, q / 4 the offset
       add(ptx::lds32<0>(ad[0][0]));   add(ptx::lds32<0>(ad[1][0]));
@@ -446,6 +456,7 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       add(ptx::lds32<640>(ad[0][1])); add(ptx::lds32<640>(ad[1][1]));
       add(ptx::lds32<768>(ad[0][2])); add(ptx::lds32<768>(ad[1][2]));
       add(ptx::lds32<896>(ad[0][3])); add(ptx::lds32<896>(ad[1][3]));
+      float s0 = acc.x, s1 = acc.y;
       s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
       s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
       if (h == 0 && col0 + 2 * k < p.N) ptx::red_add_v2(p.dbO + col0 + 2 * k, s0, s1);

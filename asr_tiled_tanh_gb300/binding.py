@@ -24,9 +24,9 @@ RNNT_F32, RNNT_BF16 = 0, 1
 RNNT_TILED, RNNT_UNTILED = 0, 1
 
 # Every symbol include/rnnt.h declares.
-EXPORTS = ("rnnt_saved_bytes", "rnnt_saved_layout", "rnnt_workspace_bytes", "rnnt_fwd",
-           "rnnt_bwd", "rnnt_device_status", "rnnt_status_string", "rnnt_profile_start",
-           "rnnt_profile_stop", "rnnt_profile_entry")
+EXPORTS = ("rnnt_saved_bytes", "rnnt_saved_layout", "rnnt_workspace_bytes",
+           "rnnt_graph_capturable", "rnnt_fwd", "rnnt_bwd", "rnnt_device_status",
+           "rnnt_status_string", "rnnt_profile_start", "rnnt_profile_stop", "rnnt_profile_entry")
 
 
 class RnntError(RuntimeError):
@@ -76,6 +76,8 @@ def load(build_if_missing: bool = False):
     lib.rnnt_saved_bytes.argtypes = [D]
     lib.rnnt_workspace_bytes.restype = S
     lib.rnnt_workspace_bytes.argtypes = [D]
+    lib.rnnt_graph_capturable.restype = ctypes.c_int
+    lib.rnnt_graph_capturable.argtypes = [D]
     lib.rnnt_saved_layout.restype = ctypes.c_int
     lib.rnnt_saved_layout.argtypes = [D, ctypes.POINTER(RnntSavedOffsets)]
     lib.rnnt_fwd.restype = ctypes.c_int
@@ -144,6 +146,12 @@ def rnnt_saved_bytes(dims: RnntDims) -> int:
 
 def rnnt_workspace_bytes(dims: RnntDims) -> int:
     return int(load().rnnt_workspace_bytes(ctypes.byref(dims)))
+
+
+def rnnt_graph_capturable(dims: RnntDims) -> int:
+    """1 if rnnt_fwd / rnnt_bwd for dims make no host synchronization (they
+    can be captured into a CUDA graph), 0 if not, -1 for invalid dims."""
+    return int(load().rnnt_graph_capturable(ctypes.byref(dims)))
 
 
 def rnnt_saved_layout(dims: RnntDims) -> RnntSavedOffsets:

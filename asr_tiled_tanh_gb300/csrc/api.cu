@@ -254,6 +254,12 @@ size_t rnnt_workspace_bytes(const rnnt_dims* dims) {
   return make_plan(dims, &p) ? p.w_total : 0;
 }
 
+int rnnt_graph_capturable(const rnnt_dims* dims) {
+  Plan p;
+  if (!make_plan(dims, &p)) return -1;
+  return cdiv(p.max_tiles, p.chunk_tiles) <= 1 ? 1 : 0;
+}
+
 rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out) {
   Plan p;
   if (!out || !make_plan(dims, &p)) return RNNT_ERR_INVALID_ARG;

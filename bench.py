@@ -14,6 +14,13 @@ back; the parameters and their gradients stay on the device, where a training
 step keeps them.  Each rank runs its own batch (weak
 scaling); there is no data-path collective.  L2 is flushed (256 MiB write)
 before every timed step, outside the step's events.
+
+When the library reports the plan capturable (rnnt_graph_capturable: the
+whole lattice fits one chunk, so the calls make no host synchronization), the
+timed steps replay a CUDA graph of the step (`config.execution`); `--eager`
+launches them one by one instead.  A second, eager run of the same number of
+steps with every kernel bracketed by CUDA events on its own stream gives the
+per-kernel times (`kernel_shares`, `roofline`) and `gpu_launches`.
 """
 from __future__ import annotations
 
@@ -177,11 +184,25 @@ def run_gpu_bench(args):
     stream = torch.cuda.current_stream()
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
 
-    def step():
-        r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
-              stream=stream)
+    def step(s=stream):
+        r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss, stream=s)
         r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads,
-              stream=stream)
+              stream=s)
+
+    def captured(fn):
+        """fn (which launches on the stream it is given) as a CUDA graph whose
+        replay runs on the current stream."""
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            fn(cap)  # warm-up on the capture stream
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn(cap)
+        torch.cuda.synchronize()
+        return g
 
     for _ in range(args.warmup):
         step()
@@ -190,32 +211,45 @@ def run_gpu_bench(args):
     if code != 0:
         raise SystemExit(f"device status {code} word {word}")
 
+    # A plan whose calls make no host synchronization (the whole lattice fits
+    # one chunk of the tile buffers) is replayed as a CUDA graph of the step.
+    use_graph = not args.eager and rn.rnnt_graph_capturable(r.dims) == 1
+    graph = captured(step) if use_graph else None
+    run = graph.replay if graph is not None else step
+
+    def timed_region(fn, profile):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if profile:
+            rn.rnnt_profile_start(1 << 16)
+        with ClockSampler(dev.index) as clk:
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                if args.flush_mb > 0:
+                    flush.fill_(i & 0xff)
+                starts[i].record(stream)
+                fn()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+        prof = rn.rnnt_profile_stop() if profile else None
+        if dist:
+            dist.barrier()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return sum(step_ms) / len(step_ms), clk, wall, prof
+
     # --- timed region: device-resident inputs ---------------------------------
     torch.cuda.reset_peak_memory_stats(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    rn.rnnt_profile_start(1 << 16)
-    with ClockSampler(dev.index) as clk:
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            if args.flush_mb > 0:
-                flush.fill_(i & 0xff)
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    prof = rn.rnnt_profile_stop()
-    if dist:
-        dist.barrier()
+    ms, clk, wall, _ = timed_region(run, profile=False)
     peak_bytes = torch.cuda.max_memory_allocated(dev)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(step_ms) / len(step_ms)
     ms_max = reduce_max(ms, dist, dev)
     value = job_value(nominal, world, ms_max)
+    # --- the same steps again, eager, with every kernel bracketed by CUDA
+    # events on its own stream: per-kernel times, shares and launch counts
+    prof_ms, _, _, prof = timed_region(step, profile=True)
 
     # --- e2e: host buffers through the C ABI ----------------------------------
     e2e_ms, h2d, d2h = None, 0, 0
@@ -226,15 +260,17 @@ def run_gpu_bench(args):
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = host_loss.numel() * 4
 
-        def e2e_step():
-            for k, v in host_in.items():
-                d[k].copy_(v, non_blocking=True)
-            step()
-            host_loss.copy_(loss, non_blocking=True)
+        def e2e_step(s=stream):
+            with torch.cuda.stream(s):
+                for k, v in host_in.items():
+                    d[k].copy_(v, non_blocking=True)
+                step(s)
+                host_loss.copy_(loss, non_blocking=True)
 
         for _ in range(max(1, args.warmup // 2)):
             e2e_step()
         torch.cuda.synchronize()
+        e2e_run = captured(e2e_step).replay if use_graph else e2e_step
         es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         if dist:
@@ -242,7 +278,7 @@ def run_gpu_bench(args):
         for i in range(args.steps):
             flush.fill_(i & 0xff)
             es[i].record(stream)
-            e2e_step()
+            e2e_run()
             ee[i].record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps, dist, dev)
@@ -287,6 +323,7 @@ def run_gpu_bench(args):
                    "H": wl.H, "V": wl.V, "tile_cells": int(r.dims.tile_cells),
                    "nominal_cells": nominal, "valid_cells": valid,
                    "l2": "flushed (256 MiB write) before each timed step",
+                   "execution": "CUDA graph of the step" if graph is not None else "eager",
                    "parallelism": f"replicas x{world}"},
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
@@ -298,6 +335,7 @@ def run_gpu_bench(args):
         "gpu_launches": int(launches),
         "roofline": roof,
         "kernel_shares": shares,
+        "profiled_ms_per_step": round(prof_ms, 4),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
     }
@@ -384,6 +422,8 @@ def main():
     ap.add_argument("--flush-mb", type=int, default=256,
                     help="L2 flush buffer written before each timed step (0: none; profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3

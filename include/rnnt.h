@@ -129,6 +129,17 @@ rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out);
  * rnnt_fwd to rnnt_bwd) and 256-byte alignment. */
 size_t rnnt_workspace_bytes(const rnnt_dims* dims);
 
+/* Whether rnnt_fwd and rnnt_bwd for dims run entirely as stream work, with
+ * no host-side synchronization, so that a caller can capture them into a
+ * CUDA graph: true when every possible lattice tile fits one chunk of the
+ * tile buffers (tiled mode with the default or a large enough tile_cells,
+ * and untiled mode); otherwise each call reads the actual tile count back to
+ * the host once.  The side streams the library forks from `stream` are
+ * joined back before each call returns, which capture supports.  Returns 1,
+ * 0, or -1 if dims are invalid.  (Not a method step: the pages have no
+ * counterpart.) */
+int rnnt_graph_capturable(const rnnt_dims* dims);
+
 /* Forward pass.  Inputs: hA [B,T,HA], hL [B,U1,HL], params, labels [B,U1]
  * int32, T_len [B], U_len [B] int32.  Outputs: loss [B] fp32 = -ln P(y_b|x_b)
  * (the batch loss of Eq. 9 is their sum), and `saved` (rnnt_saved_bytes,

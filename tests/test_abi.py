@@ -92,3 +92,12 @@ def test_untiled_saved_grows_with_lattice(lib):
     assert rn.rnnt_saved_bytes(small) > 8 * 200 * 51 * 1024 * 2
     # tiled: 20 B per position + the fp32 joint projections, nothing per vocabulary entry
     assert rn.rnnt_saved_bytes(tiled) < 8 * 200 * 51 * 24 + 4 * (8 * 200 + 8 * 51) * 512 + 65536
+
+
+def test_graph_capturable_follows_the_chunking(lib):
+    kw = dict(B=8, T=200, U1=51, HA=512, HL=512, H=512, V=1024, blank=0, dtype=rn.RNNT_BF16)
+    assert rn.rnnt_graph_capturable(rn.make_dims(**kw, mode=rn.RNNT_TILED)) == 1
+    assert rn.rnnt_graph_capturable(rn.make_dims(**kw, mode=rn.RNNT_UNTILED)) == 1
+    # one tile per chunk: the calls read the tile count back, no capture
+    assert rn.rnnt_graph_capturable(rn.make_dims(**kw, mode=rn.RNNT_TILED, tile_cells=128)) == 0
+    assert rn.rnnt_graph_capturable(rn.make_dims(**dict(kw, T=0), mode=rn.RNNT_TILED)) == -1

@@ -55,6 +55,20 @@ def test_fp32_many_chunks_and_untiled_agree():
     np.testing.assert_array_equal(one_tile["loss"], untiled["loss"])
 
 
+def test_fp32_long_label_sequences_split_over_warps():
+    # U+1 > 32 with few samples: the alpha/beta recursion of a sample is split
+    # over two warps (fp32 arithmetic), and over four for U+1 > 64
+    for U in (40, 90):
+        inp = synthetic.custom(B=3, T=30, U=U, HA=32, HL=32, H=32, V=40, dtype="f32", seed=U,
+                               bias_std=0.2)
+        gpu = run_gpu(inp)
+        orc = run_oracle(inp)
+        assert_parity(gpu, orc, inp)
+        m = valid_mask(inp)
+        for k in ("alpha", "beta"):
+            np.testing.assert_allclose(gpu[k][m], getattr(orc, k)[m], rtol=2e-5, atol=2e-5)
+
+
 def test_small_bf16_workload():
     inp = synthetic.make("small")
     gpu = run_gpu(inp)
@@ -222,3 +236,39 @@ def test_host_checked_errors():
     code = rn.rnnt_fwd(r.dims, dev["hA"], dev["hL"], bad_params, dev["labels"], dev["T_len"],
                        dev["U_len"], loss, r.saved, r.ws, check=False)
     assert code == 1
+
+
+def test_cuda_graph_capture_matches_eager():
+    # a single-chunk plan runs as stream work only: fwd + bwd captured into a
+    # CUDA graph (side streams and all) and replayed give the eager results
+    inp = synthetic.custom(B=4, T=48, U=12, HA=64, HL=96, H=128, V=256, dtype="bf16", seed=11,
+                           bias_std=0.2)
+    dev = to_device(inp)
+    r = rn.Rnnt.for_inputs(inp)
+    assert rn.rnnt_graph_capturable(r.dims) == 1
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    args = (dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    loss_e = r.fwd(*args).clone()
+    grads_e = {k: v.clone() for k, v in r.bwd(*args).items()}
+    torch.cuda.synchronize()
+    loss = torch.empty_like(loss_e)
+    grads = r.alloc_grads()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        r.fwd(*args, loss=loss, stream=s)
+        r.bwd(*args, grads=grads, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        r.fwd(*args, loss=loss, stream=s)
+        r.bwd(*args, grads=grads, stream=s)
+    for v in grads.values():
+        v.fill_(float("nan"))
+    loss.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(loss, loss_e)
+    for k in GRAD_KEYS:
+        assert rel_l2(grads[k].cpu().numpy(), grads_e[k].cpu().numpy()) < 1e-5, k

@@ -477,22 +477,6 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
   constexpr int STAGES = C::STAGES;
-  // units that hold actual lattice tiles: a prefix of the unit order (M
-  // groups, resp. K splits, are the slow index), read from the tile count
-  int units = p.units, kb_lim = p.kb_total;
-  if (p.tiles_on != TILES_NONE) {
-    const long long have = max(0LL, min(p.ch.ntiles, (long long)*p.ch.sv.total_tiles -
-                                                         p.ch.first_tile));
-    if (p.tiles_on == TILES_ON_M) {
-      const int groups = (int)((have + CL - 1) / CL);
-      // (row-complete: the V split is the fast index; otherwise N, with no K split)
-      units = min(units, groups * (p.row_complete ? max(1, p.n_split) : p.n_tiles) * CL);
-    } else {
-      kb_lim = (int)min((long long)p.kb_total, have * (BM / BK));
-      const int splits = (kb_lim + p.kb_per_split - 1) / p.kb_per_split;
-      units = min(units, splits * p.m_groups * p.n_tiles * CL);
-    }
-  }
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
@@ -537,6 +521,26 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   if (CL > 1) ptx::cluster_sync();  // peers' barriers are initialised before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Launched as the programmatic dependent of the stream's previous kernel:
+  // the set-up above overlapped its tail; its results are read only from here.
+  ptx::griddep_wait();
+  ptx::griddep_launch();
+  // units that hold actual lattice tiles: a prefix of the unit order (M
+  // groups, resp. K splits, are the slow index), read from the tile count
+  int units = p.units, kb_lim = p.kb_total;
+  if (p.tiles_on != TILES_NONE) {
+    const long long have = max(0LL, min(p.ch.ntiles, (long long)*p.ch.sv.total_tiles -
+                                                         p.ch.first_tile));
+    if (p.tiles_on == TILES_ON_M) {
+      const int groups = (int)((have + CL - 1) / CL);
+      // (row-complete: the V split is the fast index; otherwise N, with no K split)
+      units = min(units, groups * (p.row_complete ? max(1, p.n_split) : p.n_tiles) * CL);
+    } else {
+      kb_lim = (int)min((long long)p.kb_total, have * (BM / BK));
+      const int splits = (kb_lim + p.kb_per_split - 1) / p.kb_per_split;
+      units = min(units, splits * p.m_groups * p.n_tiles * CL);
+    }
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -922,6 +926,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
+  ptx::griddep_launch();  // the GEMM that follows may start its set-up
   if (!tile_in_use(c, blockIdx.x)) return;
   __shared__ TileRef tr;
   if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
@@ -1264,22 +1269,22 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   if (groups <= 0 || g.K <= 0) return cudaSuccess;
   const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
   const int grid_groups = std::min(groups, cap);
-  if (CL == 1) {
-    kern<<<grid_groups, C::THREADS, C::SMEM, s>>>(ta, tb, tc, p);
-    return cudaGetLastError();
-  }
+  // programmatic dependent launch: the kernel's set-up (barriers, TMEM,
+  // descriptor prefetch) may overlap the tail of the stream's previous kernel
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(grid_groups * CL);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 

@@ -119,6 +119,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// Wait until the grids this one depends on (the preceding kernel of the
+// stream, when this kernel was launched as its programmatic dependent) have
+// completed and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the stream's next kernel, if launched as a programmatic dependent,
+// start (it still waits for this grid's completion before reading its data).
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- clusters -------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -412,12 +412,15 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
 
   if (p.tc) {
-    // (the preparation runs beside the first chunk's z rebuild)
+    // (the preparation runs beside the first chunk's z rebuild, the
+    // encoder-side gradients beside the last chunk's dW^O)
     const PreLaunch pre = prepare;
+    const PreLaunch enc = [&](cudaStream_t es) {
+      return tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ,
+                              es);
+    };
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, st);
-    if (s != RNNT_OK) return s;
-    s = tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ, st);
+                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, &enc, st);
     return s;
   }
 

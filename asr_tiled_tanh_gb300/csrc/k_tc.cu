@@ -1467,7 +1467,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
                               const float* grad_loss, const float* pA, const float* pL, void* Zv,
                               void* Hv, bool untiled, float* dA, float* dLr, float* dWO,
                               float* dbO, float4* post, const PreLaunch* pre,
-                              cudaStream_t s) {
+                              const PreLaunch* after, cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
   long long nch = 0;
@@ -1478,6 +1478,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
     st = (*pre)(s);
     if (st != RNNT_OK) return st;
   }
+  if (nch == 0 && after) return (*after)(s);
   for (long long k = 0; k < nch; ++k) {
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     if (!untiled) {
@@ -1544,8 +1545,12 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), kClusterLattice, s) != cudaSuccess)
         return RNNT_ERR_CUDA;
     }
+    // the last chunk's dW^O runs beside the caller's work that needs only
+    // dA and dLr (the encoder-side gradients)
+    const bool last = k + 1 == nch;
+    Fork fork(s, last && after && dWO ? 1 : 0);
     if (dWO) {  // dW^O += dh^T z, split over the chunk's rows
-      ProfScope ps("tc_bwd_dwo", s);
+      ProfScope ps("tc_bwd_dwo", fork.side(0));
       GemmDesc g{Hs, 1, Z, 1, p.V, p.H, rows};
       TcParams tp{};
       const int bn = pick_bn(p.H);
@@ -1555,8 +1560,14 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.status = sv.status;
       tp.ch = c;
       tp.tiles_on = TILES_ON_K;
-      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, fork.side(0)) != cudaSuccess)
+        return RNNT_ERR_CUDA;
     }
+    if (last && after) {
+      st = (*after)(s);
+      if (st != RNNT_OK) return st;
+    }
+    if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
   }
   return RNNT_OK;
 }

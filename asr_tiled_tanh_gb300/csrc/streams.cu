@@ -8,12 +8,13 @@ constexpr int kMaxDevices = 64;
 struct DeviceStreams {
   bool tried = false;
   bool ok = false;
-  cudaStream_t side[kMaxSide] = {};
-  cudaEvent_t fork = nullptr;
-  cudaEvent_t join[kMaxSide] = {};
+  cudaStream_t side[kMaxDepth][kMaxSide] = {};
+  cudaEvent_t fork[kMaxDepth] = {};
+  cudaEvent_t join[kMaxDepth][kMaxSide] = {};
 };
 DeviceStreams g_dev[kMaxDevices];
-std::mutex g_mu;
+std::recursive_mutex g_mu;
+thread_local int t_depth = 0;  // forks this thread has open
 
 // Streams and events of the current device, created on first use (lock held).
 DeviceStreams* device_streams() {
@@ -22,10 +23,13 @@ DeviceStreams* device_streams() {
   DeviceStreams& d = g_dev[dev];
   if (!d.tried) {
     d.tried = true;
-    bool ok = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; i < kMaxSide && ok; ++i) {
-      ok = cudaStreamCreateWithFlags(&d.side[i], cudaStreamNonBlocking) == cudaSuccess &&
-           cudaEventCreateWithFlags(&d.join[i], cudaEventDisableTiming) == cudaSuccess;
+    bool ok = true;
+    for (int l = 0; l < kMaxDepth && ok; ++l) {
+      ok = cudaEventCreateWithFlags(&d.fork[l], cudaEventDisableTiming) == cudaSuccess;
+      for (int i = 0; i < kMaxSide && ok; ++i) {
+        ok = cudaStreamCreateWithFlags(&d.side[l][i], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&d.join[l][i], cudaEventDisableTiming) == cudaSuccess;
+      }
     }
     d.ok = ok;
   }
@@ -35,22 +39,23 @@ DeviceStreams* device_streams() {
 }  // namespace
 
 Fork::Fork(cudaStream_t main, int n) : main_(main), lock_(g_mu, std::try_to_lock) {
-  // a fork already open (another thread's, or an enclosing one) means this
-  // one runs everything on main
-  if (n <= 0 || !lock_.owns_lock()) return;
+  // another thread's forks are open: run everything on main
+  if (!lock_.owns_lock()) return;
+  depth_ = t_depth++;
+  if (n <= 0 || depth_ >= kMaxDepth) return;
   if (n > kMaxSide) n = kMaxSide;
   DeviceStreams* d = device_streams();
-  if (!d || cudaEventRecord(d->fork, main) != cudaSuccess) return;
-  for (int i = 0; i < n; ++i) {
-    if (cudaStreamWaitEvent(d->side[i], d->fork, 0) != cudaSuccess) {
-      // the streams that already wait are joined back; the rest run on main
-      n_ = i;
-      for (int k = 0; k < n_; ++k) { sides_[k] = d->side[k]; joins_[k] = d->join[k]; }
-      return;
-    }
+  if (!d || cudaEventRecord(d->fork[depth_], main) != cudaSuccess) return;
+  int ready = 0;
+  while (ready < n && cudaStreamWaitEvent(d->side[depth_][ready], d->fork[depth_], 0) ==
+                          cudaSuccess)
+    ++ready;
+  // the streams that wait are joined back; the rest of the work runs on main
+  n_ = ready;
+  for (int k = 0; k < n_; ++k) {
+    sides_[k] = d->side[depth_][k];
+    joins_[k] = d->join[depth_][k];
   }
-  n_ = n;
-  for (int k = 0; k < n_; ++k) { sides_[k] = d->side[k]; joins_[k] = d->join[k]; }
 }
 
 cudaError_t Fork::join() {
@@ -65,6 +70,9 @@ cudaError_t Fork::join() {
   return err;
 }
 
-Fork::~Fork() { join(); }
+Fork::~Fork() {
+  join();
+  if (depth_ >= 0) --t_depth;
+}
 
 }  // namespace rnnt

@@ -6,7 +6,8 @@
 
 namespace rnnt {
 
-constexpr int kMaxSide = 3;
+constexpr int kMaxSide = 3;   // side streams of one fork
+constexpr int kMaxDepth = 2;  // forks open at once in one thread (nested)
 
 // Launches of one library call that do not depend on one another can run at
 // the same time on up to kMaxSide side streams.  The constructor makes each
@@ -14,11 +15,13 @@ constexpr int kMaxSide = 3;
 // destructor) makes `main` wait for everything enqueued on the side streams,
 // so the call stays ordered on `main` as a whole and works under stream
 // capture.  The side streams and events are created once per device, on the
-// first fork made with that device current.  One fork is open at a time in
-// the process (a lock held from fork to join, so that calls from several
-// host threads never interleave their event records); a fork made while
-// another is open, or when n is 0 or the streams cannot be created, has
-// side() return `main`, and its launches simply run one after another.
+// first fork made with that device current, one set per nesting level: a
+// fork opened while another is open in the same thread (its `main` may be a
+// side stream of the outer one) uses the next level's streams.  Calls from
+// other host threads wait for nothing: while one thread has forks open, a
+// fork made in another thread (or past kMaxDepth levels, or when n is 0 or
+// the streams cannot be created) has side() return `main`, and its launches
+// simply run one after another.
 class Fork {
  public:
   Fork(cudaStream_t main, int n);
@@ -33,8 +36,9 @@ class Fork {
   cudaStream_t sides_[kMaxSide] = {};
   cudaEvent_t joins_[kMaxSide] = {};
   int n_ = 0;
+  int depth_ = -1;
   bool joined_ = false;
-  std::unique_lock<std::mutex> lock_;
+  std::unique_lock<std::recursive_mutex> lock_;
 };
 
 }  // namespace rnnt

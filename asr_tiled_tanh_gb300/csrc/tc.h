@@ -21,14 +21,17 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
                              cudaStream_t s);
 // Backward over every tile: dA, dLr (accumulated), dW^O, db^O.  post: the
 // per-row posterior records of one chunk (chunk_rows float4, tiled mode).
-// Launches a caller has the backward make on a side stream while the first
-// chunk's z is rebuilt (they must be done before the chunk's dh kernel).
+// Launches a caller has the backward make: `pre` on a side stream while the
+// first chunk's z is rebuilt (they must be done before the chunk's dh
+// kernel), `after` once the last chunk's dz is done (it may read dA, dLr),
+// beside that chunk's dW^O.
 using PreLaunch = std::function<rnnt_status(cudaStream_t)>;
 rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Z,
                               void* Hs, bool untiled, float* dA, float* dLr, float* dWO,
-                              float* dbO, float4* post, const PreLaunch* pre, cudaStream_t s);
+                              float* dbO, float4* post, const PreLaunch* pre,
+                              const PreLaunch* after, cudaStream_t s);
 // dh^A, dW^A, dh^L, dW^L, db^Z from dA and dLr.
 rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
                              const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,

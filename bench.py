@@ -172,6 +172,9 @@ def run_gpu_bench(args):
     rn.load(build_if_missing=True)
 
     wl = synthetic.WORKLOADS[args.workload]
+    if args.batch > 0:  # the workload's shapes and distributions with another batch size
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}-B{args.batch}", B=args.batch)
     inp = synthetic.make(wl, seed=wl.seed + 1000 * rank)
     valid = inp.valid_cells()
     nominal = wl.nominal_cells
@@ -422,6 +425,9 @@ def main():
     ap.add_argument("--flush-mb", type=int, default=256,
                     help="L2 flush buffer written before each timed step (0: none; profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="samples per batch (0: the workload's own B); for profiling on "
+                         "smaller cases of a workload's shapes")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()

@@ -8,18 +8,21 @@
 //   EPI_LSE    scores -> online log-sum-exp over V, blank/label log-probs
 //              (f^W_1 of Eq. 7 plus the gather of the two probabilities the
 //              Flash RNN-T kernel emits instead of a softmax)
-//   EPI_DH     scores -> dh = dL/dh (Eq. 10), written over the tile's score
-//              buffer ("it also overwrites the scores with their gradients")
+//   EPI_DH     scores -> dh = dL/dh (Eq. 10), written into the tile buffer
+//              that holds the scores in the untiled mode (Flash RNN-T blog,
+//              "Compute it, use it, make room": gradients replace scores)
 //   EPI_DA     dz -> da = dz (1 - z^2), reduced over u into dA[b,t] and over
 //              t into dLr[b,u] (joint-network backward, sample-wise paper §4)
 // Rows of the lattice GEMMs are lattice positions: M tile m of a chunk is the
 // 16 x 8 lattice tile (chunk's first tile + m), one position per TMEM lane.
 //
-// Roles (192 threads): warp 0 issues TMA loads into a ring of shared-memory
-// stages, warp 1 allocates TMEM and one thread issues tcgen05.mma into one of
-// two TMEM accumulators, warps 2-5 drain the other accumulator (tcgen05.ld)
-// through the epilogue.  mbarriers link the roles; every wait is bounded and a
-// timeout sets RNNT_ERR_TIMEOUT in the status word and winds the CTA down.
+// Roles: warp 0 issues TMA loads into a ring of shared-memory stages, warp 1
+// allocates TMEM and one thread issues tcgen05.mma into one of two TMEM
+// accumulators, and 8, 12 or 16 epilogue warps (by epilogue) drain the other
+// accumulator (tcgen05.ld).  mbarriers link the roles; every wait is bounded
+// and a timeout sets RNNT_ERR_TIMEOUT in the status word and winds the CTA
+// down.  Kernels launch as programmatic dependents of the stream's previous
+// kernel (set-up overlaps its tail; griddepcontrol.wait before any read).
 #include <cudaTypedefs.h>
 
 #include <algorithm>

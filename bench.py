@@ -111,13 +111,18 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
 
 
 def kernel_source_hash() -> str:
-    """sha1 of the tensor-core kernel sources (the ncu traffic figures are only
-    valid for the source they were captured from)."""
+    """sha1 of the tensor-core kernel sources with comments and whitespace
+    removed (the ncu traffic figures are only valid for the code they were
+    captured from)."""
     import hashlib
+    import re
     h = hashlib.sha1()
     for f in ("k_tc.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:12]
 
 

@@ -109,6 +109,28 @@ def test_unaligned_output_bias_gradient():
     assert rel_l2(g["dbO"].cpu().numpy(), aligned["dbO"]) < 1e-2
 
 
+@pytest.mark.parametrize("offset", [0, 1])
+def test_output_bias_gradient_without_weight_gradient(offset):
+    # dW^O not requested (NULL): db^O from the dh epilogue (aligned) or the
+    # separate column-sum pass (unaligned), the other gradients as usual
+    inp = synthetic.custom(B=5, T=40, U=11, HA=64, HL=64, H=128, V=264, dtype="bf16", seed=13,
+                           t_frac=0.2, u_frac=0.0, bias_std=0.2)
+    dev = to_device(inp)
+    r = rn.Rnnt.for_inputs(inp)
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    args = (dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    r.fwd(*args)
+    g = r.alloc_grads()
+    g["dWO"] = None
+    backing = torch.zeros(inp.wl.V + 4, dtype=torch.float32, device="cuda")
+    g["dbO"] = backing[offset:offset + inp.wl.V]
+    r.bwd(*args, grads=g)
+    torch.cuda.synchronize()
+    orc = run_oracle(inp)
+    for k in ("dbO", "dhA", "dhL", "dWA", "dWL", "dbZ"):
+        assert rel_l2(g[k].cpu().numpy(), orc.grads[k]) < 1e-2, k
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
     # Flash RNN-T: tiled and untiled execution compute the same thing.  The

@@ -920,50 +920,54 @@ namespace rnnt {
 namespace {
 
 // z rows of a chunk in bf16: tanh(pA[b,t] + pL[b,u]) (joint network, Eq. 3-4),
-// 0 on rows outside the lattice.  One block per tile; a thread item is one
-// frame t of the tile and 4 consecutive h: the frame's pA values are loaded
-// once and combined with the tile's 8 label positions (their pL rows stay in
-// L1 for the whole block), so L2 serves 48 KB of projections per 128 KB tile
-// of z (H = 512) instead of 512 KB.  Lanes take consecutive 16-byte pieces,
-// so every load instruction covers 512 contiguous bytes.
+// 0 on rows outside the lattice.  One block per tile; a thread owns 4
+// consecutive h (a column group, strided by the block size) and writes them
+// for all 128 positions of the tile: the tile's 8 pL rows are loaded once into
+// registers, each of its 16 pA rows once per frame, and the stores of a warp
+// cover 256 contiguous bytes of a z row.
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
                __nv_bfloat16* __restrict__ Z) {
   ptx::griddep_launch();  // the GEMM that follows may start its set-up
   if (!tile_in_use(c, blockIdx.x)) return;
-  __shared__ TileRef tr;
-  if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
-  __syncthreads();
-  const int H = c.sh.H;
-  const int H4 = H / 4;
-  const long long row0 = (long long)blockIdx.x * TILE;
+  const TileRef tr = tile_ref(c, blockIdx.x);
+  const int H = c.sh.H, H4 = H / 4;
+  const int nt = tr.exists ? min(TT, tr.Tb - tr.t0) : 0;      // frames of the tile in the lattice
+  const int nu = tr.exists ? min(TU, tr.Ub + 1 - tr.u0) : 0;  // label positions
+  const float* gA = pA + ((size_t)tr.b * c.sh.T + tr.t0) * H;
+  const float* gL = pL + ((size_t)tr.b * c.sh.U1 + tr.u0) * H;
   using ptx::pack_bf16x2;
   using ptx::tanh_approx;
-  for (int e = threadIdx.x; e < TT * H4; e += blockDim.x) {
-    const int ti = e / H4, k4 = (e % H4) * 4;
-    const int t = tr.t0 + ti;
-    const bool t_ok = tr.exists && t < tr.Tb;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t_ok) a = __ldg((const float4*)(pA + ((size_t)tr.b * c.sh.T + t) * H + k4));
-    __nv_bfloat16* zrow = Z + (row0 + ti * TU) * H + k4;
-    const float* lrow = pL + ((size_t)tr.b * c.sh.U1 + tr.u0) * H + k4;
+  for (int k4 = threadIdx.x; k4 < H4; k4 += blockDim.x) {
+    float4 l[TU];
 #pragma unroll
-    for (int ui = 0; ui < TU; ++ui) {
-      uint2 out = make_uint2(0, 0);
-      if (t_ok && tr.u0 + ui <= tr.Ub) {
-        const float4 l = __ldg((const float4*)(lrow + (size_t)ui * H));
-        // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
-        out.x = pack_bf16x2(tanh_approx(a.x + l.x), tanh_approx(a.y + l.y));
-        out.y = pack_bf16x2(tanh_approx(a.z + l.z), tanh_approx(a.w + l.w));
+    for (int ui = 0; ui < TU; ++ui)
+      l[ui] = ui < nu ? __ldg((const float4*)(gL + (size_t)ui * H) + k4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    __nv_bfloat16* z = Z + (long long)blockIdx.x * TILE * H + 4 * k4;
+#pragma unroll 2
+    for (int ti = 0; ti < TT; ++ti) {
+      const bool t_ok = ti < nt;
+      const float4 a = t_ok ? __ldg((const float4*)(gA + (size_t)ti * H) + k4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int ui = 0; ui < TU; ++ui) {
+        uint2 out = make_uint2(0, 0);
+        if (t_ok && ui < nu) {
+          // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
+          out.x = pack_bf16x2(tanh_approx(a.x + l[ui].x), tanh_approx(a.y + l[ui].y));
+          out.y = pack_bf16x2(tanh_approx(a.z + l[ui].z), tanh_approx(a.w + l[ui].w));
+        }
+        *(uint2*)(z + (long long)(ti * TU + ui) * H) = out;
       }
-      *(uint2*)(zrow + (long long)ui * H) = out;
     }
   }
 }
 
 cudaError_t launch_build_z_bf16(const ChunkArgs& c, const float* pA, const float* pL,
                                 __nv_bfloat16* Z, cudaStream_t s) {
-  k_build_z_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, pA, pL, Z);
+  const int threads = std::min(256, (int)cdiv(c.sh.H / 4, 32) * 32);
+  k_build_z_bf16<<<(unsigned)c.ntiles, threads, 0, s>>>(c, pA, pL, Z);
   return cudaGetLastError();
 }
 

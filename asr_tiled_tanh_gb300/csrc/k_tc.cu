@@ -352,7 +352,8 @@ __device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p
 // f^W_4 (Eq. 10): dh_v = g ((pb + pl) softmax_v - pb [v = blank] - pl [v = label]).
 struct DhState {
   float gpb, gpl;  // g pb, g pl
-  float lgn;       // log2(g (pb + pl)) - lnPD log2(e): g (pb+pl) softmax_v = 2^(h_v log2 e + lgn)
+  float lgn;       // log2|g (pb + pl)| - lnPD log2(e): |g (pb+pl)| softmax_v = 2^(h_v log2 e + lgn)
+  bool neg;        // g < 0 (the incoming gradient of the row's sample is negative)
   int lab;
 };
 
@@ -362,7 +363,8 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
   st.gpb = q.x;
   st.gpl = q.y;
   const float gg = q.x + q.y;
-  st.lgn = gg > 0.f ? ptx::lg2(gg) - q.z : -INFINITY;
+  st.lgn = gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY;
+  st.neg = gg < 0.f;
   st.lab = __float_as_int(q.w);
   return st;
 }
@@ -401,6 +403,10 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
         d0 = ptx::ex2(y.x);
         d1 = ptx::ex2(y.y);
       }
+    }
+    if (st.neg) {  // (uniform over the warp: a tile is one sample)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) d[j] = -d[j];
     }
     const int jb = p.ch.sh.blank - col0;   // uniform over the warp
     if (jb >= 0 && jb < 32) {

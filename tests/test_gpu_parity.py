@@ -294,3 +294,48 @@ def test_cuda_graph_capture_matches_eager():
     assert torch.equal(loss, loss_e)
     for k in GRAD_KEYS:
         assert rel_l2(grads[k].cpu().numpy(), grads_e[k].cpu().numpy()) < 1e-5, k
+
+
+@pytest.mark.parametrize("dtype,mode", [("f32", "tiled"), ("bf16", "tiled"), ("bf16", "untiled")])
+def test_negative_and_zero_incoming_gradients(dtype, mode):
+    # grad_loss of either sign (and 0): dh scales with g, so the gradients of
+    # sum_b g_b loss_b keep the sign of each g_b
+    inp = synthetic.custom(B=5, T=36, U=10, HA=48, HL=48, H=64, V=96, dtype=dtype, seed=19,
+                           bias_std=0.2)
+    g = np.array([1.0, -0.7, 0.0, -2.5, 0.3])
+    gpu = run_gpu(inp, mode=mode, grad_loss=g)
+    orc = run_oracle(inp, grad_loss=g)
+    assert_parity(gpu, orc, inp)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_label_sequences(dtype):
+    # U+1 = 301 > 128: the alpha/beta recursion takes the register-prefetch
+    # kernel (the shared-memory ring would not fit).  alpha and beta reach
+    # |ln P| ~ (T+U) ln V ~ 1.2e3 here, where one fp32 ulp is ~1.2e-4 in log
+    # space, so the posteriors exp(alpha + beta - ln P) - and every gradient -
+    # carry a relative error of a few 1e-4 on the fp32 path: gradients are held
+    # to 5e-4 there (the loss still to 1e-5)
+    inp = synthetic.custom(B=2, T=24, U=300, HA=32, HL=32, H=64, V=48, dtype=dtype, seed=23,
+                           bias_std=0.2)
+    gpu = run_gpu(inp)
+    orc = run_oracle(inp)
+    assert gpu["status"] == (0, 0)
+    assert_parity(gpu, orc, inp, grads=(dtype == "bf16"))
+    if dtype == "f32":
+        errs = {k: rel_l2(gpu[k], orc.grads[k]) for k in GRAD_KEYS}
+        assert max(errs.values()) < 5e-4, errs
+
+
+def test_labels_equal_to_blank_and_repeated():
+    # a label equal to the blank id is not an error: both dh terms hit column 0
+    inp = synthetic.custom(B=3, T=20, U=8, HA=32, HL=32, H=32, V=16, dtype="bf16", seed=29,
+                           bias_std=0.2)
+    labels = inp.labels.clone()
+    labels[0, 1:] = 0          # every label of sample 0 is the blank id
+    labels[1, 1:] = 5          # sample 1 repeats one label
+    inp.labels.copy_(labels)
+    gpu = run_gpu(inp)
+    orc = run_oracle(inp)
+    assert gpu["status"] == (0, 0)
+    assert_parity(gpu, orc, inp)

@@ -8,6 +8,8 @@
 //   EPI_LSE    scores -> online log-sum-exp over V, blank/label log-probs
 //              (f^W_1 of Eq. 7 plus the gather of the two probabilities the
 //              Flash RNN-T kernel emits instead of a softmax)
+//   EPI_LSEK   EPI_LSE that also writes the scores (bf16, TMA stores) for
+//              the untiled mode, which keeps them instead of recomputing
 //   EPI_DH     scores -> dh = dL/dh (Eq. 10), written into the tile buffer
 //              that holds the scores in the untiled mode (Flash RNN-T blog,
 //              "Compute it, use it, make room": gradients replace scores)
@@ -45,7 +47,10 @@ constexpr int EPI_WARP0 = 2;         // first epilogue warp
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s per wait, then give up
 constexpr int SMEM_LIMIT = 232448;   // 227 KiB opt-in maximum per block
 
-enum { EPI_STORE = 0, EPI_ATOMIC = 1, EPI_LSE = 2, EPI_DH = 3, EPI_DA = 4 };
+enum { EPI_STORE = 0, EPI_ATOMIC = 1, EPI_LSE = 2, EPI_DH = 3, EPI_DA = 4, EPI_LSEK = 5 };
+constexpr bool lse_like(int e) { return e == EPI_LSE || e == EPI_LSEK; }
+// epilogues that write 32 x 32 bf16 boxes through a per-warp staging area
+constexpr bool box_store(int e) { return e == EPI_DH || e == EPI_LSEK; }
 enum { TILES_NONE = 0, TILES_ON_M = 1, TILES_ON_K = 2 };
 
 // Per-epilogue-warp shared scratch: either 32 rows x 16 fp32 (+1 pad) for
@@ -83,13 +88,13 @@ struct TcParams {
 };
 
 // Epilogue warps of a kernel, four per TMEM lane quarter for the scores
-// (LSE) epilogue and three for the dh epilogue, whose per-element work would
-// otherwise hold the MMAs back (the dh epilogue needs the 128 registers a
-// thread gets in a 448-thread block; LSE fits the 96 of a 576-thread one);
-// two per quarter for the others.
+// (LSE) epilogue and three for the dh and kept-score epilogues, whose
+// per-element work would otherwise hold the MMAs back (these need the 128
+// registers a thread gets in a 448-thread block; LSE fits the 96 of a
+// 576-thread one); two per quarter for the others.
 template <int EPI>
 constexpr int epi_warps() {
-  return EPI == EPI_LSE ? 16 : (EPI == EPI_DH ? 12 : 8);
+  return EPI == EPI_LSE ? 16 : (box_store(EPI) ? 12 : 8);
 }
 
 template <int BN, int EPI>
@@ -101,11 +106,11 @@ struct Cfg {
   static constexpr int PARTS = EW / 4;                   // warps per TMEM lane quarter
   static constexpr int THREADS = 64 + 32 * EW;
   // per epilogue warp staging area: none for LSE, a 32 x 64 B TMA-store box
-  // for dh, transposes / row staging for the others
-  static constexpr int WSCR = EPI == EPI_LSE ? 0 : (EPI == EPI_DH ? 2048 : WSCR_BYTES);
+  // for dh and kept scores, transposes / row staging for the others
+  static constexpr int WSCR = EPI == EPI_LSE ? 0 : (box_store(EPI) ? 2048 : WSCR_BYTES);
   static constexpr int EPI_SCRATCH = EW * WSCR;
   // LSE: partials of the other parts of each row, double-buffered
-  static constexpr int COMB_BYTES = EPI == EPI_LSE ? 2 * (PARTS - 1) * 128 * 4 * 4 : 0;
+  static constexpr int COMB_BYTES = lse_like(EPI) ? 2 * (PARTS - 1) * 128 * 4 * 4 : 0;
   static constexpr int BAR_BYTES = 256;
   static constexpr int STAGES_RAW =
       (SMEM_LIMIT - 1024 - EPI_SCRATCH - COMB_BYTES - BAR_BYTES) / STAGE;
@@ -290,10 +295,9 @@ __device__ __forceinline__ void lse_init(LseState& st, const TcParams& p, const 
 }
 
 // 32 scores v[] (accumulator values, bias not yet added) of columns col0.. .
-// keep: where to store the scores (untiled mode), or NULL.
+// On return v holds the scores (columns past V: -inf) of a lattice row.
 __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const RowCell& rc,
-                                          float* v, const float* bb, int col0,
-                                          __nv_bfloat16* keep) {
+                                          float* v, const float* bb, int col0) {
   if (!rc.valid) return;
   const int nv = min(32, p.N - col0);
 #pragma unroll
@@ -329,13 +333,6 @@ __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const
   if (jb >= 0 && jb < 32) st.h_blank = pick32(v, jb);
   const int jl = st.lab - col0;
   if (jl >= 0 && jl < 32) st.h_lab = pick32(v, jl);
-  if (keep) {
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      if (j + 1 < nv) *(uint32_t*)(keep + j) = ptx::pack_bf16x2(v[j], v[j + 1]);
-      else if (j < nv) keep[j] = __float2bfloat16_rn(v[j]);
-    }
-  }
 }
 
 __device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p,
@@ -369,12 +366,37 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
   return st;
 }
 
+// A warp's 32 x 32 block d (lane = row) as bf16 into rows wrow0 .. +31,
+// columns col0 .. +31 of the map's matrix, by a TMA store from the warp's
+// staging area (32 rows x 64 bytes, 64-byte swizzle: lane r writes its
+// 16-byte piece j at piece j ^ ((r >> 1) & 3), which spreads every 8 lanes
+// over all 32 banks).  The store engine clips rows and columns past the
+// matrix.  All lanes take part; the staging area is reused only after the
+// previous store from it has been read out.
+__device__ __forceinline__ void store_box_bf16(const float (&d)[32], unsigned char* stg,
+                                               const CUtensorMap* tmC, int col0,
+                                               long long wrow0) {
+  const int lane = threadIdx.x & 31;
+  uint4 q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = pack8_bf16(d + 8 * i);
+  if (lane == 0) ptx::bulk_wait_read();
+  __syncwarp();
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * 64 + ((i ^ sw) << 4)) = q[i];
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(tmC, stg, col0, (int)wrow0);
+    ptx::bulk_commit();
+  }
+}
+
 // dh of 32 columns (Eq. 10: softmax times the position's occupancy minus the
 // blank / label posteriors).  The warp's 32 rows are written as bf16 to rows
-// wrow0 .. +31 of the dh buffer by a TMA store from the warp's staging area
-// (32 rows x 64 bytes, 64-byte swizzle: lane r writes its 16-byte piece j at
-// piece j ^ ((r >> 1) & 3), which spreads every 8 lanes over all 32 banks);
-// rows outside the lattice are 0.  When dbO is given, the block's column sums
+// wrow0 .. +31 of the dh buffer (store_box_bf16); rows outside the lattice
+// are 0.  When dbO is given, the block's column sums
 // (of the bf16 values, read back from the staging area: lane k + 16 h sums
 // columns 2k, 2k+1 over rows 16h .. 16h+15, rows of the two halves taken in
 // opposite parity so that the reads hit distinct banks) are added to it.
@@ -428,21 +450,7 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   }
   const int lane = threadIdx.x & 31;
   if (write && col0 < p.N) {  // (no store box starts past the last column)
-    uint4 q[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = pack8_bf16(d + 8 * i);
-    // the previous store from this staging area has been read out
-    if (lane == 0) ptx::bulk_wait_read();
-    __syncwarp();
-    const int sw = (lane >> 1) & 3;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * 64 + ((i ^ sw) << 4)) = q[i];
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      ptx::tma_store_2d(tmC, stg, col0, (int)wrow0);
-      ptx::bulk_commit();
-    }
+    store_box_bf16(d, stg, tmC, col0, wrow0);
     if (p.dbO) {
       // row 16h + 2q + (e ^ h): its 16-byte piece k/4 sits at (k/4 ^ (q & 3))
       const int k = lane & 15, h = lane >> 4;
@@ -703,11 +711,11 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       RowCell rc{};
       LseState ls;
       DhState ds;
-      if (EPI == EPI_LSE || EPI == EPI_DH || EPI == EPI_DA) {
+      if (lse_like(EPI) || EPI == EPI_DH || EPI == EPI_DA) {
         tr = tile_ref(p.ch, w.m);
         rc = row_of(tr, row);
       }
-      if (EPI == EPI_LSE) lse_init(ls, p, rc);
+      if (lse_like(EPI)) lse_init(ls, p, rc);
       if (EPI == EPI_DH) ds = dh_state(post_cur);
       bool ok = true;
       for (int n = w.n0; n < w.n1; ++n) {
@@ -721,7 +729,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         float v[32], vn[DB ? 32 : 1];
         ptx::tmem_ld32(tbase + hf * 32, v);
         // bias values of the current chunk; the next chunk's are loaded early
-        constexpr bool USE_BIAS = (EPI == EPI_STORE || EPI == EPI_LSE || EPI == EPI_DH);
+        constexpr bool USE_BIAS = (EPI == EPI_STORE || lse_like(EPI) || EPI == EPI_DH);
         uint4 bq[4];
         if (USE_BIAS) load_bias_q(p.bias, p.N, n * BN + hf * 32, bq);
         // dz epilogue: z rows of the current chunk, loaded one chunk ahead
@@ -770,9 +778,19 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                   if (col0 + j < p.N) ptx::red_add_f32(dst + j, v[j]);
               }
             }
-          } else if constexpr (EPI == EPI_LSE) {
-            lse_chunk(ls, p, rc, v, bb, col0,
-                      p.Hout ? p.Hout + ((long long)w.m * BM + row) * p.N + col0 : nullptr);
+          } else if constexpr (lse_like(EPI)) {
+            lse_chunk(ls, p, rc, v, bb, col0);
+            if constexpr (EPI == EPI_LSEK) {
+              // the scores as the untiled mode keeps them (rows outside the
+              // lattice: 0)
+              if (!rc.valid) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+              }
+              if (w.m < p.ch.ntiles && col0 < p.N)
+                store_box_bf16(v, (unsigned char*)wscr, &tmC, col0,
+                               (long long)w.m * BM + sub * 32);
+            }
           } else if constexpr (EPI == EPI_DH) {
             dh_chunk(ds, p, rc, v, bq, col0, (long long)w.m * BM + sub * 32,
                      (unsigned char*)wscr, &tmC, w.m < p.ch.ntiles);
@@ -870,7 +888,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         ptx::mbar_arrive(&acc_empty[acc]);
         if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      if (EPI == EPI_LSE && ok) {
+      if (lse_like(EPI) && ok) {
         // combine the column parts of each row: parts 1.. hand their partial
         // (max, sum, blank score, label score) to part 0
         float* cb = comb + ((uidx & 1) * (PARTS - 1)) * 128 * 4;
@@ -907,8 +925,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
       }
     }
-    // the dh stores issued by this warp are complete before the CTA ends
-    if (EPI == EPI_DH && lane == 0) ptx::bulk_wait_all();
+    // the box stores issued by this warp are complete before the CTA ends
+    if (box_store(EPI) && lane == 0) ptx::bulk_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -1007,39 +1025,251 @@ k_posteriors(ChunkArgs c, const float* __restrict__ grad_loss, float4* __restric
   post[(long long)blockIdx.x * TILE + threadIdx.x] = rec;
 }
 
-// dh from kept bf16 scores, in place (untiled mode; no recompute).
+// dh from the kept bf16 scores, in place (untiled mode: no recompute; Flash
+// RNN-T blog, "Compute it, use it, make room"), from the same per-position
+// records as the dh epilogue: dh_v = g (pb + pl) exp(h_v - lnPD)
+// - g pb [v = blank] - g pl [v = label] (Eq. 10), as
+// sign(g) exp2(h_v log2(e) + log2|g (pb + pl)| - lnPD log2(e)).  One block per
+// tile; thread (k, s) owns the 8 consecutive columns of column group k
+// (groups strided by the group width) for the rows s, s + S, s + 2S, ..., so
+// a warp reads and writes 512 contiguous bytes of a row per access.  With
+// dbO (16-byte aligned), each thread's column sums of the bf16 dh over its
+// rows are added to it.
 __global__ void __launch_bounds__(256)
-k_dh_rows_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float* __restrict__ grad_loss) {
-  __shared__ TileRef tr;
-  if (threadIdx.x == 0) tr = tile_ref(c, blockIdx.x);
-  __syncthreads();
-  const int V = c.sh.V, lane = threadIdx.x & 31, U1 = c.sh.U1;
-  for (int i = threadIdx.x >> 5; i < TILE; i += blockDim.x >> 5) {
-    __nv_bfloat16* h = Hs + ((long long)blockIdx.x * TILE + i) * V;
-    const RowCell rc = row_of(tr, i);
-    if (!rc.valid) {
-      for (int v = lane; v < V; v += 32) h[v] = __float2bfloat16_rn(0.f);
-      continue;
+k_dh_kept_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float4* __restrict__ post,
+               float* __restrict__ dbO, int groups) {
+  // only the batch's tiles: the forward kept scores for exactly these
+  if ((long long)blockIdx.x >= (long long)*c.sv.total_tiles - c.first_tile) return;
+  const int V = c.sh.V, V8 = V / 8, blank = c.sh.blank;
+  const int S = blockDim.x / groups, s0 = threadIdx.x / groups;
+  __nv_bfloat16* tile = Hs + (long long)blockIdx.x * TILE * V;
+  const float4* rec = post + (long long)blockIdx.x * TILE;
+  const float2 l2 = make_float2(kLog2e, kLog2e);
+  for (int k8 = threadIdx.x % groups; k8 < V8; k8 += groups) {
+    const int v0 = 8 * k8;
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                     make_float2(0.f, 0.f)};
+#pragma unroll 4
+    for (int r = s0; r < TILE; r += S) {
+      const float4 q = __ldg(rec + r);  // (g pb, g pl, lnPD log2(e), label)
+      uint4* hp = (uint4*)(tile + (long long)r * V + v0);
+      const uint4 x = *hp;
+      const float gg = q.x + q.y;
+      const float lgn = gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY;
+      const float2 g2 = make_float2(lgn, lgn);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      float d[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 y = __ffma2_rn(make_float2(ptx::bf16lo(w[k]), ptx::bf16hi(w[k])), l2, g2);
+        d[2 * k] = ptx::ex2(y.x);
+        d[2 * k + 1] = ptx::ex2(y.y);
+      }
+      if (gg < 0.f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = -d[j];
+      }
+      const int jb = blank - v0, jl = __float_as_int(q.w) - v0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        d[j] = (j == jb) ? d[j] - q.x : d[j];
+        d[j] = (j == jl) ? d[j] - q.y : d[j];
+      }
+      const uint4 o = pack8_bf16(d);
+      *hp = o;
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        acc[k] = __fadd2_rn(acc[k], make_float2(ptx::bf16lo(ow[k]), ptx::bf16hi(ow[k])));
     }
-    const SavedView& sv = c.sv;
-    const size_t cell = ((size_t)rc.b * c.sh.T + rc.t) * U1 + rc.u;
-    const float lnP = sv.lnP[rc.b];
-    const float a = sv.alpha[cell];
-    float bn;
-    if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
-    else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
-    const float pb = __expf(a + sv.lpb[cell] + bn - lnP);
-    const float pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
-    const int y = (rc.u < rc.Ub) ? c.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
-    const float g = grad_loss ? grad_loss[rc.b] : 1.f;
-    const float lnPD = sv.lnPD[cell], gam = pb + pl;
-    for (int v = lane; v < V; v += 32) {
-      float d = gam * __expf(__bfloat162float(h[v]) - lnPD);
-      if (v == c.sh.blank) d -= pb;
-      if (v == y) d -= pl;
-      h[v] = __float2bfloat16_rn(g * d);
+    if (dbO) {
+      ptx::red_add_v4(dbO + v0, acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+      ptx::red_add_v4(dbO + v0 + 4, acc[2].x, acc[2].y, acc[3].x, acc[3].y);
     }
   }
+}
+
+// The same pass streamed through shared memory (V <= 16384): a tile's kept
+// scores are one contiguous range (128 rows x V bf16), which the block moves
+// in chunks of whole rows (R rows, at most 32 KiB) through a ring of
+// DHK_STAGES shared-memory buffers with 1-D bulk copies that one thread
+// issues, so that many bytes are in flight with few registers.  dh is formed
+// in place in shared memory (thread (k, s): column groups k, k + groups, ...
+// of rows s, s + S, ... of the chunk; a warp touches 512 contiguous bytes)
+// and the chunk is written back by a bulk store; a buffer is refilled once
+// the store issued from it one chunk earlier has been read out.  The per-row
+// terms are formed once per block from the posterior records.  Every wait is
+// bounded: on a timeout the block sets RNNT_ERR_TIMEOUT, waits (bounded) for
+// the copies it issued and leaves.
+constexpr int DHK_STAGES = 3;
+constexpr int DHK_CHUNK_MAX = 32768;
+constexpr int DHK_GROUPS_MAX = 8;  // column groups a thread may own (V <= 256 * 8 * 8)
+
+template <int NG>  // column groups a thread owns at most
+__global__ void __launch_bounds__(256)
+k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
+                      const float4* __restrict__ post, float* __restrict__ dbO, int groups,
+                      int R, int stage_bytes) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ uint64_t full[DHK_STAGES];
+  __shared__ float4 rinfo[TILE];  // (g pb, g pl, log2|g (pb+pl)| - lnPD log2(e), label)
+  const long long have = (long long)*c.sv.total_tiles - c.first_tile;
+  if ((long long)blockIdx.x >= have) return;
+  const int V = c.sh.V, V8 = V / 8, blank = c.sh.blank;
+  const int nchunks = TILE / R;
+  const uint32_t cbytes = (uint32_t)R * (uint32_t)V * 2u;
+  unsigned char* gtile = (unsigned char*)(Hs + (long long)blockIdx.x * TILE * V);
+  const bool leader = threadIdx.x == 0;
+  int issued = 0;
+  if (leader) {
+    for (int i = 0; i < DHK_STAGES; ++i) ptx::mbar_init(&full[i], 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (leader) {
+    for (; issued < DHK_STAGES && issued < nchunks; ++issued) {
+      ptx::mbar_arrive_expect_tx(&full[issued], cbytes);
+      ptx::bulk_load(dsm + issued * stage_bytes, gtile + (size_t)issued * cbytes, cbytes,
+                     &full[issued]);
+    }
+  }
+  if (threadIdx.x < TILE) {
+    const float4 q = __ldg(post + (long long)blockIdx.x * TILE + threadIdx.x);
+    const float gg = q.x + q.y;
+    rinfo[threadIdx.x] =
+        make_float4(q.x, q.y, gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY, q.w);
+  }
+  __syncthreads();
+  const int S = blockDim.x / groups, s0 = threadIdx.x / groups, k0 = threadIdx.x % groups;
+  const float2 l2 = make_float2(kLog2e, kLog2e);
+  float2 acc[NG][4];
+#pragma unroll
+  for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[gi][k] = make_float2(0.f, 0.f);
+  bool ok = true;
+  int i = 0;
+  for (; i < nchunks; ++i) {
+    const int st = i % DHK_STAGES;
+    bool got = ptx::mbar_wait(&full[st], (uint32_t)(i / DHK_STAGES) & 1u, WAIT_NS);
+    if (got) {
+      unsigned char* buf = dsm + st * stage_bytes;
+      for (int r = s0; r < R; r += S) {
+        const float4 ri = rinfo[i * R + r];
+        const float2 g2 = make_float2(ri.z, ri.z);
+        const bool neg = ri.x + ri.y < 0.f;
+        const int lab = __float_as_int(ri.w);
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+          const int k8 = k0 + gi * groups;
+          if (k8 < V8) {
+            uint4* pp = (uint4*)(buf + ((size_t)r * V8 + k8) * 16);
+            const uint4 x = *pp;
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            float d[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 y =
+                  __ffma2_rn(make_float2(ptx::bf16lo(w[k]), ptx::bf16hi(w[k])), l2, g2);
+              d[2 * k] = ptx::ex2(y.x);
+              d[2 * k + 1] = ptx::ex2(y.y);
+            }
+            if (neg) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) d[j] = -d[j];
+            }
+            const int jb = blank - 8 * k8, jl = lab - 8 * k8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              d[j] = (j == jb) ? d[j] - ri.x : d[j];
+              d[j] = (j == jl) ? d[j] - ri.y : d[j];
+            }
+            const uint4 o = pack8_bf16(d);
+            *pp = o;
+            const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              acc[gi][k] =
+                  __fadd2_rn(acc[gi][k], make_float2(ptx::bf16lo(ow[k]), ptx::bf16hi(ow[k])));
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();  // the dh writes are visible to the bulk store
+    }
+    if (!__syncthreads_and(got)) {
+      ok = false;
+      break;
+    }
+    if (leader) {
+      ptx::bulk_store(gtile + (size_t)i * cbytes, dsm + st * stage_bytes, cbytes);
+      ptx::bulk_commit();
+      // refill the buffer of the previous chunk once its store has read it
+      if (i >= 1 && issued < nchunks) {
+        ptx::bulk_wait_read_1();
+        const int rs = (i - 1) % DHK_STAGES;
+        ptx::mbar_arrive_expect_tx(&full[rs], cbytes);
+        ptx::bulk_load(dsm + rs * stage_bytes, gtile + (size_t)issued * cbytes, cbytes,
+                       &full[rs]);
+        ++issued;
+      }
+    }
+  }
+  if (leader) {
+    if (!ok) {
+      atomicOr(c.sv.status, status_bit(RNNT_ERR_TIMEOUT));
+      // the loads issued and not consumed land before the block leaves
+      for (int j = i; j < issued; ++j)
+        ptx::mbar_wait(&full[j % DHK_STAGES], (uint32_t)(j / DHK_STAGES) & 1u, WAIT_NS);
+    }
+    ptx::bulk_wait_all();
+  }
+  if (ok && dbO) {
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const int k8 = k0 + gi * groups;
+      if (k8 < V8 && s0 < R) {
+        ptx::red_add_v4(dbO + 8 * k8, acc[gi][0].x, acc[gi][0].y, acc[gi][1].x, acc[gi][1].y);
+        ptx::red_add_v4(dbO + 8 * k8 + 4, acc[gi][2].x, acc[gi][2].y, acc[gi][3].x,
+                        acc[gi][3].y);
+      }
+    }
+  }
+}
+
+cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const float4* post,
+                                float* dbO, cudaStream_t s) {
+  // column groups: V/8 rounded up to whole warps, at most 256; row groups
+  // fill the block up to 256 threads
+  const int V = c.sh.V;
+  const int groups = std::min(256, (int)cdiv(V / 8, 32) * 32);
+  const int S = std::max(1, 256 / groups);
+  const long long row_bytes = 2LL * V;
+  const long long ng = cdiv(V / 8, groups);
+  if (row_bytes <= DHK_CHUNK_MAX && ng <= DHK_GROUPS_MAX) {
+    // rows per chunk: the largest power of two whose rows fit 16 KiB (at
+    // least one row, at most the tile)
+    int R = 1;
+    while (R < TILE && 2 * R * row_bytes <= 16384) R *= 2;
+    const int stage_bytes = (int)(((long long)R * row_bytes + 127) / 128 * 128);
+    const int smem = DHK_STAGES * stage_bytes;
+    auto kern = ng <= 1 ? k_dh_kept_stream_bf16<1>
+                        : (ng <= 2 ? k_dh_kept_stream_bf16<2>
+                                   : k_dh_kept_stream_bf16<DHK_GROUPS_MAX>);
+    // dynamic plus static shared memory pass the 48 KiB default: opt in once
+    // per instantiation to the largest ring
+    static bool opted[3] = {false, false, false};
+    const int which = ng <= 1 ? 0 : (ng <= 2 ? 1 : 2);
+    if (!opted[which]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DHK_STAGES * DHK_CHUNK_MAX) != cudaSuccess)
+        return cudaErrorInvalidValue;
+      opted[which] = true;
+    }
+    kern<<<(unsigned)c.ntiles, groups * S, smem, s>>>(c, Hs, post, dbO, groups, R, stage_bytes);
+    return cudaGetLastError();
+  }
+  k_dh_kept_bf16<<<(unsigned)c.ntiles, groups * S, 0, s>>>(c, Hs, post, dbO, groups);
+  return cudaGetLastError();
 }
 
 int g_num_sms = 0;
@@ -1238,10 +1468,10 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   const bool ok_b =
       BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN / CL);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
-  // dh epilogue: the store map of the dh buffer [M][N]; the other epilogues
-  // never read the third map
+  // dh / kept-score epilogues: the store map of the [M][N] tile buffer; the
+  // other epilogues never read the third map
   CUtensorMap tc = ta;
-  if (EPI == EPI_DH && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
+  if (box_store(EPI) && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
   static int max_clusters = -1;  // per instantiation
   if (max_clusters < 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1309,8 +1539,14 @@ cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, int cl, cu
   // Only the operand layouts / cluster sizes each epilogue is used with are
   // instantiated: the lattice epilogues take K-major scores/z (and an
   // MN-major W^O for dz); the store and atomic epilogues take every layout.
-  if (g.M <= BM) cl = 1;
-  if constexpr (EPI == EPI_LSE || EPI == EPI_DH) {
+  if constexpr (EPI != EPI_LSEK) {
+    if (g.M <= BM) cl = 1;
+  }
+  if constexpr (EPI == EPI_LSEK) {  // (untiled mode: single CTAs only)
+    if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
+    if (bn == 256) return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
+    return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
+  } else if constexpr (EPI == EPI_LSE || EPI == EPI_DH) {
     if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
     if (bn == 256) {
       if (cl >= 4) return launch_gemm_t<256, 0, 0, EPI, 4>(g, p, 0, s);
@@ -1470,7 +1706,9 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     tp.Hout = (__nv_bfloat16*)Hkeep;
     tp.status = sv.status;
     tp.tiles_on = TILES_ON_M;
-    if (launch_gemm<EPI_LSE>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    const cudaError_t e = Hkeep ? launch_gemm<EPI_LSEK>(g, tp, 256, 1, s)
+                                : launch_gemm<EPI_LSE>(g, tp, 256, kClusterLattice, s);
+    if (e != cudaSuccess) return RNNT_ERR_CUDA;
   }
   return RNNT_OK;
 }
@@ -1535,11 +1773,18 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.tiles_on = TILES_ON_M;
       if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
+      {
+        ProfScope ps("tc_posteriors", s);
+        k_posteriors<<<(unsigned)c.ntiles, TILE, 0, s>>>(c, grad_loss, post);
+        if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      }
+      // dh over the kept scores, db^O in the same pass (16-byte aligned db^O)
       ProfScope ps("tc_dh_kept", s);
-      k_dh_rows_bf16<<<(unsigned)c.ntiles, 256, 0, s>>>(c, Hs, grad_loss);
-      if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_dh_kept_bf16(c, Hs, post, dbO && ((uintptr_t)dbO & 15) == 0 ? dbO : nullptr,
+                              s) != cudaSuccess)
+        return RNNT_ERR_CUDA;
     }
-    if (dbO && (untiled || ((uintptr_t)dbO & 15) != 0)) {
+    if (dbO && ((uintptr_t)dbO & 15) != 0) {
       // db^O += sum over the chunk's positions of dh (rows outside are 0)
       ProfScope ps("tc_colsum_dh", s);
       if (launch_colsum_bf16(Hs, rows, p.V, dbO, s, sv.total_tiles, c.first_tile) != cudaSuccess)

@@ -50,18 +50,87 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def _smi_index(cuda_index: int) -> int:
+    """nvidia-smi / NVML index of a CUDA device (CUDA_VISIBLE_DEVICES, when it
+    lists plain indices, renumbers the devices a process sees)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if ids and all(x.isdigit() for x in ids) and cuda_index < len(ids):
+        return int(ids[cuda_index])
+    return cuda_index
+
+
+class _Nvml:
+    """SM clock and clock-event reasons read in-process through the NVIDIA
+    management library (the library nvidia-smi itself reads). Read-only."""
+
+    CLOCK_SM = 1
+    IDLE = 0x1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.dev)) != 0:
+            lib.nvmlShutdown()
+            raise OSError("no NVML device %d" % index)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.dev, self.CLOCK_SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def read(self):
+        """(sm MHz, reason bits) or None."""
+        ct = self.ct
+        mhz, bits = ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, self.CLOCK_SM, ct.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn is not None:
+            self.reasons_fn(self.dev, ct.byref(bits))
+        return float(mhz.value), int(bits.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """SM clocks and throttle reasons during a timed region: an in-process
+    NVML poll every 2 ms on a background thread (so that even a region of a
+    few milliseconds is covered; `sample_now()` adds one from the caller
+    while its queued work runs), plus nvidia-smi every 200 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu_index: int, poll_s: float = 0.002):
+        self.gpu = _smi_index(gpu_index)
+        self.poll_s = poll_s
         self.proc = None
+        self.nvml = None
+        self.nvml_samples = []
+        self.lines = []
+
+    def sample_now(self):
+        if self.nvml is not None:
+            r = self.nvml.read()
+            if r is not None:
+                self.nvml_samples.append(r)
+
+    def _poll(self):
+        while not self._stop.is_set():
+            self.sample_now()
+            self._stop.wait(self.poll_s)
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -69,10 +138,23 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+        try:
+            self.nvml = _Nvml(self.gpu)
+        except Exception:
+            self.nvml = None
+        self._stop = threading.Event()
+        self._thread = None
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self.nvml is not None:
+            self.nvml.close()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -83,9 +165,13 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
+        """Median SM clock over the samples taken under load (NVML samples
+        flagged GPU-idle are left out when others exist), the maximum clock
+        and every throttle reason seen active."""
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for l in getattr(self, "lines", []):
+        n_smi = 0
+        for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -94,13 +180,29 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            n_smi += 1
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        busy = [s for s in self.nvml_samples if not s[1] & _Nvml.IDLE] or self.nvml_samples
+        for mhz, bits in busy:
+            sm.append(mhz)
+            for bit, n in _Nvml.REASONS.items():
+                if bits & bit:
+                    reasons.add(n)
+        if busy and self.nvml is not None:
+            mx.append(self.nvml.max_mhz)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "sources": {"nvml_2ms": len(busy), "nvidia_smi_200ms": n_smi}}
+
+
+# Algorithmic DRAM bytes per valid lattice position of the memory-bound
+# kernels that can dominate a step: the untiled dh pass reads the kept bf16
+# scores and the 16-byte posterior record and writes dh over the scores.
+KERNEL_BYTES_PER_CELL = {"tc_dh_kept": lambda V: 4 * V + 16}
 
 
 # Algorithmic tensor work of each tensor-core kernel, per valid lattice
@@ -183,7 +285,7 @@ def run_gpu_bench(args):
     inp = synthetic.make(wl, seed=wl.seed + 1000 * rank)
     valid = inp.valid_cells()
     nominal = wl.nominal_cells
-    r = rn.Rnnt.for_inputs(inp, tile_cells=args.tile_cells, device=dev)
+    r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=args.tile_cells, device=dev)
     d = {k: getattr(inp, k).to(dev) for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO", "labels",
                                                "T_len", "U_len")}
     params = rn.make_params(d["WA"], d["WL"], d["bZ"], d["WO"], d["bO"])
@@ -241,6 +343,7 @@ def run_gpu_bench(args):
                 starts[i].record(stream)
                 fn()
                 ends[i].record(stream)
+            clk.sample_now()
             torch.cuda.synchronize()
             wall = time.perf_counter() - t0
         prof = rn.rnnt_profile_stop() if profile else None
@@ -314,6 +417,15 @@ def run_gpu_bench(args):
                 "peak_source": f"{peak_src} bf16 {peak_kind}",
                 "flops_per_launch": flops_per_launch, "launches": top_n,
                 "avg_launch_ms": top_ms / top_n}
+    elif top_name in KERNEL_BYTES_PER_CELL:
+        bytes_per_launch = KERNEL_BYTES_PER_CELL[top_name](V) * valid / max(1, top_n // args.steps)
+        ach = bytes_per_launch / (top_ms / top_n / 1e3) / 1e9
+        roof = {"kernel": top_name, "bound": "hbm", "achieved": round(ach, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                "traffic": recorded_traffic(top_name, wl.name),
+                "peak_source": f"{peak_src} copy bandwidth",
+                "bytes_per_launch": bytes_per_launch, "launches": top_n,
+                "avg_launch_ms": top_ms / top_n}
     else:
         roof = {"kernel": top_name, "bound": "alu", "achieved": None, "peak": None,
                 "unit": "TFLOP/s", "frac": None, "traffic": None,
@@ -332,7 +444,7 @@ def run_gpu_bench(args):
                    "nominal_cells": nominal, "valid_cells": valid,
                    "l2": "flushed (256 MiB write) before each timed step",
                    "execution": "CUDA graph of the step" if graph is not None else "eager",
-                   "parallelism": f"replicas x{world}"},
+                   "mode": args.mode, "parallelism": f"replicas x{world}"},
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / peak_tf, 4),
@@ -343,6 +455,8 @@ def run_gpu_bench(args):
         "gpu_launches": int(launches),
         "roofline": roof,
         "kernel_shares": shares,
+        "kernel_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in
+                               sorted(prof.items(), key=lambda kv: -kv[1][0])},
         "profiled_ms_per_step": round(prof_ms, 4),
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
@@ -435,6 +549,8 @@ def main():
                          "smaller cases of a workload's shapes")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--mode", default="tiled", choices=["tiled", "untiled"],
+                    help="untiled keeps z and the scores from the forward (no recompute)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3

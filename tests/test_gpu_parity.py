@@ -87,13 +87,15 @@ def test_bf16_ragged_shapes_with_biases():
     assert_parity(gpu, orc, inp)
 
 
-def test_unaligned_output_bias_gradient():
+@pytest.mark.parametrize("mode", ["tiled", "untiled"])
+def test_unaligned_output_bias_gradient(mode):
     # db^O at an address that is not 16-byte aligned: the column sums of dh
-    # then take the separate pass instead of the dh epilogue's vector adds
+    # then take the separate pass instead of the vector adds of the pass that
+    # forms dh (the dh epilogue, or the untiled dh pass over the kept scores)
     inp = synthetic.custom(B=6, T=45, U=13, HA=64, HL=192, H=128, V=320, dtype="bf16", seed=7,
                            t_frac=0.1, u_frac=0.0, bias_std=0.3)
     dev = to_device(inp)
-    r = rn.Rnnt.for_inputs(inp)
+    r = rn.Rnnt.for_inputs(inp, mode=mode)
     params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
     r.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
     g = r.alloc_grads()
@@ -104,19 +106,20 @@ def test_unaligned_output_bias_gradient():
     torch.cuda.synchronize()
     orc = run_oracle(inp)
     assert rel_l2(g["dbO"].cpu().numpy(), orc.grads["dbO"]) < 1e-2
-    aligned = run_gpu(inp, keep_saved=False)
+    aligned = run_gpu(inp, mode=mode, keep_saved=False)
     assert rel_l2(aligned["dbO"], orc.grads["dbO"]) < 1e-2
     assert rel_l2(g["dbO"].cpu().numpy(), aligned["dbO"]) < 1e-2
 
 
+@pytest.mark.parametrize("mode", ["tiled", "untiled"])
 @pytest.mark.parametrize("offset", [0, 1])
-def test_output_bias_gradient_without_weight_gradient(offset):
-    # dW^O not requested (NULL): db^O from the dh epilogue (aligned) or the
-    # separate column-sum pass (unaligned), the other gradients as usual
+def test_output_bias_gradient_without_weight_gradient(offset, mode):
+    # dW^O not requested (NULL): db^O from the pass that forms dh (aligned) or
+    # the separate column-sum pass (unaligned), the other gradients as usual
     inp = synthetic.custom(B=5, T=40, U=11, HA=64, HL=64, H=128, V=264, dtype="bf16", seed=13,
                            t_frac=0.2, u_frac=0.0, bias_std=0.2)
     dev = to_device(inp)
-    r = rn.Rnnt.for_inputs(inp)
+    r = rn.Rnnt.for_inputs(inp, mode=mode)
     params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
     args = (dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
     r.fwd(*args)
@@ -156,6 +159,24 @@ def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
         assert rel_l2(untiled[k], runs[0][k]) < tol_untiled, k
     for r in runs + [untiled]:
         assert_parity(r, orc, inp)
+
+
+@pytest.mark.parametrize("V", [4096, 16384, 20480])
+def test_untiled_large_vocabularies(V):
+    # untiled dh over the kept scores at vocabulary sizes where a thread owns
+    # two or eight column groups (4096, 16384: one 32 KiB row per streamed
+    # chunk) and past the streamed form (20480: the register form); db^O is
+    # summed in the same pass
+    inp = synthetic.custom(B=3, T=9, U=4, HA=64, HL=64, H=64, V=V, dtype="bf16", seed=31,
+                           bias_std=0.2)
+    orc = run_oracle(inp)
+    untiled = run_gpu(inp, mode="untiled")
+    tiled = run_gpu(inp)
+    assert untiled["status"] == (0, 0)
+    np.testing.assert_array_equal(untiled["loss"], tiled["loss"])
+    assert_parity(untiled, orc, inp)
+    for k in GRAD_KEYS:
+        assert rel_l2(untiled[k], tiled[k]) < 1e-2, k
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -1069,11 +1069,15 @@ k_dh_kept_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float4* __rest
 #pragma unroll
         for (int j = 0; j < 8; ++j) d[j] = -d[j];
       }
+      // the blank and label terms touch at most two pieces of a row
       const int jb = blank - v0, jl = __float_as_int(q.w) - v0;
+      if ((unsigned)jb < 8u) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        d[j] = (j == jb) ? d[j] - q.x : d[j];
-        d[j] = (j == jl) ? d[j] - q.y : d[j];
+        for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? d[j] - q.x : d[j];
+      }
+      if ((unsigned)jl < 8u) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? d[j] - q.y : d[j];
       }
       const uint4 o = pack8_bf16(d);
       *hp = o;
@@ -1178,11 +1182,15 @@ k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
 #pragma unroll
               for (int j = 0; j < 8; ++j) d[j] = -d[j];
             }
+            // the blank and label terms touch at most two pieces of a row
             const int jb = blank - 8 * k8, jl = lab - 8 * k8;
+            if ((unsigned)jb < 8u) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              d[j] = (j == jb) ? d[j] - ri.x : d[j];
-              d[j] = (j == jl) ? d[j] - ri.y : d[j];
+              for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? d[j] - ri.x : d[j];
+            }
+            if ((unsigned)jl < 8u) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? d[j] - ri.y : d[j];
             }
             const uint4 o = pack8_bf16(d);
             *pp = o;

@@ -66,6 +66,8 @@ struct TcParams {
   int m_groups;          // M tiles in groups of the cluster size
   int row_complete;      // a unit is one M tile with all of its N tiles, in order
   int n_split;           // row-complete units: N tiles split into this many units (1 for LSE)
+  int n_split_auto;      // n_split is a maximum: the kernel picks the split from the
+                         // batch's tile count (whole waves of row units)
   float* C;              // STORE / ATOMIC output, row-major with ldc
   long long ldc;
   const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
@@ -128,12 +130,11 @@ struct Unit {
 // B tiles at the same time.  M tiles past the matrix are padding: their A
 // loads are zero-filled and their epilogues write nothing.
 template <int CL>
-__device__ __forceinline__ Unit unit_of(const TcParams& p, int u, int kb_lim) {
+__device__ __forceinline__ Unit unit_of(const TcParams& p, int u, int kb_lim, int kbps, int ns) {
   Unit w;
   const int r = u % CL;
   int rest = u / CL;
   if (p.row_complete) {
-    const int ns = p.n_split > 1 ? p.n_split : 1;
     const int per = (p.n_tiles + ns - 1) / ns;
     const int sp = rest % ns;
     w.m = (rest / ns) * CL + r;
@@ -149,8 +150,8 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u, int kb_lim) {
     const int ks = rest / p.m_groups;
     w.m = mg * CL + r;
     w.n0 = n; w.n1 = n + 1;
-    w.kb0 = ks * p.kb_per_split;
-    w.kb1 = min(kb_lim, w.kb0 + p.kb_per_split);
+    w.kb0 = ks * kbps;
+    w.kb1 = min(kb_lim, w.kb0 + kbps);
   }
   return w;
 }
@@ -544,17 +545,25 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   ptx::griddep_launch();
   // units that hold actual lattice tiles: a prefix of the unit order (M
   // groups, resp. K splits, are the slow index), read from the tile count
-  int units = p.units, kb_lim = p.kb_total;
+  int units = p.units, kb_lim = p.kb_total, kbps = p.kb_per_split;
+  int ns = max(1, p.n_split);  // row-complete units: V split of a tile
   if (p.tiles_on != TILES_NONE) {
     const long long have = max(0LL, min(p.ch.ntiles, (long long)*p.ch.sv.total_tiles -
                                                          p.ch.first_tile));
     if (p.tiles_on == TILES_ON_M) {
       const int groups = (int)((have + CL - 1) / CL);
+      // fewer than ~4 waves of tiles: each tile's V range is split over
+      // several units so that the last wave is not mostly idle
+      if (p.n_split_auto && groups > 0)
+        ns = max(1, min(ns, (int)((4LL * (gridDim.x / CL) + groups - 1) / groups)));
       // (row-complete: the V split is the fast index; otherwise N, with no K split)
-      units = min(units, groups * (p.row_complete ? max(1, p.n_split) : p.n_tiles) * CL);
+      units = min(units, groups * (p.row_complete ? ns : p.n_tiles) * CL);
     } else {
       kb_lim = (int)min((long long)p.kb_total, have * (BM / BK));
-      const int splits = (kb_lim + p.kb_per_split - 1) / p.kb_per_split;
+      // the host's split count (chosen for whole waves) over the K blocks
+      // that exist: equal splits instead of fewer, full-length ones
+      kbps = max(1, (kb_lim + p.k_splits - 1) / p.k_splits);
+      const int splits = (kb_lim + kbps - 1) / kbps;
       units = min(units, splits * p.m_groups * p.n_tiles * CL);
     }
   }
@@ -567,7 +576,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
       bool first_fill = true;
       for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -633,7 +642,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
+        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, wait_ns)) {
@@ -693,14 +702,14 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     // dh epilogue: the row's record of the next unit is loaded one unit ahead
     float4 post_next = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
     if (EPI == EPI_DH && cluster_id * CL < units) {
-      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank, kb_lim);
+      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank, kb_lim, kbps, ns);
       if (w0.m < p.ch.ntiles) post_next = __ldg(p.post + (long long)w0.m * BM + row);
     }
     for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-      const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim);
+      const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
       const float4 post_cur = post_next;
       if (EPI == EPI_DH && (gi + n_clusters) * CL < units) {
-        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank, kb_lim);
+        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank, kb_lim, kbps, ns);
         post_next = (wn.m < p.ch.ntiles) ? __ldg(p.post + (long long)wn.m * BM + row)
                                          : make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
       }
@@ -1770,10 +1779,10 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.grad_loss = grad_loss;
       tp.Hout = Hs;
       tp.post = post;
-      // fewer than ~4 waves of tiles: split each tile's V range over several
-      // units so that the last wave is not mostly idle
-      tp.n_split = (int)std::max<long long>(1, std::min<long long>(
-                       4, cdiv(4LL * num_sms(), std::max<long long>(1, p.chunk_tiles))));
+      // each tile's V range split over up to 4 units, the kernel choosing
+      // from the batch's tile count
+      tp.n_split = 4;
+      tp.n_split_auto = 1;
       tp.status = sv.status;
       // db^O: column sums of dh formed in the same epilogue (vector
       // reductions need a 16-byte aligned db^O)

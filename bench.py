@@ -402,6 +402,8 @@ def run_gpu_bench(args):
     peak_kind = "sustained" if ms_max * args.steps >= 1000.0 else "burst"
     peak_tf = tf_sust if peak_kind == "sustained" else tf_burst
     launches = sum(c for _, c in prof.values())
+    # the ncu summaries key their traffic figures by workload (and mode)
+    traffic_key = wl.name if args.mode == "tiled" else f"{wl.name}-untiled"
     top = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("none", (0.0, 1))
     top_name, (top_ms, top_n) = top
     H, V = wl.H, wl.V
@@ -413,7 +415,7 @@ def run_gpu_bench(args):
         peak = peak_tf
         roof = {"kernel": top_name, "bound": "tensor", "achieved": round(ach, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                "traffic": recorded_traffic(top_name, wl.name),
+                "traffic": recorded_traffic(top_name, traffic_key),
                 "peak_source": f"{peak_src} bf16 {peak_kind}",
                 "flops_per_launch": flops_per_launch, "launches": top_n,
                 "avg_launch_ms": top_ms / top_n}
@@ -422,7 +424,7 @@ def run_gpu_bench(args):
         ach = bytes_per_launch / (top_ms / top_n / 1e3) / 1e9
         roof = {"kernel": top_name, "bound": "hbm", "achieved": round(ach, 1),
                 "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
-                "traffic": recorded_traffic(top_name, wl.name),
+                "traffic": recorded_traffic(top_name, traffic_key),
                 "peak_source": f"{peak_src} copy bandwidth",
                 "bytes_per_launch": bytes_per_launch, "launches": top_n,
                 "avg_launch_ms": top_ms / top_n}

@@ -5,14 +5,15 @@ ABI of ``include/rnnt.h``; this package is its thin Python binding.
 """
 from .binding import (EXPORTS, RNNT_BF16, RNNT_F32, RNNT_TILED, RNNT_UNTILED, Rnnt, RnntDims,
                       RnntError, RnntParams, RnntSavedOffsets, load, make_dims, make_params,
-                      rnnt_bwd, rnnt_device_status, rnnt_fwd, rnnt_graph_capturable,
+                      rnnt_bwd, rnnt_device_status, rnnt_fwd, rnnt_fwd_bwd,
+                      rnnt_graph_capturable,
                       rnnt_saved_bytes, rnnt_saved_layout,
                       rnnt_profile_start, rnnt_profile_stop, rnnt_status_string,
                       rnnt_workspace_bytes)
 
 __all__ = ["EXPORTS", "RNNT_BF16", "RNNT_F32", "RNNT_TILED", "RNNT_UNTILED", "Rnnt", "RnntDims",
            "RnntError", "RnntParams", "RnntSavedOffsets", "load", "make_dims", "make_params",
-           "rnnt_bwd", "rnnt_device_status", "rnnt_fwd", "rnnt_graph_capturable",
+           "rnnt_bwd", "rnnt_device_status", "rnnt_fwd", "rnnt_fwd_bwd", "rnnt_graph_capturable",
            "rnnt_saved_bytes", "rnnt_saved_layout",
            "rnnt_profile_start", "rnnt_profile_stop", "rnnt_status_string",
            "rnnt_workspace_bytes"]

@@ -25,7 +25,7 @@ RNNT_TILED, RNNT_UNTILED = 0, 1
 
 # Every symbol include/rnnt.h declares.
 EXPORTS = ("rnnt_saved_bytes", "rnnt_saved_layout", "rnnt_workspace_bytes",
-           "rnnt_graph_capturable", "rnnt_fwd", "rnnt_bwd", "rnnt_device_status",
+           "rnnt_graph_capturable", "rnnt_fwd", "rnnt_bwd", "rnnt_fwd_bwd", "rnnt_device_status",
            "rnnt_status_string", "rnnt_profile_start", "rnnt_profile_stop", "rnnt_profile_entry")
 
 
@@ -85,6 +85,9 @@ def load(build_if_missing: bool = False):
     lib.rnnt_bwd.restype = ctypes.c_int
     lib.rnnt_bwd.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P,
                              P, P, P, P, P, P, P, P, S, P]
+    lib.rnnt_fwd_bwd.restype = ctypes.c_int
+    lib.rnnt_fwd_bwd.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P, P,
+                                 P, P, P, P, P, P, P, P, S, P]
     lib.rnnt_device_status.restype = ctypes.c_int
     lib.rnnt_device_status.argtypes = [D, P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.rnnt_status_string.restype = ctypes.c_char_p
@@ -187,6 +190,19 @@ def rnnt_bwd(dims, hA, hL, params: RnntParams, labels, T_len, U_len, grad_loss, 
     return code
 
 
+def rnnt_fwd_bwd(dims, hA, hL, params: RnntParams, labels, T_len, U_len, loss, grad_loss, saved,
+                 dhA, dhL, dWA, dWL, dbZ, dWO, dbO, ws, stream=None, check=True) -> int:
+    code = load().rnnt_fwd_bwd(ctypes.byref(dims), _p(hA), _p(hL), ctypes.byref(params),
+                               _p(labels), _p(T_len), _p(U_len), _p(loss), _p(grad_loss),
+                               _p(saved), _p(dhA), _p(dhL), _p(dWA), _p(dWL), _p(dbZ), _p(dWO),
+                               _p(dbO), _p(ws),
+                               ws.numel() * ws.element_size() if ws is not None else 0,
+                               _stream(stream))
+    if check:
+        _check(code, "rnnt_fwd_bwd")
+    return code
+
+
 def rnnt_device_status(dims, saved, stream=None):
     """(status code, raw status word)."""
     w = ctypes.c_int32(0)
@@ -283,6 +299,17 @@ class Rnnt:
                  g["dhA"], g["dhL"], g["dWA"], g["dWL"], g["dbZ"], g["dWO"], g["dbO"], self.ws,
                  stream)
         return g
+
+    def fwd_bwd(self, hA, hL, params, labels, T_len, U_len, loss=None, grad_loss=None,
+                grads=None, stream=None):
+        """One training step (rnnt_fwd_bwd): returns (loss, grads)."""
+        if loss is None:
+            loss = torch.empty(self.dims.B, dtype=torch.float32, device=self.device)
+        g = grads if grads is not None else self.alloc_grads()
+        rnnt_fwd_bwd(self.dims, hA, hL, params, labels, T_len, U_len, loss, grad_loss,
+                     self.saved, g["dhA"], g["dhL"], g["dWA"], g["dWL"], g["dbZ"], g["dWO"],
+                     g["dbO"], self.ws, stream)
+        return loss, g
 
     def saved_arrays(self) -> SavedArrays:
         d, L = self.dims, self.layout

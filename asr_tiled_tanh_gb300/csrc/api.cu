@@ -367,6 +367,33 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
                      float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
                      void* ws, size_t ws_bytes, rnnt_stream stream) {
+  return rnnt::bwd_impl(dims, hA, hL, pr, labels, T_len, U_len, grad_loss, saved, dhA, dhL, dWA,
+                        dWL, dbZ, dWO, dbO, ws, ws_bytes, stream, false);
+}
+
+rnnt_status rnnt_fwd_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                         const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                         const int32_t* U_len, float* loss, const float* grad_loss, void* saved,
+                         float* dhA, float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO,
+                         float* dbO, void* ws, size_t ws_bytes, rnnt_stream stream) {
+  rnnt_status s = rnnt::fwd_impl(dims, hA, hL, pr, labels, T_len, U_len, loss, saved, ws,
+                                 ws_bytes, stream, true);
+  if (s != RNNT_OK) return s;
+  // the forward's z of a single-chunk plan is still in the workspace
+  return rnnt::bwd_impl(dims, hA, hL, pr, labels, T_len, U_len, grad_loss, saved, dhA, dhL, dWA,
+                        dWL, dbZ, dWO, dbO, ws, ws_bytes, stream, true);
+}
+
+}  // extern "C"
+
+// The backward pass.  z_resident: the workspace still holds the z tiles the
+// forward built (rnnt_fwd_bwd), so that a single-chunk plan skips its rebuild.
+rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
+                           const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                           const int32_t* U_len, const float* grad_loss, void* saved,
+                           float* dhA, float* dhL, float* dWA, float* dWL, float* dbZ,
+                           float* dWO, float* dbO, void* ws, size_t ws_bytes,
+                           rnnt_stream stream, bool z_resident) {
   Plan p;
   rnnt_status st0 = check_common(dims, hA, hL, pr, labels, T_len, U_len, saved, ws, ws_bytes, &p);
   if (st0 != RNNT_OK) return st0;
@@ -420,7 +447,8 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                               es);
     };
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, &enc, st);
+                          z_resident, dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, &enc,
+                          st);
     return s;
   }
 
@@ -496,6 +524,8 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
   if (dbZ) LAUNCH("colsum", launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, st));
   return RNNT_OK;
 }
+
+extern "C" {
 
 rnnt_status rnnt_device_status(const rnnt_dims* dims, const void* saved, rnnt_stream stream,
                                int32_t* word) {

@@ -1733,7 +1733,8 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
 rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Zv,
-                              void* Hv, bool untiled, float* dA, float* dLr, float* dWO,
+                              void* Hv, bool untiled, bool z_resident, float* dA, float* dLr,
+                              float* dWO,
                               float* dbO, float4* post, const PreLaunch* pre,
                               const PreLaunch* after, cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
@@ -1763,7 +1764,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
           k_posteriors<<<(unsigned)c.ntiles, TILE, 0, fork.side(0)>>>(c, grad_loss, post);
           if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
         }
-        {
+        if (!(z_resident && nch == 1)) {
           ProfScope ps("tc_build_z", s);
           if (launch_build_z_bf16(c, pA, pL, Z, s) != cudaSuccess) return RNNT_ERR_CUDA;
         }

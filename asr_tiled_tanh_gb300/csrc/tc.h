@@ -24,12 +24,15 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
 // Launches a caller has the backward make: `pre` on a side stream while the
 // first chunk's z is rebuilt (they must be done before the chunk's dh
 // kernel), `after` once the last chunk's dz is done (it may read dA, dLr),
-// beside that chunk's dW^O.
+// beside that chunk's dW^O.  z_resident: Z already holds the z tiles of a
+// single-chunk plan (built by the forward of the same call), which are then
+// not rebuilt.
 using PreLaunch = std::function<rnnt_status(cudaStream_t)>;
 rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                               const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                               const float* grad_loss, const float* pA, const float* pL, void* Z,
-                              void* Hs, bool untiled, float* dA, float* dLr, float* dWO,
+                              void* Hs, bool untiled, bool z_resident, float* dA, float* dLr,
+                              float* dWO,
                               float* dbO, float4* post, const PreLaunch* pre,
                               const PreLaunch* after, cudaStream_t s);
 // dh^A, dW^A, dh^L, dW^L, db^Z from dA and dLr.

@@ -1,8 +1,9 @@
 """Benchmark: RNN-T joint + output layer + transducer loss, forward + backward.
 
-One step = rnnt_fwd + rnnt_bwd over one batch of the synthetic workload (every
+One step = one training step over one batch of the synthetic workload (every
 row of the hot path: validation, projections, the tiled joint/output/LSE
-forward, alpha/beta, the tiled recompute backward, the encoder gradients).
+forward, alpha/beta, the tiled recompute backward, the encoder gradients),
+through rnnt_fwd_bwd (`--api separate`: rnnt_fwd then rnnt_bwd).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small] [--impl reference]
 
@@ -295,6 +296,10 @@ def run_gpu_bench(args):
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
 
     def step(s=stream):
+        if args.api == "step":  # rnnt_fwd_bwd: one call for the training step
+            r.fwd_bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
+                      grads=grads, stream=s)
+            return
         r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss, stream=s)
         r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads,
               stream=s)
@@ -446,7 +451,9 @@ def run_gpu_bench(args):
                    "nominal_cells": nominal, "valid_cells": valid,
                    "l2": "flushed (256 MiB write) before each timed step",
                    "execution": "CUDA graph of the step" if graph is not None else "eager",
-                   "mode": args.mode, "parallelism": f"replicas x{world}"},
+                   "mode": args.mode,
+                   "api": "rnnt_fwd_bwd" if args.api == "step" else "rnnt_fwd + rnnt_bwd",
+                   "parallelism": f"replicas x{world}"},
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / peak_tf, 4),
@@ -551,6 +558,8 @@ def main():
                          "smaller cases of a workload's shapes")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--api", default="step", choices=["step", "separate"],
+                    help="step: one rnnt_fwd_bwd call per step; separate: rnnt_fwd + rnnt_bwd")
     ap.add_argument("--mode", default="tiled", choices=["tiled", "untiled"],
                     help="untiled keeps z and the scores from the forward (no recompute)")
     args = ap.parse_args()

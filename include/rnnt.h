@@ -166,6 +166,22 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
                      void* ws, size_t ws_bytes, rnnt_stream stream);
 
+/* One training step: rnnt_fwd followed by rnnt_bwd on the same buffers, with
+ * the arguments of both (loss is written as by rnnt_fwd; grad_loss and the
+ * gradient outputs are as for rnnt_bwd) and the same results.  Because the
+ * workspace is not handed back to the caller between the two passes, a plan
+ * whose lattice fits one chunk (rnnt_graph_capturable) reuses the z tiles
+ * that the forward built instead of rebuilding them in the backward; the
+ * scores are still recomputed per tile (Flash RNN-T blog, "Compute it, use
+ * it, make room").  Errors: those of rnnt_fwd, then those of rnnt_bwd; the
+ * backward does not run when the forward returns an error. */
+rnnt_status rnnt_fwd_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
+                         const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
+                         const int32_t* U_len, float* loss, const float* grad_loss,
+                         void* saved, float* dhA, float* dhL, float* dWA, float* dWL,
+                         float* dbZ, float* dWO, float* dbO, void* ws, size_t ws_bytes,
+                         rnnt_stream stream);
+
 /* Size of the fixed device scratch array used by rnnt_fwd_noalloc. */
 #define RNNT_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -179,6 +179,35 @@ def test_untiled_large_vocabularies(V):
         assert rel_l2(untiled[k], tiled[k]) < 1e-2, k
 
 
+@pytest.mark.parametrize("dtype,mode,tile_cells", [("bf16", "tiled", 0), ("bf16", "tiled", 640),
+                                                   ("bf16", "untiled", 0), ("f32", "tiled", 0)])
+def test_training_step_call_matches_separate_calls(dtype, mode, tile_cells):
+    # rnnt_fwd_bwd is rnnt_fwd then rnnt_bwd; a single-chunk tiled plan reuses
+    # the forward's z tiles (tile_cells 0), a multi-chunk one rebuilds them (640)
+    H, V = (64, 96) if dtype == "f32" else (128, 192)
+    inp = synthetic.custom(B=4, T=40, U=12, HA=64, HL=96, H=H, V=V, dtype=dtype, seed=37,
+                           bias_std=0.2)
+    g = np.array([1.0, -0.5, 2.0, 0.3])
+    sep = run_gpu(inp, mode=mode, tile_cells=tile_cells, grad_loss=g, keep_saved=False)
+    dev = to_device(inp)
+    r = rn.Rnnt.for_inputs(inp, mode=mode, tile_cells=tile_cells)
+    assert rn.rnnt_graph_capturable(r.dims) == (1 if tile_cells == 0 else 0)
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    loss, grads = r.fwd_bwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"],
+                            dev["U_len"], grad_loss=torch.as_tensor(g, dtype=torch.float32,
+                                                                    device="cuda"))
+    torch.cuda.synchronize()
+    assert r.status() == (0, 0)
+    fused = dict(loss=loss.double().cpu().numpy(), **{k: v.cpu().numpy() for k, v in grads.items()})
+    np.testing.assert_array_equal(fused["loss"], sep["loss"])
+    # the same kernels on the same data; only the order of fp32 atomics differs
+    # (bf16: which can flip a rounding of dA to bf16 before the encoder GEMMs)
+    tol = 1e-5 if dtype == "f32" else 1e-3
+    for k in GRAD_KEYS:
+        assert rel_l2(fused[k], sep[k]) < tol, k
+    assert_parity(fused, run_oracle(inp, grad_loss=g), inp, check_saved=False)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_padding_is_never_read(dtype):
     H, V = (32, 48) if dtype == "f32" else (128, 128)

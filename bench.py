@@ -525,7 +525,8 @@ def run_reference(args):
     cells = wl.T * wl.U1
     value = cells / (ms / 1e3)
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
-           "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+           "n_gpus": args.gpus, "device": "host cores (the oracle runs on no GPU)",
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
            "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "

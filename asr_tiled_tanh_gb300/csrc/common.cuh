@@ -28,6 +28,16 @@ constexpr size_t ALIGN = 256;
 __host__ __device__ inline size_t align_up(size_t x, size_t a = ALIGN) {
   return (x + a - 1) / a * a;
 }
+
+// Host state that a launcher sets up once per device (function attributes,
+// occupancy figures, SM counts) is kept in per-device slots, so that a process
+// may drive several GPUs.
+constexpr int kDeviceSlots = 64;
+inline int device_slot() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0) d = 0;
+  return d % kDeviceSlots;
+}
 __host__ __device__ inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 // Status word bits: bit k <=> rnnt_status k.

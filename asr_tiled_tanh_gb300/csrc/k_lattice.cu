@@ -579,12 +579,13 @@ template <int NJ, bool FAST, int W>
 static cudaError_t launch_ab_smem(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
                                   SavedView sv, float* loss, int R, size_t smem,
                                   cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kDeviceSlots] = {};  // per instantiation and device
+  bool& done = attr[device_slot()];
+  if (!done) {
     cudaError_t e = cudaFuncSetAttribute(k_alpha_beta_smem<NJ, FAST, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
+    done = true;
   }
   k_alpha_beta_smem<NJ, FAST, W><<<dim3(sh.B, 2), 32 * W, smem, s>>>(sh, T_len, U_len, sv, loss,
                                                                        R);
@@ -592,7 +593,8 @@ static cudaError_t launch_ab_smem(const Shape& sh, const int32_t* T_len, const i
 }
 
 static int sm_count() {
-  static int n = 0;
+  static int count[kDeviceSlots] = {};
+  int& n = count[device_slot()];
   if (n == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

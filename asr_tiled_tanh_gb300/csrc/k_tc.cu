@@ -1274,13 +1274,13 @@ cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const flo
                                    : k_dh_kept_stream_bf16<DHK_GROUPS_MAX>);
     // dynamic plus static shared memory pass the 48 KiB default: opt in once
     // per instantiation to the largest ring
-    static bool opted[3] = {false, false, false};
-    const int which = ng <= 1 ? 0 : (ng <= 2 ? 1 : 2);
-    if (!opted[which]) {
+    static bool opted[3][kDeviceSlots] = {};
+    bool& done = opted[ng <= 1 ? 0 : (ng <= 2 ? 1 : 2)][device_slot()];
+    if (!done) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                DHK_STAGES * DHK_CHUNK_MAX) != cudaSuccess)
         return cudaErrorInvalidValue;
-      opted[which] = true;
+      done = true;
     }
     kern<<<(unsigned)c.ntiles, groups * S, smem, s>>>(c, Hs, post, dbO, groups, R, stage_bytes);
     return cudaGetLastError();
@@ -1289,16 +1289,16 @@ cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const flo
   return cudaGetLastError();
 }
 
-int g_num_sms = 0;
-
 int num_sms() {
-  if (g_num_sms == 0) {
+  static int count[kDeviceSlots] = {};
+  int& n = count[device_slot()];
+  if (n == 0) {
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
   }
-  return g_num_sms;
+  return n;
 }
 
 // out[n] += sum over rows of a bf16 [R][N] matrix (N % 8 == 0).  A block is
@@ -1489,8 +1489,9 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   // other epilogues never read the third map
   CUtensorMap tc = ta;
   if (box_store(EPI) && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
-  static int max_clusters = -1;  // per instantiation
-  if (max_clusters < 0) {
+  static int clusters_of[kDeviceSlots] = {};  // per instantiation and device (0: not set up)
+  int& max_clusters = clusters_of[device_slot()];
+  if (max_clusters <= 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;

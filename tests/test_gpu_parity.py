@@ -308,11 +308,27 @@ def test_host_checked_errors():
     code = rn.rnnt_fwd(r.dims, dev["hA"], dev["hL"], bad_params, dev["labels"], dev["T_len"],
                        dev["U_len"], loss, r.saved, r.ws, check=False)
     assert code == 1
+    # the training-step call returns the forward's error and then runs no backward
+    # (which would overwrite dW^O)
+    g = r.alloc_grads()
+    g["dWO"].fill_(7.0)
+    code = rn.rnnt_fwd_bwd(r.dims, dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"],
+                           dev["U_len"], loss, None, r.saved, g["dhA"], g["dhL"], g["dWA"],
+                           g["dWL"], g["dbZ"], g["dWO"], g["dbO"], small_ws, check=False)
+    assert code == 3
+    code = rn.rnnt_fwd_bwd(r.dims, dev["hA"], dev["hL"], params, None, dev["T_len"],
+                           dev["U_len"], loss, None, r.saved, g["dhA"], g["dhL"], g["dWA"],
+                           g["dWL"], g["dbZ"], g["dWO"], g["dbO"], r.ws, check=False)
+    assert code == 1
+    torch.cuda.synchronize()
+    assert bool((g["dWO"] == 7.0).all())
 
 
-def test_cuda_graph_capture_matches_eager():
-    # a single-chunk plan runs as stream work only: fwd + bwd captured into a
-    # CUDA graph (side streams and all) and replayed give the eager results
+@pytest.mark.parametrize("api", ["separate", "step"])
+def test_cuda_graph_capture_matches_eager(api):
+    # a single-chunk plan runs as stream work only: fwd + bwd (or the
+    # training-step call) captured into a CUDA graph (side streams and all)
+    # and replayed give the eager results
     inp = synthetic.custom(B=4, T=48, U=12, HA=64, HL=96, H=128, V=256, dtype="bf16", seed=11,
                            bias_std=0.2)
     dev = to_device(inp)
@@ -325,17 +341,23 @@ def test_cuda_graph_capture_matches_eager():
     torch.cuda.synchronize()
     loss = torch.empty_like(loss_e)
     grads = r.alloc_grads()
+
+    def step(st):
+        if api == "step":
+            r.fwd_bwd(*args, loss=loss, grads=grads, stream=st)
+        else:
+            r.fwd(*args, loss=loss, stream=st)
+            r.bwd(*args, grads=grads, stream=st)
+
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):  # warm-up on the capture stream
-        r.fwd(*args, loss=loss, stream=s)
-        r.bwd(*args, grads=grads, stream=s)
+        step(s)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        r.fwd(*args, loss=loss, stream=s)
-        r.bwd(*args, grads=grads, stream=s)
+        step(s)
     for v in grads.values():
         v.fill_(float("nan"))
     loss.fill_(float("nan"))

@@ -691,7 +691,9 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     // two parts the next chunk's tcgen05.ld is in flight while the current one
     // is processed; with more, the other warps of the quarter cover it.
     constexpr int PARTS = C::PARTS;
-    constexpr bool DB = PARTS == 2;              // double-buffered TMEM loads
+    // double-buffered TMEM loads (not for dz: its epilogue is at the register
+    // limit of a 320-thread block, and the extra 32 values spill)
+    constexpr bool DB = PARTS == 2 && EPI != EPI_DA;
     const int sub = warp & 3;                    // TMEM lane quarter of this warp
     const int hf = (warp - EPI_WARP0) >> 2;      // part: chunks c % PARTS == hf
     const int row = sub * 32 + lane;             // accumulator row owned by this thread

@@ -1,0 +1,48 @@
+"""bench.py's DRAM-traffic bookkeeping on the host: a traffic line from an ncu
+summary is reported only for its kernel and workload key and only while the
+kernel sources still hash to the value it was captured from."""
+import os
+
+import bench
+
+
+def _profiles(tmp_path, lines):
+    d = tmp_path / "profiles"
+    d.mkdir()
+    (d / "k.md").write_text("summary text\n\n" + "\n".join(lines) + "\n")
+    return str(tmp_path)
+
+
+def test_traffic_line_matches_kernel_workload_and_source(tmp_path, monkeypatch):
+    h = "0123456789ab"
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    root = _profiles(tmp_path, [f"traffic tc_bwd_dz small 210150912 src={h}",
+                                f"traffic tc_dh_kept small-untiled 209008128 src={h}",
+                                "traffic tc_bwd_dh audio40 1870576181 src=000000000000"])
+    monkeypatch.setattr(bench, "ROOT", root)
+    assert bench.recorded_traffic("tc_bwd_dz", "small") == 210150912
+    assert bench.recorded_traffic("tc_dh_kept", "small-untiled") == 209008128
+    assert bench.recorded_traffic("tc_bwd_dz", "small-untiled") is None
+    assert bench.recorded_traffic("tc_bwd_dh", "small") is None
+    # captured from other kernel sources: not reported
+    assert bench.recorded_traffic("tc_bwd_dh", "audio40") is None
+
+
+def test_source_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
+    src = tmp_path / "asr_tiled_tanh_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k_tc.cu").write_text("int f() { return 1; }  // a comment\n")
+    (src / "ptx.cuh").write_text("/* header */\n#define X 1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (src / "k_tc.cu").write_text("int  f()\n{ return 1; }  // another comment\n")
+    assert bench.kernel_source_hash() == h0
+    (src / "k_tc.cu").write_text("int f() { return 2; }\n")
+    assert bench.kernel_source_hash() != h0
+
+
+def test_committed_profiles_cover_the_current_sources():
+    # the summaries in profiles/ were captured from the kernels as they stand
+    assert bench.recorded_traffic("tc_bwd_dz", "small") is not None
+    assert bench.recorded_traffic("tc_bwd_dh", "audio40") is not None
+    assert os.path.isdir(os.path.join(bench.ROOT, "profiles"))

@@ -231,10 +231,10 @@ def rnnt_profile_stop() -> dict:
 
 
 def rnnt_testing_gemm_bf16(A, a_mn, B, b_mn, C, M, N, K, accumulate=0, k_splits=1, bn=256,
-                           cluster=1, stream=None):
+                           stream=None):
     """The library's tcgen05 GEMM alone (include/rnnt_testing.h)."""
     _check(load().rnnt_testing_gemm_bf16(M, N, K, _p(A), a_mn, _p(B), b_mn, _p(C), accumulate,
-                                         k_splits, bn, cluster, _stream(stream)),
+                                         k_splits, bn, _stream(stream)),
            "rnnt_testing_gemm_bf16")
 
 

@@ -221,6 +221,14 @@ rnnt_status check_common(const rnnt_dims* dims, const void* hA, const void* hL,
                          const int32_t* U_len, void* saved, void* ws, size_t ws_bytes,
                          Plan* p) {
   if (!make_plan(dims, p)) return RNNT_ERR_INVALID_ARG;
+  if (p->mode == RNNT_UNTILED) {
+    // Untiled mode keeps every position's z and scores in `saved`: a plan
+    // whose saved state exceeds the device's memory is refused first, before
+    // any buffer is looked at (the 40 s, batch-1024 lattice would need ~0.9 TB)
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) == cudaSuccess && p->s_total > total_b)
+      return RNNT_ERR_WORKSPACE_TOO_SMALL;
+  }
   if (!pr || !saved || !ws) return RNNT_ERR_INVALID_ARG;
   if (!aligned(saved) || !aligned(ws)) return RNNT_ERR_INVALID_ARG;
   if (p->B > 0 && (!hA || !hL || !labels || !T_len || !U_len)) return RNNT_ERR_INVALID_ARG;
@@ -232,11 +240,6 @@ rnnt_status check_common(const rnnt_dims* dims, const void* hA, const void* hL,
     if (s != RNNT_OK) return s;
   }
   if (ws_bytes < p->w_total) return RNNT_ERR_WORKSPACE_TOO_SMALL;
-  if (p->mode == RNNT_UNTILED) {
-    size_t free_b = 0, total_b = 0;
-    if (cudaMemGetInfo(&free_b, &total_b) == cudaSuccess && p->s_total > total_b)
-      return RNNT_ERR_WORKSPACE_TOO_SMALL;
-  }
   return RNNT_OK;
 }
 

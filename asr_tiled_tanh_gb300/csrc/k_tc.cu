@@ -62,8 +62,7 @@ constexpr int STAGE_PITCH = 80;
 struct TcParams {
   int M, N, K;
   int m_tiles, n_tiles, k_splits, kb_total, kb_per_split;
-  int units;             // including the padding units of a ragged last cluster group
-  int m_groups;          // M tiles in groups of the cluster size
+  int units;
   int row_complete;      // a unit is one M tile with all of its N tiles, in order
   int n_split;           // row-complete units: N tiles split into this many units (1 for LSE)
   int n_split_auto;      // n_split is a maximum: the kernel picks the split from the
@@ -125,30 +124,25 @@ struct Unit {
   int m, n0, n1, kb0, kb1;  // M tile, N tiles [n0,n1), K blocks [kb0,kb1)
 };
 
-// Unit u of a cluster of CL CTAs: consecutive units differ only in M (by the
-// CTA's rank in the cluster), so the CTAs of a cluster always need the same
-// B tiles at the same time.  M tiles past the matrix are padding: their A
-// loads are zero-filled and their epilogues write nothing.
-template <int CL>
+// Unit u of a GEMM.  Row-complete units: M tile, then the V split of its N
+// tiles.  Other units: N fastest, then M, then the K split, so that the CTAs
+// working at the same time share K ranges and each K block of A and B is
+// fetched from DRAM about once and served to the other units from L2.
 __device__ __forceinline__ Unit unit_of(const TcParams& p, int u, int kb_lim, int kbps, int ns) {
   Unit w;
-  const int r = u % CL;
-  int rest = u / CL;
+  int rest = u;
   if (p.row_complete) {
     const int per = (p.n_tiles + ns - 1) / ns;
     const int sp = rest % ns;
-    w.m = (rest / ns) * CL + r;
+    w.m = rest / ns;
     w.n0 = sp * per; w.n1 = min(p.n_tiles, w.n0 + per);
     w.kb0 = 0; w.kb1 = (w.n1 > w.n0) ? p.kb_total : 0;
   } else {
-    // N fastest, then M, then the K split: the clusters working at the same
-    // time share K ranges, so each K block of A and B is fetched from DRAM
-    // about once and served to the other units from L2
     const int n = rest % p.n_tiles;
     rest /= p.n_tiles;
-    const int mg = rest % p.m_groups;
-    const int ks = rest / p.m_groups;
-    w.m = mg * CL + r;
+    const int mt = rest % p.m_tiles;
+    const int ks = rest / p.m_tiles;
+    w.m = mt;
     w.n0 = n; w.n1 = n + 1;
     w.kb0 = ks * kbps;
     w.kb1 = min(kb_lim, w.kb0 + kbps);
@@ -182,12 +176,10 @@ struct RowCell {
   int b, t, u, Tb, Ub;
 };
 
-// Whether tile m of a chunk is read by any GEMM: the actual tiles, and the
-// padding tiles that complete the last cluster group (up to 4 CTAs) - the
-// chunk itself is sized by an upper bound, and the GEMMs skip the rest.
+// Whether tile m of a chunk is read by any GEMM: the actual tiles only (the
+// chunk itself is sized by an upper bound, and the GEMMs skip the rest).
 __device__ __forceinline__ bool tile_in_use(const ChunkArgs& c, int m) {
-  const long long have = (long long)*c.sv.total_tiles - c.first_tile;
-  return m < ((have + 3) / 4) * 4;
+  return (long long)m < (long long)*c.sv.total_tiles - c.first_tile;
 }
 
 __device__ __forceinline__ RowCell row_of(const TileRef& tr, int row) {
@@ -482,17 +474,12 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   }
 }
 
-template <int BN, int A_MN, int B_MN, int EPI, int CL>
+template <int BN, int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(Cfg<BN, EPI>::THREADS, 1)
 k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using C = Cfg<BN, EPI>;
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
-  static_assert(!B_MN || BN / 64 >= CL, "each CTA of a cluster loads whole 64-column B boxes");
-  // CTAs of a cluster share each B stage: CTA r loads slice r and multicasts it
-  const uint32_t crank = CL > 1 ? ptx::cluster_ctarank() : 0;
-  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
-  const int cluster_id = blockIdx.x / CL, n_clusters = gridDim.x / CL;
+  const int cta = blockIdx.x, n_ctas = gridDim.x;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
   constexpr int STAGES = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -515,7 +502,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], CL);  // released by the MMAs of every CTA of the cluster
+      ptx::mbar_init(&empty[s], 1);  // released by the MMA commit of the stage
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&acc_full[a], 1);
@@ -536,7 +523,6 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (CL > 1) ptx::cluster_sync();  // peers' barriers are initialised before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // Launched as the programmatic dependent of the stream's previous kernel:
@@ -551,20 +537,20 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const long long have = max(0LL, min(p.ch.ntiles, (long long)*p.ch.sv.total_tiles -
                                                          p.ch.first_tile));
     if (p.tiles_on == TILES_ON_M) {
-      const int groups = (int)((have + CL - 1) / CL);
+      const int tiles = (int)have;
       // fewer than ~4 waves of tiles: each tile's V range is split over
       // several units so that the last wave is not mostly idle
-      if (p.n_split_auto && groups > 0)
-        ns = max(1, min(ns, (int)((4LL * (gridDim.x / CL) + groups - 1) / groups)));
+      if (p.n_split_auto && tiles > 0)
+        ns = max(1, min(ns, (int)((4LL * n_ctas + tiles - 1) / tiles)));
       // (row-complete: the V split is the fast index; otherwise N, with no K split)
-      units = min(units, groups * (p.row_complete ? ns : p.n_tiles) * CL);
+      units = min(units, tiles * (p.row_complete ? ns : p.n_tiles));
     } else {
       kb_lim = (int)min((long long)p.kb_total, have * (BM / BK));
       // the host's split count (chosen for whole waves) over the K blocks
       // that exist: equal splits instead of fewer, full-length ones
       kbps = max(1, (kb_lim + p.k_splits - 1) / p.k_splits);
       const int splits = (kb_lim + kbps - 1) / kbps;
-      units = min(units, splits * p.m_groups * p.n_tiles * CL);
+      units = min(units, splits * p.m_tiles * p.n_tiles);
     }
   }
 
@@ -575,8 +561,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       uint32_t phase = 0;
       int issued[6] = {-1, -1, -1, -1, -1, -1};  // parity of the last fill per stage
       bool first_fill = true;
-      for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
+      for (int gi = cta; gi < units && !*abort_flag; gi += n_ctas) {
+        const Unit w = unit_of(p, gi, kb_lim, kbps, ns);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -599,24 +585,12 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               ptx::tma_load_2d(a, &tmA, &full[stage], w.m * BM, kb * BK);
               ptx::tma_load_2d(a + 64 * 128, &tmA, &full[stage], w.m * BM + 64, kb * BK);
             }
-            if (CL == 1) {
-              if (!B_MN) {
-                ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
-              } else {
-#pragma unroll
-                for (int j = 0; j < BN / 64; ++j)
-                  ptx::tma_load_2d(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j, kb * BK);
-              }
-            } else if (!B_MN) {
-              // rows [crank * BN/CL, +BN/CL) of the B tile, to every CTA of the cluster
-              ptx::tma_load_2d_mc(b + crank * (BN / CL) * 128, &tmB, &full[stage], kb * BK,
-                                  n * BN + (int)crank * (BN / CL), kMask);
+            if (!B_MN) {
+              ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
-                if (j % CL == (int)crank)
-                  ptx::tma_load_2d_mc(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j,
-                                      kb * BK, kMask);
+                ptx::tma_load_2d(b + j * 64 * 128, &tmB, &full[stage], n * BN + 64 * j, kb * BK);
             }
 #pragma unroll
             for (int k = 0; k < 6; ++k)
@@ -641,8 +615,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-        const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
+      for (int gi = cta; gi < units && !*abort_flag; gi += n_ctas) {
+        const Unit w = unit_of(p, gi, kb_lim, kbps, ns);
         if (w.kb1 <= w.kb0) continue;
         for (int n = w.n0; n < w.n1 && !*abort_flag; ++n) {
           if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, wait_ns)) {
@@ -671,8 +645,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                                        : ptx::sdesc_sw128(b0 + k * 32, 16, 1024);
               ptx::mma_bf16(d_tmem, ad, bd, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
             }
-            if (CL == 1) ptx::mma_commit(&empty[stage]);
-            else ptx::mma_commit_mc(&empty[stage], kMask);
+            ptx::mma_commit(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
@@ -703,20 +676,20 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint32_t acc_phase = 0;
     // dh epilogue: the row's record of the next unit is loaded one unit ahead
     float4 post_next = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
-    if (EPI == EPI_DH && cluster_id * CL < units) {
-      const Unit w0 = unit_of<CL>(p, cluster_id * CL + (int)crank, kb_lim, kbps, ns);
+    if (EPI == EPI_DH && cta < units) {
+      const Unit w0 = unit_of(p, cta, kb_lim, kbps, ns);
       if (w0.m < p.ch.ntiles) post_next = __ldg(p.post + (long long)w0.m * BM + row);
     }
-    for (int gi = cluster_id; gi * CL < units && !*abort_flag; gi += n_clusters) {
-      const Unit w = unit_of<CL>(p, gi * CL + (int)crank, kb_lim, kbps, ns);
+    for (int gi = cta; gi < units && !*abort_flag; gi += n_ctas) {
+      const Unit w = unit_of(p, gi, kb_lim, kbps, ns);
       const float4 post_cur = post_next;
-      if (EPI == EPI_DH && (gi + n_clusters) * CL < units) {
-        const Unit wn = unit_of<CL>(p, (gi + n_clusters) * CL + (int)crank, kb_lim, kbps, ns);
+      if (EPI == EPI_DH && gi + n_ctas < units) {
+        const Unit wn = unit_of(p, gi + n_ctas, kb_lim, kbps, ns);
         post_next = (wn.m < p.ch.ntiles) ? __ldg(p.post + (long long)wn.m * BM + row)
                                          : make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
       }
       if (w.kb1 <= w.kb0) continue;
-      const int uidx = gi / n_clusters;   // this CTA's unit counter
+      const int uidx = gi / n_ctas;   // this CTA's unit counter
       // per-unit state of the lattice epilogues
       TileRef tr{};
       RowCell rc{};
@@ -941,7 +914,6 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (CL > 1) ptx::cluster_sync();  // no CTA leaves while a peer may still signal it
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
@@ -1478,47 +1450,28 @@ struct GemmDesc {
   int M, N, K;
 };
 
-template <int BN, int AMN, int BMN, int EPI, int CL>
-cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStream_t s) {
+template <int BN, int AMN, int BMN, int EPI>
+cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   using C = Cfg<BN, EPI>;
-  auto kern = k_tc_gemm<BN, AMN, BMN, EPI, CL>;
+  auto kern = k_tc_gemm<BN, AMN, BMN, EPI>;
   CUtensorMap ta, tb;
   const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64) : make_tmap(&ta, g.A, g.M, g.K, BM);
-  const bool ok_b =
-      BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN / CL);
+  const bool ok_b = BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   // dh / kept-score epilogues: the store map of the [M][N] tile buffer; the
   // other epilogues never read the third map
   CUtensorMap tc = ta;
   if (box_store(EPI) && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
-  static int clusters_of[kDeviceSlots] = {};  // per instantiation and device (0: not set up)
-  int& max_clusters = clusters_of[device_slot()];
-  if (max_clusters <= 0) {
+  static bool opted_in[kDeviceSlots] = {};  // per instantiation and device
+  bool& opted = opted_in[device_slot()];
+  if (!opted) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
-    max_clusters = num_sms();
-    if (CL > 1) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = CL;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(CL * 64);
-      cfg.blockDim = dim3(C::THREADS);
-      cfg.dynamicSmemBytes = C::SMEM;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
-        n = num_sms() / CL;
-      max_clusters = n;
-    }
+    opted = true;
   }
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.m_tiles = (int)cdiv(g.M, BM);
-  p.m_groups = (int)cdiv(p.m_tiles, CL);
   p.n_tiles = (int)cdiv(g.N, BN);
   p.kb_total = (int)cdiv(g.K, BK);
   if (p.k_splits < 1) p.k_splits = 1;
@@ -1526,83 +1479,49 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, int max_units, cudaStre
   p.k_splits = (int)cdiv(p.kb_total, p.kb_per_split);
   if (p.n_split < 1 || !p.row_complete) p.n_split = 1;
   if (p.n_split > p.n_tiles) p.n_split = p.n_tiles;
-  const int groups =
-      p.row_complete ? p.m_groups * p.n_split : p.m_groups * p.n_tiles * p.k_splits;
-  p.units = groups * CL;
-  if (groups <= 0 || g.K <= 0) return cudaSuccess;
-  const int cap = max_units > 0 ? max_units : (CL > 1 ? max_clusters : num_sms());
-  const int grid_groups = std::min(groups, cap);
+  p.units = p.row_complete ? p.m_tiles * p.n_split : p.m_tiles * p.n_tiles * p.k_splits;
+  if (p.units <= 0 || g.K <= 0) return cudaSuccess;
+  // persistent: at most one CTA per SM, each walking units gridDim apart
+  const int grid = std::min(p.units, num_sms());
   // programmatic dependent launch: the kernel's set-up (barriers, TMEM,
   // descriptor prefetch) may overlap the tail of the stream's previous kernel
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = CL;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(grid_groups * CL);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = CL > 1 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 
-// Cluster size used for a GEMM: CTAs of a cluster share B tiles over TMA
-// multicast.  Needs at least CL M tiles (padding units cover the rest).
-
 template <int EPI>
-cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, int cl, cudaStream_t s) {
-  // Only the operand layouts / cluster sizes each epilogue is used with are
-  // instantiated: the lattice epilogues take K-major scores/z (and an
-  // MN-major W^O for dz); the store and atomic epilogues take every layout.
-  if constexpr (EPI != EPI_LSEK) {
-    if (g.M <= BM) cl = 1;
-  }
-  if constexpr (EPI == EPI_LSEK) {  // (untiled mode: single CTAs only)
+cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, cudaStream_t s) {
+  // Only the operand layouts each epilogue is used with are instantiated:
+  // the lattice epilogues take K-major scores/z (and an MN-major W^O for
+  // dz); the store and atomic epilogues take every layout.
+  if constexpr (lse_like(EPI) || EPI == EPI_DH) {
     if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
-    if (bn == 256) return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
-    return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
-  } else if constexpr (EPI == EPI_LSE || EPI == EPI_DH) {
-    if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
-    if (bn == 256) {
-      if (cl >= 4) return launch_gemm_t<256, 0, 0, EPI, 4>(g, p, 0, s);
-      if (cl == 2) return launch_gemm_t<256, 0, 0, EPI, 2>(g, p, 0, s);
-      return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
-    }
-    return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
+    if (bn == 256) return launch_gemm_t<256, 0, 0, EPI>(g, p, s);
+    return launch_gemm_t<128, 0, 0, EPI>(g, p, s);
   } else if constexpr (EPI == EPI_DA) {
     if (g.a_mn || !g.b_mn) return cudaErrorInvalidValue;
-    if (bn == 256) {
-      if (cl >= 4) return launch_gemm_t<256, 0, 1, EPI, 4>(g, p, 0, s);
-      if (cl == 2) return launch_gemm_t<256, 0, 1, EPI, 2>(g, p, 0, s);
-      return launch_gemm_t<256, 0, 1, EPI, 1>(g, p, 0, s);
-    }
-    if (cl >= 2) return launch_gemm_t<128, 0, 1, EPI, 2>(g, p, 0, s);
-    return launch_gemm_t<128, 0, 1, EPI, 1>(g, p, 0, s);
+    if (bn == 256) return launch_gemm_t<256, 0, 1, EPI>(g, p, s);
+    return launch_gemm_t<128, 0, 1, EPI>(g, p, s);
   } else {
-    if (EPI == EPI_ATOMIC && g.a_mn && g.b_mn && cl > 1) {
-      if (bn == 256) {
-        if (cl >= 4) return launch_gemm_t<256, 1, 1, EPI, 4>(g, p, 0, s);
-        return launch_gemm_t<256, 1, 1, EPI, 2>(g, p, 0, s);
-      }
-      return launch_gemm_t<128, 1, 1, EPI, 2>(g, p, 0, s);
-    }
-    if (EPI == EPI_STORE && !g.a_mn && !g.b_mn && cl > 1 && bn == 256)
-      return launch_gemm_t<256, 0, 0, EPI, 2>(g, p, 0, s);
     const int code = (bn == 256 ? 4 : 0) | (g.a_mn ? 2 : 0) | (g.b_mn ? 1 : 0);
     switch (code) {
-      case 0: return launch_gemm_t<128, 0, 0, EPI, 1>(g, p, 0, s);
-      case 1: return launch_gemm_t<128, 0, 1, EPI, 1>(g, p, 0, s);
-      case 2: return launch_gemm_t<128, 1, 0, EPI, 1>(g, p, 0, s);
-      case 3: return launch_gemm_t<128, 1, 1, EPI, 1>(g, p, 0, s);
-      case 4: return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, 0, s);
-      case 5: return launch_gemm_t<256, 0, 1, EPI, 1>(g, p, 0, s);
-      case 6: return launch_gemm_t<256, 1, 0, EPI, 1>(g, p, 0, s);
-      default: return launch_gemm_t<256, 1, 1, EPI, 1>(g, p, 0, s);
+      case 0: return launch_gemm_t<128, 0, 0, EPI>(g, p, s);
+      case 1: return launch_gemm_t<128, 0, 1, EPI>(g, p, s);
+      case 2: return launch_gemm_t<128, 1, 0, EPI>(g, p, s);
+      case 3: return launch_gemm_t<128, 1, 1, EPI>(g, p, s);
+      case 4: return launch_gemm_t<256, 0, 0, EPI>(g, p, s);
+      case 5: return launch_gemm_t<256, 0, 1, EPI>(g, p, s);
+      case 6: return launch_gemm_t<256, 1, 0, EPI>(g, p, s);
+      default: return launch_gemm_t<256, 1, 1, EPI>(g, p, s);
     }
   }
 }
@@ -1632,13 +1551,6 @@ int pick_splits(int units_mn, int K) {
   return best;
 }
 
-// Cluster size of the lattice GEMMs (scores, dh, dz, dW^O) and the
-// encoder-side weight gradients.  Measured on GB300: 2-CTA clusters sharing
-// B over multicast gave no gain (the kernels are not L2-bound) and pair the
-// CTAs' unit schedules, so single CTAs are used; the cluster path stays
-// available (and tested) for larger B tiles.
-constexpr int kClusterLattice = 1;
-
 #define TC_CHECK(expr)                                   \
   do {                                                   \
     cudaError_t e_ = (expr);                             \
@@ -1667,7 +1579,7 @@ cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const voi
   tp.C = out;
   tp.ldc = p.H;
   tp.bias = (const __nv_bfloat16*)bias;
-  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), 1, s);
+  return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), s);
 }
 
 namespace {
@@ -1726,8 +1638,8 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
     tp.Hout = (__nv_bfloat16*)Hkeep;
     tp.status = sv.status;
     tp.tiles_on = TILES_ON_M;
-    const cudaError_t e = Hkeep ? launch_gemm<EPI_LSEK>(g, tp, 256, 1, s)
-                                : launch_gemm<EPI_LSE>(g, tp, 256, kClusterLattice, s);
+    const cudaError_t e = Hkeep ? launch_gemm<EPI_LSEK>(g, tp, 256, s)
+                                : launch_gemm<EPI_LSE>(g, tp, 256, s);
     if (e != cudaSuccess) return RNNT_ERR_CUDA;
   }
   return RNNT_OK;
@@ -1792,7 +1704,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       // reductions need a 16-byte aligned db^O)
       if (dbO && ((uintptr_t)dbO & 15) == 0) tp.dbO = dbO;
       tp.tiles_on = TILES_ON_M;
-      if (launch_gemm<EPI_DH>(g, tp, 256, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_gemm<EPI_DH>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
       {
         ProfScope ps("tc_posteriors", s);
@@ -1821,7 +1733,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.dLr = dLr;
       tp.status = sv.status;
       tp.tiles_on = TILES_ON_M;
-      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), kClusterLattice, s) != cudaSuccess)
+      if (launch_gemm<EPI_DA>(g, tp, pick_bn(p.H, rows), s) != cudaSuccess)
         return RNNT_ERR_CUDA;
     }
     // the last chunk's dW^O runs beside the caller's work that needs only
@@ -1839,7 +1751,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.status = sv.status;
       tp.ch = c;
       tp.tiles_on = TILES_ON_K;
-      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, fork.side(0)) != cudaSuccess)
+      if (launch_gemm<EPI_ATOMIC>(g, tp, bn, fork.side(0)) != cudaSuccess)
         return RNNT_ERR_CUDA;
     }
     if (last && after) {
@@ -1892,14 +1804,14 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HA, bn)), MA);
     tp.C = dWA;
     tp.ldc = p.HA;
-    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, s) != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, s) != cudaSuccess) return RNNT_ERR_CUDA;
   }
   if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
     GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};
     TcParams tp{};
     tp.C = dhA;
     tp.ldc = p.HA;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), 1, fork.side(0)) != cudaSuccess)
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), fork.side(0)) != cudaSuccess)
       return RNNT_ERR_CUDA;
   }
   if (dhL) {
@@ -1907,7 +1819,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     TcParams tp{};
     tp.C = dhL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), 1, fork.side(1)) != cudaSuccess)
+    if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), fork.side(1)) != cudaSuccess)
       return RNNT_ERR_CUDA;
   }
   if (dWL) {
@@ -1917,7 +1829,7 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     tp.k_splits = pick_splits((int)(cdiv(p.H, BM) * cdiv(p.HL, bn)), ML);
     tp.C = dWL;
     tp.ldc = p.HL;
-    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, kClusterLattice, fork.side(2)) != cudaSuccess)
+    if (launch_gemm<EPI_ATOMIC>(g, tp, bn, fork.side(2)) != cudaSuccess)
       return RNNT_ERR_CUDA;
   }
   if (dbZ) {  // db^Z = sum of dA over frames (= sum of da over every position)
@@ -1948,7 +1860,7 @@ extern "C" rnnt_status rnnt_testing_gemm_timeout(int M, int N, int K, const void
   tp.status = status;
   tp.wait_ns = wait_ns;
   tp.skip_first_fill = 1;
-  cudaError_t e = launch_gemm<EPI_STORE>(g, tp, 128, 1, (cudaStream_t)stream);
+  cudaError_t e = launch_gemm<EPI_STORE>(g, tp, 128, (cudaStream_t)stream);
   return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
 }
 
@@ -1956,12 +1868,11 @@ extern "C" rnnt_status rnnt_testing_gemm_timeout(int M, int N, int K, const void
 // Test hook (include/rnnt_testing.h): one raw GEMM through the same kernel.
 extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A, int a_mn,
                                               const void* B, int b_mn, float* C, int accumulate,
-                                              int k_splits, int bn, int cluster, void* stream) {
+                                              int k_splits, int bn, void* stream) {
   using namespace rnnt;
   if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C) return RNNT_ERR_INVALID_ARG;
   if ((a_mn ? M : K) % 8 || (b_mn ? N : K) % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
   if (bn != 128 && bn != 256) return RNNT_ERR_INVALID_ARG;
-  if (cluster != 1 && cluster != 2 && cluster != 4) return RNNT_ERR_INVALID_ARG;
   if (!encode_fn()) return RNNT_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   GemmDesc g{A, a_mn, B, b_mn, M, N, K};
@@ -1969,7 +1880,7 @@ extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A
   tp.C = C;
   tp.ldc = N;
   tp.k_splits = k_splits;
-  cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, cluster, s)
-                             : launch_gemm<EPI_STORE>(g, tp, bn, cluster, s);
+  cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, s)
+                             : launch_gemm<EPI_STORE>(g, tp, bn, s);
   return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
 }

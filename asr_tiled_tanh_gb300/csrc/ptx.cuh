@@ -82,17 +82,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA of
-// the cluster in `mask`, each CTA's mbarrier (same offset) receiving the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                               int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 // 2-D tiled store: the box at (x, y) of the tensor is written from shared
 // memory by the TMA engine, in this thread's current bulk async-group.  The
 // shared-memory source must not change until bulk_wait_read() says it has
@@ -154,18 +143,6 @@ __device__ __forceinline__ void griddep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ---- clusters -------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// All threads of all CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // ---- tcgen05 --------------------------------------------------------------
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
 // written to shared memory at `dst`.  Warp-wide.
@@ -202,14 +179,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of
-// the cluster in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 // 32 lanes x 32 consecutive fp32 columns: thread l of the warp gets lane

@@ -5,7 +5,12 @@ row of the hot path: validation, projections, the tiled joint/output/LSE
 forward, alpha/beta, the tiled recompute backward, the encoder gradients),
 through rnnt_fwd_bwd (`--api separate`: rnnt_fwd then rnnt_bwd).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload audio40] [--impl reference]
+
+The default workload is the 40 s, batch-1024 configuration (B=1024, T=1000,
+U=100, H=512, V=4096, bf16, tiled); the other workloads of
+asr_tiled_tanh_gb300/synthetic.py are parity-test cases that can be timed the
+same way with --workload.
 
 Prints one JSON line (rank 0).  `value` is lattice cells B*T*(U+1) per second
 over all ranks with inputs already in HBM; `e2e` is the same metric through
@@ -13,7 +18,9 @@ the C ABI with host buffers: every timed step copies its batch (hA, hL,
 labels, lengths) from pinned host memory to the device and reads its losses
 back; the parameters and their gradients stay on the device, where a training
 step keeps them.  Each rank runs its own batch (weak
-scaling); there is no data-path collective.  L2 is flushed (256 MiB write)
+scaling, data-parallel): with N ranks every step ends with one all-reduce
+(sum) of the parameter gradients, the only exchange the path has.  `--gpus N`
+starts N processes itself when no launcher did.  L2 is flushed (256 MiB write)
 before every timed step, outside the step's events.
 
 When the library reports the plan capturable (rnnt_graph_capturable: the
@@ -214,14 +221,21 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
 
 
 def kernel_source_hash() -> str:
-    """sha1 of the tensor-core kernel sources with comments and whitespace
-    removed (the ncu traffic figures are only valid for the code they were
-    captured from)."""
+    """sha1 of every library source (kernels, headers, the host plan and
+    launch code in csrc/) with comments and whitespace removed: the ncu
+    traffic figures are only valid for the code they were captured from, and
+    tile geometry, plan layout and launch parameters change a kernel's DRAM
+    bytes as much as its body does."""
+    import glob
     import hashlib
     import re
     h = hashlib.sha1()
-    for f in ("k_tc.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc", f)) as fh:
+    csrc = os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")))
+    for path in files:
+        h.update(os.path.basename(path).encode())
+        with open(path) as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
@@ -244,6 +258,18 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def _tiles_per_chunk(rn, dims) -> int:
+    """Lattice tiles whose intermediates a plan holds at once, read back from
+    the workspace size: each tile of a chunk adds 128 rows of bf16 z and
+    scores and a 16-byte posterior record per row."""
+    import copy
+    one = copy.copy(dims)
+    one.tile_cells = 128
+    per_tile = 128 * (2 * dims.H + 2 * dims.V + 16)
+    extra = rn.rnnt_workspace_bytes(dims) - rn.rnnt_workspace_bytes(one)
+    return 1 + int(round(extra / per_tile))
+
+
 def reduce_max(x: float, dist, device) -> float:
     """Max of a per-rank float over all ranks (the slowest rank sets the job time)."""
     if dist is None:
@@ -264,7 +290,7 @@ def run_gpu_bench(args):
     import torch
 
     import asr_tiled_tanh_gb300 as rn
-    from asr_tiled_tanh_gb300 import synthetic
+    from asr_tiled_tanh_gb300 import shard, synthetic
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -290,7 +316,9 @@ def run_gpu_bench(args):
     d = {k: getattr(inp, k).to(dev) for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO", "labels",
                                                "T_len", "U_len")}
     params = rn.make_params(d["WA"], d["WL"], d["bZ"], d["WO"], d["bO"])
-    grads = r.alloc_grads()
+    # parameter gradients in one flat buffer: with several ranks, one
+    # all-reduce (sum) of it ends every step (data-parallel training)
+    grad_flat, grads = shard.alloc_grads(wl.B, wl.T, wl.U1, wl.HA, wl.HL, wl.H, wl.V, device=dev)
     loss = torch.empty(wl.B, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(max(1, args.flush_mb) << 20, dtype=torch.uint8, device=dev)
@@ -299,10 +327,14 @@ def run_gpu_bench(args):
         if args.api == "step":  # rnnt_fwd_bwd: one call for the training step
             r.fwd_bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
                       grads=grads, stream=s)
-            return
-        r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss, stream=s)
-        r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads,
-              stream=s)
+        else:
+            r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss,
+                  stream=s)
+            r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads,
+                  stream=s)
+        if dist is not None:
+            with torch.cuda.stream(s):
+                shard.allreduce_param_grads(grad_flat, dist)
 
     def captured(fn):
         """fn (which launches on the stream it is given) as a CUDA graph whose
@@ -328,7 +360,7 @@ def run_gpu_bench(args):
 
     # A plan whose calls make no host synchronization (the whole lattice fits
     # one chunk of the tile buffers) is replayed as a CUDA graph of the step.
-    use_graph = not args.eager and rn.rnnt_graph_capturable(r.dims) == 1
+    use_graph = not args.eager and rn.rnnt_graph_capturable(r.dims) == 1 and dist is None
     graph = captured(step) if use_graph else None
     run = graph.replay if graph is not None else step
 
@@ -399,6 +431,34 @@ def run_gpu_bench(args):
         torch.cuda.synchronize()
         e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / args.steps, dist, dev)
         assert np.isfinite(host_loss.numpy()).all()
+        e2e_run = None
+
+    # --- peak HBM at a second tile size -------------------------------------------
+    # Tiled mode holds the large intermediates only for the tiles of one chunk,
+    # so the peak should move with the tile buffers and not with B*T*U*V.  The
+    # first plan's buffers are freed, a plan with a quarter of its tiles per
+    # chunk (whole waves of SMs) runs one step, and both peaks are reported
+    # with their tiles per chunk.
+    tiles_first = _tiles_per_chunk(rn, r.dims)
+    peak_by_tiles = {str(tiles_first): round(peak_bytes / 1e9, 4)}
+    peak_tc = args.peak_tile_cells
+    if peak_tc < 0 and args.mode == "tiled":
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak_tc = max(nsm, (tiles_first // 4) // nsm * nsm) * 128
+    if peak_tc > 0 and args.mode == "tiled" and peak_tc < tiles_first * 128:
+        graph = run = None
+        r.saved = r.ws = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=peak_tc, device=dev)
+        step()
+        torch.cuda.synchronize()
+        code, word = r.status()
+        if code != 0:
+            raise SystemExit(f"device status {code} word {word} (second tile size)")
+        peak_by_tiles[str(_tiles_per_chunk(rn, r.dims))] = \
+            round(torch.cuda.max_memory_allocated(dev) / 1e9, 4)
 
     # --- roofline of the dominant kernel ----------------------------------------
     hbm_peak, tf_burst, tf_sust, peak_src = _peaks()
@@ -453,9 +513,12 @@ def run_gpu_bench(args):
                    "execution": "CUDA graph of the step" if graph is not None else "eager",
                    "mode": args.mode,
                    "api": "rnnt_fwd_bwd" if args.api == "step" else "rnnt_fwd + rnnt_bwd",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"dp{world}",
+                   "collective": ("one all-reduce (sum, NCCL) of the parameter gradients per "
+                                  "step" if world > 1 else "none")},
         "valid_cells_per_s": round(valid * world / (ms_max / 1e3), 1),
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
+        "peak_hbm_gb_by_tiles_per_chunk": peak_by_tiles,
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / peak_tf, 4),
         "e2e": None if e2e_ms is None else {
             "value": round(job_value(nominal, world, e2e_ms), 1), "unit": UNIT,
@@ -479,9 +542,17 @@ def run_gpu_bench(args):
         print(json.dumps(out), flush=True)
 
 
-def _oracle_sample(inp, nsamp):
+def _by_size(inp):
+    """Sample indices of a batch from the smallest lattice to the largest."""
+    cells = (inp.T_len.long() * (inp.U_len.long() + 1)).tolist()
+    return sorted(range(len(cells)), key=lambda b: (cells[b], b))
+
+
+def _oracle_sample(inp, idx):
+    """The oracle, fwd+bwd in fp64, on the samples `idx` of the batch:
+    (seconds, the sub-batch)."""
     import oracle
-    sub = inp.subset(list(range(nsamp)))
+    sub = inp.subset(list(idx))
     f = lambda t: t.double().numpy()
     t0 = time.perf_counter()
     oracle.rnnt(f(sub.hA), f(sub.hL), f(sub.WA), f(sub.WL), f(sub.bZ), f(sub.WO), f(sub.bO),
@@ -489,20 +560,33 @@ def _oracle_sample(inp, nsamp):
     return time.perf_counter() - t0, sub
 
 
+def nominal_equivalent(valid_cells_per_s: float, inp) -> float:
+    """A rate over valid lattice positions expressed in the metric's unit
+    (nominal cells B*T*(U+1) per second of the whole batch): the oracle's cost
+    is per valid position, so a sample's valid-position rate is scaled by the
+    batch's nominal / valid ratio."""
+    return valid_cells_per_s * inp.wl.nominal_cells / max(1, inp.valid_cells())
+
+
 def cpu_baseline(inp, budget_s):
-    """The oracle, as it stands, on a bounded sample of the same workload."""
+    """The oracle, as it stands, on a bounded sample of the same workload: the
+    smallest lattices of the batch first, as many as fit the time budget."""
     import oracle
     oracle.build()
+    order = _by_size(inp)
     n = 1
-    dt, sub = _oracle_sample(inp, n)
+    dt, sub = _oracle_sample(inp, order[:1])
     if dt < budget_s / 3 and inp.wl.B > 1:
         n = max(1, min(inp.wl.B, int(budget_s / max(dt, 1e-3))))
-        dt, sub = _oracle_sample(inp, n)
-    cells = sub.wl.T * sub.wl.U1 * n
-    return {"value": round(cells / dt, 2), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"first {n} sample(s) of the workload, fwd+bwd, fp64 "
-                      f"({sub.valid_cells()} valid of {cells} nominal cells)"}
+        dt, sub = _oracle_sample(inp, order[:n])
+    valid = sub.valid_cells()
+    return {"value": round(nominal_equivalent(valid / dt, inp), 2), "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle", "seconds": round(dt, 3),
+            "valid_cells_per_s": round(valid / dt, 2),
+            "sample": f"the {n} smallest lattice(s) of the workload's batch, fwd+bwd, fp64 "
+                      f"({valid} valid positions in {dt:.1f} s); value = that valid-position "
+                      f"rate x the batch's nominal/valid ratio "
+                      f"({inp.wl.nominal_cells}/{inp.valid_cells()})"}
 
 
 def run_reference(args):
@@ -514,16 +598,22 @@ def run_reference(args):
     oracle.build()
     wl = synthetic.WORKLOADS[args.workload]
     inp = synthetic.make(wl)
-    # one step = the oracle on a bounded sample (1 sample of the workload)
-    for _ in range(args.warmup if args.warmup < 2 else 1):
-        _oracle_sample(inp, 1)
+    # one step = the oracle on a bounded sample of the workload: the batch's
+    # smallest lattice (the full batch would take the oracle hours)
+    idx = _by_size(inp)[:1]
+    for _ in range(min(args.warmup, 1)):
+        _oracle_sample(inp, idx)
     times = []
     for _ in range(args.steps):
-        dt, sub = _oracle_sample(inp, 1)
+        dt, sub = _oracle_sample(inp, idx)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
-    cells = wl.T * wl.U1
-    value = cells / (ms / 1e3)
+    valid = sub.valid_cells()
+    value = nominal_equivalent(valid / (ms / 1e3), inp)
+    sample = (f"sample {idx[0]} of the workload's batch (its smallest lattice: T_b="
+              f"{int(sub.T_len[0])}, U_b={int(sub.U_len[0])}, {valid} valid positions), fwd+bwd, "
+              f"fp64, per step; value = its valid-position rate x the batch's nominal/valid "
+              f"ratio ({wl.nominal_cells}/{inp.valid_cells()})")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
            "n_gpus": args.gpus, "device": "host cores (the oracle runs on no GPU)",
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
@@ -531,11 +621,9 @@ def run_reference(args):
            "data": "synthetic",
            "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "
                                   f"V={wl.V} {wl.dtype}", "B": wl.B, "T": wl.T, "U": wl.U,
-                      "H": wl.H, "V": wl.V},
+                      "H": wl.H, "V": wl.V, "sample": sample},
            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "kind": "oracle",
-                            "cores": oracle.num_threads(),
-                            "sample": "sample 0 of the workload (full T, U), fwd+bwd, fp64, "
-                                      "per step"},
+                            "cores": oracle.num_threads(), "sample": sample},
            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -546,8 +634,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="small")
+    ap.add_argument("--workload", default="audio40",
+                    help="synthetic workload (asr_tiled_tanh_gb300/synthetic.py); the default "
+                         "is the 40 s, batch-1024 configuration")
     ap.add_argument("--tile-cells", type=int, default=0)
+    ap.add_argument("--peak-tile-cells", type=int, default=-1,
+                    help="after the timed steps, peak HBM of one step at this second tile "
+                         "size (-1: a quarter of the first plan's tile buffers; 0: skip)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -566,6 +659,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by a launcher: start one process per GPU here
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+        raise SystemExit(subprocess.call(cmd))
     if args.impl == "reference":
         run_reference(args)
     else:

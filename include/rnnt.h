@@ -54,7 +54,9 @@ typedef enum {
   RNNT_ERR_INVALID_ARG = 1,        /* NULL pointer, negative or zero size, bad enum */
   RNNT_ERR_UNSUPPORTED_SHAPE = 2,  /* shape this build's kernels do not handle */
   RNNT_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes < rnnt_workspace_bytes(), or an
-                                      untiled lattice that cannot be addressed */
+                                      untiled plan whose saved state exceeds the
+                                      device's memory (checked first, before any
+                                      pointer argument) */
   RNNT_ERR_LENGTH_RANGE = 4,       /* device: some T_len not in [1,T] or U_len not in [0,U1-1] */
   RNNT_ERR_LABEL_RANGE = 5,        /* device: some labels[b,1..U_len[b]] not in [0,V) */
   RNNT_ERR_TIMEOUT = 6,            /* device: a bounded wait inside a kernel gave up */
@@ -195,9 +197,12 @@ rnnt_status rnnt_fwd_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
  * that every GPU loading this library holds until the process exits.
  * Returns RNNT_ERR_WORKSPACE_TOO_SMALL, before doing anything else, when
  * rnnt_workspace_bytes(dims) exceeds that size (use a smaller tile_cells, or
- * rnnt_fwd with your own buffer).  The first call on a device looks up the
- * array's device address on that device (cudaGetSymbolAddress, with the
- * device current); make that first call before any stream capture.  Every
+ * rnnt_fwd with your own buffer).  The first call made in a CUDA context
+ * looks up the array's device address in that context (cudaGetSymbolAddress,
+ * with the context current): the primary context of the current device, or
+ * the caller's own context if one is current; after a device reset the new
+ * context gets its own lookup.  Make that first call before any stream
+ * capture.  Every
  * call on a device shares the one array and it keeps the last call's
  * contents; the forward needs none of it cleared.  Calls whose work overlaps
  * on the GPU (other streams, other host threads) race on the array and must

@@ -18,14 +18,12 @@ extern "C" {
  * B is [N,K] row-major (b_mn = 0, i.e. C = A B^T) or [K,N] row-major
  * (b_mn = 1).  accumulate = 0: C is overwritten (k_splits ignored);
  * accumulate = 1: the product is added to C with fp32 atomics, K split into
- * k_splits ranges.  bn: 128 or 256 (the kernel's N tile).  cluster: 1, 2 or
- * 4 CTAs per thread-block cluster sharing B tiles over TMA multicast (where
- * this build has that variant; otherwise 1 is used).  The contiguous
+ * k_splits ranges.  bn: 128 or 256 (the kernel's N tile).  The contiguous
  * extent of each operand must be a multiple of 8 elements and the pointers
  * 16-byte aligned.  Asynchronous on `stream` (a cudaStream_t). */
 rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A, int a_mn, const void* B,
                                    int b_mn, float* C, int accumulate, int k_splits, int bn,
-                                   int cluster, void* stream);
+                                   void* stream);
 
 /* Failure-detection hook: the same GEMM (A [M,K], B [N,K], both K-major,
  * C = A B^T) with the first pipeline stage never filled, so the kernel's

@@ -3,7 +3,9 @@
 Tolerances: fp32 inputs, loss relative error <= 1e-5 and gradient relative L2
 error <= 1e-4; bf16 inputs (the oracle gets the same bf16-rounded values),
 2e-3 and 1e-2.  The -inf pattern of every saved array (which positions are
-outside a lattice, which have no label transition) must match exactly.
+outside a lattice, which have no label transition) must match exactly, and
+their finite values (blank/label log-probabilities, ln P_D, alpha, beta) agree
+to the loss tolerance.
 """
 import numpy as np
 import pytest
@@ -11,8 +13,8 @@ import torch
 
 import asr_tiled_tanh_gb300 as rn
 from asr_tiled_tanh_gb300 import synthetic
-from tests.helpers import (GRAD_KEYS, assert_parity, rel_l2, run_gpu, run_oracle, to_device,
-                           valid_mask)
+from tests.helpers import (GRAD_KEYS, assert_parity, fp32_grad_tol, rel_l2, run_gpu, run_oracle,
+                           to_device, valid_mask)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +33,10 @@ def test_tiny_fp32_workload():
     m = valid_mask(inp)
     for k in ("lpb", "lnPD", "alpha", "beta"):
         np.testing.assert_allclose(gpu[k][m], getattr(orc, k)[m], rtol=2e-5, atol=2e-5)
+    # label log-probabilities exist below the last label position only
+    ml = m & np.isfinite(orc.lpl)
+    assert ml.sum() == inp.wl.B * inp.wl.T * inp.wl.U
+    np.testing.assert_allclose(gpu["lpl"][ml], orc.lpl[ml], rtol=2e-5, atol=2e-5)
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -67,6 +73,8 @@ def test_fp32_long_label_sequences_split_over_warps():
         m = valid_mask(inp)
         for k in ("alpha", "beta"):
             np.testing.assert_allclose(gpu[k][m], getattr(orc, k)[m], rtol=2e-5, atol=2e-5)
+        ml = m & np.isfinite(orc.lpl)
+        np.testing.assert_allclose(gpu["lpl"][ml], orc.lpl[ml], rtol=2e-5, atol=2e-5)
 
 
 def test_small_bf16_workload():
@@ -384,19 +392,24 @@ def test_negative_and_zero_incoming_gradients(dtype, mode):
 def test_long_label_sequences(dtype):
     # U+1 = 301 > 128: the alpha/beta recursion takes the register-prefetch
     # kernel (the shared-memory ring would not fit).  alpha and beta reach
-    # |ln P| ~ (T+U) ln V ~ 1.2e3 here, where one fp32 ulp is ~1.2e-4 in log
+    # |ln P| ~ (T+U) ln V ~ 1.25e3 here, where one fp32 ulp is ~1.2e-4 in log
     # space, so the posteriors exp(alpha + beta - ln P) - and every gradient -
     # carry a relative error of a few 1e-4 on the fp32 path: gradients are held
-    # to 5e-4 there (the loss still to 1e-5)
-    inp = synthetic.custom(B=2, T=24, U=300, HA=32, HL=32, H=64, V=48, dtype=dtype, seed=23,
+    # to helpers.fp32_grad_tol(T, U, V) = 8 u (T+U) ln V = 6.0e-4 there (the
+    # loss still to 1e-5).  That is a limit of the fp32 saved alpha/beta of
+    # this implementation, not of the method.
+    T, U, V = 24, 300, 48
+    inp = synthetic.custom(B=2, T=T, U=U, HA=32, HL=32, H=64, V=V, dtype=dtype, seed=23,
                            bias_std=0.2)
     gpu = run_gpu(inp)
     orc = run_oracle(inp)
     assert gpu["status"] == (0, 0)
     assert_parity(gpu, orc, inp, grads=(dtype == "bf16"))
     if dtype == "f32":
+        tg = fp32_grad_tol(T, U, V)
+        assert 5e-4 < tg < 7e-4
         errs = {k: rel_l2(gpu[k], orc.grads[k]) for k in GRAD_KEYS}
-        assert max(errs.values()) < 5e-4, errs
+        assert max(errs.values()) < tg, errs
 
 
 def test_labels_equal_to_blank_and_repeated():

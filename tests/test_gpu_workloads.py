@@ -7,7 +7,9 @@ samples, (b) the gradients of a sub-batch of those samples against the
 oracle, and (c) properties that hold at any size: every loss finite and
 positive, the output-bias gradient summing to zero over the vocabulary
 (sum_v dh = 0 at every position), batched = sum of sample-wise, and the tile
-buffer, not the lattice, setting the memory.
+buffer, not the lattice, setting the memory.  The large-vocabulary shapes get
+full gradient parity on short lattices, and the 40 s batch's longest lattice
+(full T and U) its loss parity.
 """
 import numpy as np
 import pytest
@@ -82,12 +84,40 @@ def test_bigvocab_workload():
         assert rel_l2(ones[0][k] + ones[1][k], pair[k]) < 1e-4, k
 
 
+@pytest.mark.parametrize("mode,tile_cells", [("tiled", 0), ("tiled", 128), ("untiled", 0)])
+def test_bigvocab_shapes_gradients_against_oracle(mode, tile_cells):
+    # The large-vocabulary configuration's shapes (H = HA = HL = 1024,
+    # V = 16384, Zipf(1.1) labels) on lattices short enough for the oracle's
+    # gradients: every gradient compared with the oracle, in one chunk, in one
+    # tile per chunk (several chunks) and untiled.
+    inp = synthetic.custom(B=3, T=20, U=6, HA=1024, HL=1024, H=1024, V=16384, dtype="bf16",
+                           seed=41, t_frac=0.5, u_frac=0.5, labels="zipf1.1", bias_std=0.1)
+    gpu = run_gpu(inp, mode=mode, tile_cells=tile_cells)
+    assert gpu["status"] == (0, 0)
+    orc = _oracle_cached(inp.wl)
+    errs = assert_parity(gpu, orc, inp)
+    print(mode, tile_cells, "gradient rel L2:", errs)
+
+
+@functools.lru_cache(maxsize=1)
+def _oracle_cached(wl):
+    inp = synthetic.make(wl, bias_std=0.1)
+    return run_oracle(inp)
+
+
 def test_audio40_large_batch_workload():
     inp = _workload("audio40")
     torch.cuda.reset_peak_memory_stats()
     full = run_gpu(inp, keep_saved=False)
     peak = torch.cuda.max_memory_allocated()
     _check_full_batch(inp, full, n_loss=2, n_grad=2)
+    # the longest lattice: sample 0 has the full T = 1000 frames and U = 100
+    # labels (101,000 positions, |ln P| ~ 9e3); its loss from the full-batch
+    # run against the oracle's forward on that sample alone
+    assert int(inp.T_len[0]) == inp.wl.T and int(inp.U_len[0]) == inp.wl.U
+    o0 = run_oracle(inp.subset([0]), want_grad=False)
+    lrel = abs(full["loss"][0] - o0.loss[0]) / abs(o0.loss[0])
+    assert lrel <= TOL["bf16"][0], (full["loss"][0], o0.loss[0], lrel)
     # memory is set by the tile buffer, not by B*T*(U+1)*V (847 GB of bf16 scores)
     nominal_scores = inp.wl.B * inp.wl.T * inp.wl.U1 * inp.wl.V * 2
     assert peak < nominal_scores / 40, peak
@@ -116,3 +146,22 @@ def test_audio40_memory_tracks_tile_size():
     # the difference in peak memory is the difference in tile buffers (allocator slack 64 MiB)
     assert abs((peaks[1] - peaks[0]) - (ws[1] - ws[0])) < 64 << 20
     assert torch.equal(losses[0], losses[1])
+
+
+def test_untiled_mode_refuses_the_40s_batch():
+    # Untiled mode keeps z and the scores of every lattice position: at the
+    # 40 s, batch-1024 shapes that is ~0.9 TB of bf16 scores, more than the
+    # device holds, so rnnt_fwd refuses the plan before it looks at any buffer
+    # (the pointers are all NULL: no launch can happen whatever the outcome;
+    # a missing check would show as RNNT_ERR_INVALID_ARG instead)
+    dims = rn.make_dims(1024, 1000, 101, 512, 512, 512, 4096, 0, rn.RNNT_BF16, rn.RNNT_UNTILED, 0)
+    assert rn.rnnt_saved_bytes(dims) > torch.cuda.get_device_properties(0).total_memory
+    params = rn.make_params(None, None, None, None, None)
+    code = rn.rnnt_fwd(dims, None, None, params, None, None, None, None, None, None,
+                       check=False)
+    assert code == 3  # RNNT_ERR_WORKSPACE_TOO_SMALL
+    # the same shapes tiled are a valid plan (they fail here only on the NULL buffers)
+    tiled = rn.make_dims(1024, 1000, 101, 512, 512, 512, 4096, 0, rn.RNNT_BF16, rn.RNNT_TILED, 0)
+    code = rn.rnnt_fwd(tiled, None, None, params, None, None, None, None, None, None,
+                       check=False)
+    assert code == 1  # RNNT_ERR_INVALID_ARG

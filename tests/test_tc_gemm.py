@@ -53,23 +53,6 @@ def test_gemm_layouts_split_k_atomic(a_mn, b_mn):
     assert err < 1e-3 * K ** 0.5, err
 
 
-@pytest.mark.parametrize("cluster,bn,layout", [(2, 256, (0, 0)), (2, 256, (1, 1)),
-                                               (4, 256, (1, 1)), (2, 128, (1, 1))])
-def test_gemm_cluster_multicast(cluster, bn, layout):
-    # CTAs of a cluster share B tiles over TMA multicast; M spans a ragged
-    # number of 128-row tiles, so the last cluster group carries padding tiles
-    a_mn, b_mn = layout
-    M, N, K = 128 * 7 + 40, 2 * bn + 64, 448
-    A, B, ref = _case(M, N, K, a_mn, b_mn, 31 + cluster)
-    accumulate = 1 if (a_mn or b_mn) else 0
-    C = torch.zeros((M, N), device="cuda")
-    binding.rnnt_testing_gemm_bf16(A, a_mn, B, b_mn, C, M, N, K, accumulate=accumulate,
-                                   k_splits=3 if accumulate else 1, bn=bn, cluster=cluster)
-    torch.cuda.synchronize()
-    err = (C.double().cpu() - ref).abs().max().item()
-    assert err < 1e-3 * K ** 0.5, err
-
-
 def test_gemm_many_tiles_persistent():
     # more output tiles than SMs: every CTA walks several units
     M, N, K = 128 * 40, 512, 320
@@ -79,7 +62,9 @@ def test_gemm_many_tiles_persistent():
     torch.cuda.synchronize()
     err = (C.double().cpu() - ref).abs().max().item()
     assert err < 1e-3 * K ** 0.5, err
+    # the same product again with 128-wide N tiles (twice the units per CTA):
+    # each output element is one K-ordered fp32 accumulation either way
     C2 = torch.empty((M, N), device="cuda")
-    binding.rnnt_testing_gemm_bf16(A, 0, B, 0, C2, M, N, K, bn=256, cluster=2)
+    binding.rnnt_testing_gemm_bf16(A, 0, B, 0, C2, M, N, K, bn=128)
     torch.cuda.synchronize()
     assert torch.equal(C, C2)

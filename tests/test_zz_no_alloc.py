@@ -4,9 +4,10 @@ Some callers cannot allocate device memory: hosts that reserve all memory up
 front, plugin interfaces that provide no allocator, latency-critical loops.
 rnnt_fwd_noalloc takes its scratch from a fixed device array inside the
 library instead of a caller buffer.  This test calls it through the C ABI
-twice in a row and checks that both calls give what rnnt_fwd gives with a
-caller-provided workspace; it runs last (file name) so that a failure here
-never hides the rest of the suite, and it needs no earlier test's state.
+several times in a row (different values, lengths and chunk counts) and checks
+that every call gives what rnnt_fwd gives with a fresh caller-provided
+workspace; it runs last (file name) so that a failure here never hides the
+rest of the suite, and it needs no earlier test's state.
 """
 import ctypes
 
@@ -36,39 +37,62 @@ def _saved_state(r):
     return {k: getattr(sa, k).clone() for k in ("lnP", "lpb", "lpl", "lnPD", "alpha", "beta")}
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_noalloc_forward_matches_rnnt_fwd_twice(dtype):
-    H, V = (128, 256) if dtype == "bf16" else (64, 96)
-    inp = synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=23,
-                           bias_std=0.1)
+def _call_noalloc(f, r, dev, params, B):
+    loss = torch.full((B,), float("nan"), device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    code = f(ctypes.byref(r.dims), dev["hA"].data_ptr(), dev["hL"].data_ptr(),
+             ctypes.byref(params), dev["labels"].data_ptr(), dev["T_len"].data_ptr(),
+             dev["U_len"].data_ptr(), loss.data_ptr(), r.saved.data_ptr(), stream)
+    assert code == 0, rn.rnnt_status_string(code)
+    torch.cuda.synchronize()
+    return loss
+
+
+def _check_against_rnnt_fwd(f, inp, tile_cells, tag):
+    """One rnnt_fwd_noalloc call against rnnt_fwd with a fresh caller workspace."""
+    dtype = inp.wl.dtype
     dev = to_device(inp)
     params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
-    ref = rn.Rnnt.for_inputs(inp)
+    ref = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)
+    assert rn.rnnt_workspace_bytes(ref.dims) <= 32 << 20
     ref_loss = ref.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
     torch.cuda.synchronize()
+    assert ref.status() == (0, 0)
     ref_state = _saved_state(ref)
-    assert rn.rnnt_workspace_bytes(ref.dims) <= 32 << 20
-
-    f = _noalloc_fn()
-    stream = torch.cuda.current_stream().cuda_stream
+    r = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)  # fresh `saved`; scratch from the library
+    loss = _call_noalloc(f, r, dev, params, inp.wl.B)
+    assert r.status() == (0, 0)
     tl = TOL[dtype][0]
-    for call in range(2):
-        r = rn.Rnnt.for_inputs(inp)   # fresh `saved`; scratch comes from the library
-        loss = torch.full((inp.wl.B,), float("nan"), device="cuda")
-        code = f(ctypes.byref(r.dims), dev["hA"].data_ptr(), dev["hL"].data_ptr(),
-                 ctypes.byref(params), dev["labels"].data_ptr(), dev["T_len"].data_ptr(),
-                 dev["U_len"].data_ptr(), loss.data_ptr(), r.saved.data_ptr(), stream)
-        assert code == 0, rn.rnnt_status_string(code)
-        torch.cuda.synchronize()
-        assert r.status() == (0, 0)
-        got, want = loss.double().cpu().numpy(), ref_loss.double().cpu().numpy()
-        assert np.all(np.abs(got - want) <= tl * np.abs(want)), (call, got, want)
-        state = _saved_state(r)
-        for k, v in ref_state.items():
-            a, b = state[k].cpu().numpy(), v.cpu().numpy()
-            assert np.array_equal(np.isneginf(a), np.isneginf(b)), (call, k)
-            fin = np.isfinite(b)
-            assert np.allclose(a[fin], b[fin], rtol=tl, atol=tl), (call, k)
+    got, want = loss.double().cpu().numpy(), ref_loss.double().cpu().numpy()
+    assert np.all(np.abs(got - want) <= tl * np.abs(want)), (tag, got, want)
+    state = _saved_state(r)
+    for k, v in ref_state.items():
+        a, b = state[k].cpu().numpy(), v.cpu().numpy()
+        assert np.array_equal(np.isneginf(a), np.isneginf(b)), (tag, k)
+        fin = np.isfinite(b)
+        assert np.allclose(a[fin], b[fin], rtol=tl, atol=tl), (tag, k)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(dtype):
+    # Three calls in a row share the library's scratch array, each left with
+    # the previous call's contents: full-ish lengths; then other values with
+    # much shorter lattices (more positions of the same tiles outside every
+    # lattice); then a plan of several chunks (small tile buffers), so that
+    # every chunk reuses tile buffers the previous one wrote.
+    H, V = (128, 256) if dtype == "bf16" else (64, 96)
+    f = _noalloc_fn()
+    cases = [
+        (synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=23,
+                          bias_std=0.1), 0, "first"),
+        (synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=24,
+                          t_frac=0.1, u_frac=0.1, full_first=False, bias_std=0.2), 0,
+         "shorter lengths"),
+        (synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=25,
+                          bias_std=0.1), 3 * 128, "three tiles per chunk"),
+    ]
+    for inp, tile_cells, tag in cases:
+        _check_against_rnnt_fwd(f, inp, tile_cells, tag)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():

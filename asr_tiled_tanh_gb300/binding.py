@@ -103,7 +103,7 @@ def load(build_if_missing: bool = False):
     lib.rnnt_testing_gemm_bf16.restype = ctypes.c_int
     lib.rnnt_testing_gemm_bf16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                            ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
-                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+                                           ctypes.c_int, ctypes.c_int, P]
     lib.rnnt_testing_gemm_timeout.restype = ctypes.c_int
     lib.rnnt_testing_gemm_timeout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
                                               P, ctypes.c_ulonglong, P]

@@ -635,8 +635,13 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_u32(sA + stage * C::A_BYTES);
             const uint32_t b0 = ptx::smem_u32(sB + stage * C::B_BYTES);
+            // a partial last K block (K not a multiple of 64) issues only the
+            // 16-wide steps that hold data; the rest of the stage is the TMA's
+            // zero fill
+            const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
+              if (k >= ksteps) break;
               // K-major: 16 elements = 32 bytes along the swizzled row.
               // MN-major: 16 K rows = two 8-row groups of 1024 bytes.
               const uint64_t ad = A_MN ? ptx::sdesc_sw128(a0 + k * 2048, 64 * 128, 1024)

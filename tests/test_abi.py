@@ -101,3 +101,32 @@ def test_graph_capturable_follows_the_chunking(lib):
     # one tile per chunk: the calls read the tile count back, no capture
     assert rn.rnnt_graph_capturable(rn.make_dims(**kw, mode=rn.RNNT_TILED, tile_cells=128)) == 0
     assert rn.rnnt_graph_capturable(rn.make_dims(**dict(kw, T=0), mode=rn.RNNT_TILED)) == -1
+
+
+def _declared_arity():
+    """Parameter count of every rnnt_* prototype in include/*.h."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b(rnnt_[a-z0-9_]+)\s*\(([^()]*)\)\s*;", src):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_headers(lib):
+    # a ctypes prototype with the wrong number of arguments would pass garbage
+    # to the library (or fail only on a GPU box): every function the binding
+    # declares must take exactly the header's parameters
+    arity = _declared_arity()
+    assert "rnnt_fwd" in arity and arity["rnnt_fwd"] == 12
+    checked = 0
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+        checked += 1
+    assert checked >= len(rn.EXPORTS) - 3

@@ -145,17 +145,21 @@ def test_output_bias_gradient_without_weight_gradient(offset, mode):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_tiled_and_untiled_and_tile_sizes_agree(dtype):
     # Flash RNN-T: tiled and untiled execution compute the same thing.  The
-    # forward is bit-identical across tile sizes and modes; the backward differs
-    # only by fp32 atomic order across tile sizes, and in bf16 untiled mode by
-    # the rounding of the kept scores to bf16.
+    # forward is bit-identical across tile sizes (the same kernels walk the
+    # same tiles); untiled mode's score epilogue also stores the scores and
+    # splits a row's columns over three warps instead of four, so its partial
+    # log-sum-exps combine in another order and its losses agree to fp32
+    # rounding.  The backward differs only by fp32 atomic order across tile
+    # sizes, and in bf16 untiled mode by the rounding of the kept scores to bf16.
     H, V = (64, 64) if dtype == "f32" else (128, 256)
     inp = synthetic.custom(B=4, T=50, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=7,
                            bias_std=0.1)
     orc = run_oracle(inp)
     runs = [run_gpu(inp, tile_cells=tc) for tc in (128, 128 * 3, 128 * 7, 0)]
     untiled = run_gpu(inp, mode="untiled")
-    for r in runs[1:] + [untiled]:
+    for r in runs[1:]:
         np.testing.assert_array_equal(r["loss"], runs[0]["loss"])
+    np.testing.assert_allclose(untiled["loss"], runs[0]["loss"], rtol=1e-6)
     # bf16: dA is rounded to bf16 before the encoder GEMMs, so an fp32 atomic-order
     # difference can flip a rounding there
     tol_tiles = 1e-5 if dtype == "f32" else 1e-3
@@ -181,7 +185,9 @@ def test_untiled_large_vocabularies(V):
     untiled = run_gpu(inp, mode="untiled")
     tiled = run_gpu(inp)
     assert untiled["status"] == (0, 0)
-    np.testing.assert_array_equal(untiled["loss"], tiled["loss"])
+    # (the untiled score epilogue combines its column partials in another
+    # order: equal to fp32 rounding)
+    np.testing.assert_allclose(untiled["loss"], tiled["loss"], rtol=1e-6)
     assert_parity(untiled, orc, inp)
     for k in GRAD_KEYS:
         assert rel_l2(untiled[k], tiled[k]) < 1e-2, k

@@ -20,7 +20,9 @@ RNNT_OK = 0
 STATUS_NAMES = {0: "RNNT_OK", 1: "RNNT_ERR_INVALID_ARG", 2: "RNNT_ERR_UNSUPPORTED_SHAPE",
                 3: "RNNT_ERR_WORKSPACE_TOO_SMALL", 4: "RNNT_ERR_LENGTH_RANGE",
                 5: "RNNT_ERR_LABEL_RANGE", 6: "RNNT_ERR_TIMEOUT", 7: "RNNT_ERR_CUDA"}
-RNNT_F32, RNNT_BF16 = 0, 1
+RNNT_F32, RNNT_BF16, RNNT_BF16_E4M3 = 0, 1, 2
+# Rnnt(dtype=...) names
+DTYPES = {"f32": RNNT_F32, "bf16": RNNT_BF16, "bf16-e4m3": RNNT_BF16_E4M3}
 RNNT_TILED, RNNT_UNTILED = 0, 1
 
 # Every symbol include/rnnt.h declares.
@@ -104,6 +106,8 @@ def load(build_if_missing: bool = False):
     lib.rnnt_testing_gemm_bf16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                            ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, P]
+    lib.rnnt_testing_quantize_wo.restype = ctypes.c_int
+    lib.rnnt_testing_quantize_wo.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
     lib.rnnt_testing_gemm_timeout.restype = ctypes.c_int
     lib.rnnt_testing_gemm_timeout.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
                                               P, ctypes.c_ulonglong, P]
@@ -238,6 +242,14 @@ def rnnt_testing_gemm_bf16(A, a_mn, B, b_mn, C, M, N, K, accumulate=0, k_splits=
            "rnnt_testing_gemm_bf16")
 
 
+def rnnt_testing_quantize_wo(WO, Q, Wdq, nscale, stream=None):
+    """The e4m3 W^O quantization alone (include/rnnt_testing.h)."""
+    V, H = WO.shape
+    _check(load().rnnt_testing_quantize_wo(V, H, _p(WO), _p(Q), _p(Wdq), _p(nscale),
+                                           _stream(stream)),
+           "rnnt_testing_quantize_wo")
+
+
 def rnnt_testing_gemm_timeout(A, B, C, status, M, N, K, wait_ns, stream=None):
     """The GEMM with a stage that is never filled (include/rnnt_testing.h)."""
     _check(load().rnnt_testing_gemm_timeout(M, N, K, _p(A), _p(B), _p(C), _p(status),
@@ -262,8 +274,7 @@ class Rnnt:
 
     def __init__(self, B, T, U1, HA, HL, H, V, blank=0, dtype="bf16", mode="tiled",
                  tile_cells=0, device="cuda"):
-        self.dims = make_dims(B, T, U1, HA, HL, H, V, blank,
-                              RNNT_BF16 if dtype == "bf16" else RNNT_F32,
+        self.dims = make_dims(B, T, U1, HA, HL, H, V, blank, DTYPES[dtype],
                               RNNT_UNTILED if mode == "untiled" else RNNT_TILED, tile_cells)
         sb, wb = rnnt_saved_bytes(self.dims), rnnt_workspace_bytes(self.dims)
         if sb == 0 or wb == 0:
@@ -274,9 +285,14 @@ class Rnnt:
         self.device = device
 
     @classmethod
-    def for_inputs(cls, inp, mode="tiled", tile_cells=0, device="cuda"):
+    def for_inputs(cls, inp, mode="tiled", tile_cells=0, device="cuda", e4m3_scores=False):
+        """Buffers for a batch of `inp`'s shapes; e4m3_scores: bf16 inputs with
+        the score products on e4m3 tensor cores (RNNT_BF16_E4M3)."""
         wl = inp.wl
-        return cls(wl.B, wl.T, wl.U1, wl.HA, wl.HL, wl.H, wl.V, 0, wl.dtype, mode, tile_cells,
+        dtype = "bf16-e4m3" if e4m3_scores else wl.dtype
+        if e4m3_scores and wl.dtype != "bf16":
+            raise ValueError("e4m3 scores take bf16 inputs")
+        return cls(wl.B, wl.T, wl.U1, wl.HA, wl.HL, wl.H, wl.V, 0, dtype, mode, tile_cells,
                    device)
 
     def fwd(self, hA, hL, params, labels, T_len, U_len, loss=None, stream=None):

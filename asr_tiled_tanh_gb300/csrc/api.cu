@@ -39,13 +39,14 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   if (d->B < 0 || d->T < 1 || d->U1 < 1 || d->HA < 1 || d->HL < 1 || d->H < 1 || d->V < 1)
     return false;
   if (d->blank < 0 || d->blank >= d->V) return false;
-  if (d->dtype != RNNT_F32 && d->dtype != RNNT_BF16) return false;
+  if (d->dtype != RNNT_F32 && d->dtype != RNNT_BF16 && d->dtype != RNNT_BF16_E4M3) return false;
   if (d->mode != RNNT_TILED && d->mode != RNNT_UNTILED) return false;
   if (d->tile_cells < 0) return false;
   std::memset(p, 0, sizeof(*p));
   p->B = d->B; p->T = d->T; p->U1 = d->U1; p->HA = d->HA; p->HL = d->HL; p->H = d->H;
   p->V = d->V; p->blank = d->blank; p->dtype = d->dtype; p->mode = d->mode;
-  p->tc = (d->dtype == RNNT_BF16) && tc_path_enabled();
+  p->tc = (d->dtype == RNNT_BF16 || d->dtype == RNNT_BF16_E4M3) && tc_path_enabled();
+  p->f8 = p->tc && d->dtype == RNNT_BF16_E4M3;
   p->max_tiles = (long long)d->B * cdiv(d->T, TT) * cdiv(d->U1, TU);
   if (p->max_tiles > kMaxI32 / TILE) return false;
   if ((long long)d->B * d->T * d->U1 > kMaxI32 * 8LL) return false;
@@ -107,6 +108,12 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
     p->w_dLr16 = put(2 * B * U1 * H);
     p->w_hAm = put(2 * B * T * HA);
     p->w_hLm = put(2 * B * U1 * HL);
+  }
+  if (p->f8) {
+    p->w_z8 = put(rows * H);              // e4m3(2^8 z) rows of a chunk
+    p->w_wo8 = put(V * H);                // W^O in e4m3, per 256-row block scales
+    p->w_wodq = put(2 * V * H);           // the dequantized W^O_q, bf16
+    p->w_nscale = put(4 * ((V + 255) / 256));
   }
   p->w_len = put(8 * (B ? B : 1));  // effective lengths of accepted samples (2 x int32 [B])
   p->w_total = o;
@@ -336,8 +343,14 @@ rnnt_status rnnt::fwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
   void* Z = untiled ? (char*)saved + p.s_z : w + p.w_z;
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
   if (p.tc) {
+    TcF8 f8{};
+    if (p.f8) {
+      f8 = TcF8{(unsigned char*)(w + p.w_z8), w + p.w_wo8, w + p.w_wodq, (float*)(w + p.w_nscale)};
+      LAUNCH("tc_quantize_wo", tc_quantize_wo(p, pr->WO, w + p.w_wo8, w + p.w_wodq,
+                                              (float*)(w + p.w_nscale), st));
+    }
     s = tc_forward_tiles(p, sv, pr, labels, T_len, U_len, pA, pL, Z, untiled ? Hs : nullptr,
-                         st);
+                         p.f8 ? &f8 : nullptr, st);
     if (s != RNNT_OK) return s;
   } else {
     long long nch = 0;
@@ -442,6 +455,12 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
   void* Hs = untiled ? (char*)saved + p.s_h : w + p.w_h;
 
   if (p.tc) {
+    TcF8 f8{};
+    if (p.f8) {
+      f8 = TcF8{(unsigned char*)(w + p.w_z8), w + p.w_wo8, w + p.w_wodq, (float*)(w + p.w_nscale)};
+      LAUNCH("tc_quantize_wo", tc_quantize_wo(p, pr->WO, w + p.w_wo8, w + p.w_wodq,
+                                              (float*)(w + p.w_nscale), st));
+    }
     // (the preparation runs beside the first chunk's z rebuild, the
     // encoder-side gradients beside the last chunk's dW^O)
     const PreLaunch pre = prepare;
@@ -450,8 +469,8 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
                               es);
     };
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          z_resident, dA, dLr, dWO, dbO, (float4*)(w + p.w_post), &pre, &enc,
-                          st);
+                          z_resident, dA, dLr, dWO, dbO, (float4*)(w + p.w_post),
+                          p.f8 ? &f8 : nullptr, &pre, &enc, st);
     return s;
   }
 

@@ -47,6 +47,7 @@ __host__ __device__ constexpr int status_bit(int code) { return 1 << code; }
 struct Plan {
   int B, T, U1, HA, HL, H, V, blank, dtype, mode;
   bool tc;                  // bf16 tensor-core path (else fp32 SIMT path)
+  bool f8;                  // the score GEMMs on e4m3 operands (dtype RNNT_BF16_E4M3)
   long long max_tiles;      // tiles when every sample has full lengths
   long long chunk_tiles;    // tiles whose intermediates are held at once
   long long chunk_rows;     // = chunk_tiles * TILE
@@ -55,8 +56,8 @@ struct Plan {
   size_t s_status, s_prefix, s_tiles, s_lnP, s_lpb, s_lpl, s_lnPD, s_alpha, s_beta, s_pA, s_pL, s_z, s_h,
       s_total;
   // workspace layout
-  size_t w_dA, w_dLr, w_z, w_h, w_dz, w_post, w_dA16, w_dLr16, w_hAm, w_hLm, w_len,
-      w_total;
+  size_t w_dA, w_dLr, w_z, w_h, w_dz, w_post, w_dA16, w_dLr16, w_hAm, w_hLm, w_z8, w_wo8,
+      w_wodq, w_nscale, w_len, w_total;
 };
 
 // Header words at saved + s_status.

@@ -72,6 +72,7 @@ struct TcParams {
   const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
   ChunkArgs ch;          // lattice epilogues: chunk, lengths, labels, saved arrays
   const float* grad_loss;
+  const float* nscale;   // e4m3 score GEMMs: dequantization scale per N tile (NULL: 1)
   __nv_bfloat16* Hout;   // LSE: kept scores (untiled) [rows][N]; DH: dh [rows][N]
   const __nv_bfloat16* Zin;  // DA: z [rows][N]
   float* dA;
@@ -288,14 +289,17 @@ __device__ __forceinline__ void lse_init(LseState& st, const TcParams& p, const 
 }
 
 // 32 scores v[] (accumulator values, bias not yet added) of columns col0.. .
-// On return v holds the scores (columns past V: -inf) of a lattice row.
+// sc: the accumulator's dequantization scale (1 for bf16 operands; the same
+// instruction count as a plain add).  On return v holds the scores (columns
+// past V: -inf) of a lattice row.
 __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const RowCell& rc,
-                                          float* v, const float* bb, int col0) {
+                                          float* v, const float* bb, int col0, float sc) {
   if (!rc.valid) return;
   const int nv = min(32, p.N - col0);
+  const float2 s2 = make_float2(sc, sc);
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const float2 x = __fadd2_rn(make_float2(v[j], v[j + 1]), make_float2(bb[j], bb[j + 1]));
+    const float2 x = __ffma2_rn(make_float2(v[j], v[j + 1]), s2, make_float2(bb[j], bb[j + 1]));
     v[j] = x.x;
     v[j + 1] = x.y;
   }
@@ -397,14 +401,16 @@ __device__ __forceinline__ void store_box_bf16(const float (&d)[32], unsigned ch
 __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, const RowCell& rc,
                                          float (&d)[32], const uint4 (&bq)[4], int col0,
                                          long long wrow0, unsigned char* stg,
-                                         const CUtensorMap* tmC, bool write) {
+                                         const CUtensorMap* tmC, bool write, float sc) {
   // d holds the chunk's scores on entry and dh on exit
   const int nv = min(32, p.N - col0);
   if (rc.valid) {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
     // (pairs of columns through the packed fp32 add / fma)
+    // (sc: the accumulator's dequantization scale, 1 for bf16 operands)
     const float2 l2 = make_float2(kLog2e, kLog2e), g2 = make_float2(st.lgn, st.lgn);
+    const float2 s2 = make_float2(sc, sc);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t w[4] = {bq[i].x, bq[i].y, bq[i].z, bq[i].w};
@@ -412,7 +418,7 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
       for (int k = 0; k < 4; ++k) {
         float& d0 = d[8 * i + 2 * k];
         float& d1 = d[8 * i + 2 * k + 1];
-        const float2 x = __fadd2_rn(make_float2(d0, d1),
+        const float2 x = __ffma2_rn(make_float2(d0, d1), s2,
                                     make_float2(ptx::bf16lo(w[k]), ptx::bf16hi(w[k])));
         const float2 y = __ffma2_rn(x, l2, g2);
         d0 = ptx::ex2(y.x);
@@ -474,11 +480,19 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   }
 }
 
-template <int BN, int A_MN, int B_MN, int EPI>
+// F8: A and B are e4m3 (K-major only; tcgen05.mma kind::f8f6f4, 128 elements
+// = 128 bytes of K per stage, 32 per instruction) and each N tile's
+// accumulator is scaled by nscale[n] in the epilogue; otherwise bf16 (kind::f16,
+// 64 elements of K per stage, 16 per instruction).  A stage holds the same
+// bytes either way.
+template <int BN, int A_MN, int B_MN, int EPI, int F8>
 __global__ void __launch_bounds__(Cfg<BN, EPI>::THREADS, 1)
 k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using C = Cfg<BN, EPI>;
+  static_assert(!F8 || (!A_MN && !B_MN), "e4m3 operands are K-major");
+  constexpr int BKE = F8 ? 128 : BK;     // K elements per stage
+  constexpr int KSTEP = F8 ? 32 : 16;    // K elements per instruction
   const int cta = blockIdx.x, n_ctas = gridDim.x;
   const uint64_t wait_ns = p.wait_ns ? p.wait_ns : WAIT_NS;
   constexpr int STAGES = C::STAGES;
@@ -580,13 +594,13 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             unsigned char* a = sA + stage * C::A_BYTES;
             unsigned char* b = sB + stage * C::B_BYTES;
             if (!A_MN) {
-              ptx::tma_load_2d(a, &tmA, &full[stage], kb * BK, w.m * BM);
+              ptx::tma_load_2d(a, &tmA, &full[stage], kb * BKE, w.m * BM);
             } else {
               ptx::tma_load_2d(a, &tmA, &full[stage], w.m * BM, kb * BK);
               ptx::tma_load_2d(a + 64 * 128, &tmA, &full[stage], w.m * BM + 64, kb * BK);
             }
             if (!B_MN) {
-              ptx::tma_load_2d(b, &tmB, &full[stage], kb * BK, n * BN);
+              ptx::tma_load_2d(b, &tmB, &full[stage], kb * BKE, n * BN);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
@@ -610,7 +624,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (ptx::elect_one()) {
-      constexpr uint32_t IDESC = ptx::idesc_bf16(BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC =
+          F8 ? ptx::idesc_e4m3(BM, BN, A_MN, B_MN) : ptx::idesc_bf16(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -635,20 +650,22 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_u32(sA + stage * C::A_BYTES);
             const uint32_t b0 = ptx::smem_u32(sB + stage * C::B_BYTES);
-            // a partial last K block (K not a multiple of 64) issues only the
-            // 16-wide steps that hold data; the rest of the stage is the TMA's
-            // zero fill
-            const int ksteps = min(BK / 16, (p.K - kb * BK + 15) / 16);
+            // a partial last K block (K not a multiple of the stage's K)
+            // issues only the steps that hold data; the rest of the stage is
+            // the TMA's zero fill
+            const int ksteps = min(BKE / KSTEP, (p.K - kb * BKE + KSTEP - 1) / KSTEP);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
+            for (int k = 0; k < BKE / KSTEP; ++k) {
               if (k >= ksteps) break;
-              // K-major: 16 elements = 32 bytes along the swizzled row.
-              // MN-major: 16 K rows = two 8-row groups of 1024 bytes.
+              // K-major: one step = 32 bytes along the swizzled row (16 bf16
+              // or 32 e4m3).  MN-major: 16 K rows = two 8-row groups of 1024 bytes.
               const uint64_t ad = A_MN ? ptx::sdesc_sw128(a0 + k * 2048, 64 * 128, 1024)
                                        : ptx::sdesc_sw128(a0 + k * 32, 16, 1024);
               const uint64_t bd = B_MN ? ptx::sdesc_sw128(b0 + k * 2048, 64 * 128, 1024)
                                        : ptx::sdesc_sw128(b0 + k * 32, 16, 1024);
-              ptx::mma_bf16(d_tmem, ad, bd, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
+              const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
+              if constexpr (F8) ptx::mma_e4m3(d_tmem, ad, bd, IDESC, accum);
+              else ptx::mma_bf16(d_tmem, ad, bd, IDESC, accum);
             }
             ptx::mma_commit(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -715,6 +732,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(sub * 32) << 16);
+        const float sc = (F8 && p.nscale) ? __ldg(p.nscale + n) : 1.f;
         float v[32], vn[DB ? 32 : 1];
         ptx::tmem_ld32(tbase + hf * 32, v);
         // bias values of the current chunk; the next chunk's are loaded early
@@ -768,7 +786,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               }
             }
           } else if constexpr (lse_like(EPI)) {
-            lse_chunk(ls, p, rc, v, bb, col0);
+            lse_chunk(ls, p, rc, v, bb, col0, sc);
             if constexpr (EPI == EPI_LSEK) {
               // the scores as the untiled mode keeps them (rows outside the
               // lattice: 0)
@@ -782,7 +800,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
           } else if constexpr (EPI == EPI_DH) {
             dh_chunk(ds, p, rc, v, bq, col0, (long long)w.m * BM + sub * 32,
-                     (unsigned char*)wscr, &tmC, w.m < p.ch.ntiles);
+                     (unsigned char*)wscr, &tmC, w.m < p.ch.ntiles, sc);
           } else if constexpr (EPI == EPI_DA) {
             // da = dz (1 - z^2) on the thread's own row, then 16-column halves
             // of the warp's 32 x 32 block are transposed through the warp's
@@ -937,9 +955,17 @@ namespace {
 // for all 128 positions of the tile: the tile's 8 pL rows are loaded once into
 // registers, each of its 16 pA rows once per frame, and the stores of a warp
 // cover 256 contiguous bytes of a z row.
+//
+// OUT selects the outputs: bit 0 the bf16 z rows (Z, [rows][H]), bit 1 the
+// e4m3 operand of the e4m3 score GEMMs (Z8, [rows][H] bytes): e4m3(z 2^8),
+// rounded to nearest even (|z| < 1, so 2^8 z stays below the e4m3 maximum
+// of 448; the scale is a power of two, so the GEMM's result is scaled back
+// exactly).
+constexpr float kZ8Scale = 256.f;
+template <int OUT>
 __global__ void __launch_bounds__(256)
 k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restrict__ pL,
-               __nv_bfloat16* __restrict__ Z) {
+               __nv_bfloat16* __restrict__ Z, unsigned char* __restrict__ Z8) {
   ptx::griddep_launch();  // the GEMM that follows may start its set-up
   if (!tile_in_use(c, blockIdx.x)) return;
   const TileRef tr = tile_ref(c, blockIdx.x);
@@ -957,6 +983,7 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
       l[ui] = ui < nu ? __ldg((const float4*)(gL + (size_t)ui * H) + k4)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     __nv_bfloat16* z = Z + (long long)blockIdx.x * TILE * H + 4 * k4;
+    unsigned char* z8 = Z8 + (long long)blockIdx.x * TILE * H + 4 * k4;
 #pragma unroll 2
     for (int ti = 0; ti < TT; ++ti) {
       const bool t_ok = ti < nt;
@@ -964,22 +991,88 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
                             : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int ui = 0; ui < TU; ++ui) {
-        uint2 out = make_uint2(0, 0);
-        if (t_ok && ui < nu) {
-          // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
-          out.x = pack_bf16x2(tanh_approx(a.x + l[ui].x), tanh_approx(a.y + l[ui].y));
-          out.y = pack_bf16x2(tanh_approx(a.z + l[ui].z), tanh_approx(a.w + l[ui].w));
-        }
-        *(uint2*)(z + (long long)(ti * TU + ui) * H) = out;
+        // tanh.approx (relative error ~2^-11) is below the bf16 rounding of z
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t_ok && ui < nu)
+          t = make_float4(tanh_approx(a.x + l[ui].x), tanh_approx(a.y + l[ui].y),
+                          tanh_approx(a.z + l[ui].z), tanh_approx(a.w + l[ui].w));
+        const long long r = (long long)(ti * TU + ui) * H;
+        if (OUT & 1)
+          *(uint2*)(z + r) = make_uint2(pack_bf16x2(t.x, t.y), pack_bf16x2(t.z, t.w));
+        if (OUT & 2)
+          *(uint32_t*)(z8 + r) =
+              (uint32_t)ptx::pack_e4m3x2(t.x * kZ8Scale, t.y * kZ8Scale) |
+              ((uint32_t)ptx::pack_e4m3x2(t.z * kZ8Scale, t.w * kZ8Scale) << 16);
       }
     }
   }
 }
 
+// Z (bf16) and/or Z8 (e4m3) rows of a chunk; a NULL output is not written.
 cudaError_t launch_build_z_bf16(const ChunkArgs& c, const float* pA, const float* pL,
-                                __nv_bfloat16* Z, cudaStream_t s) {
+                                __nv_bfloat16* Z, unsigned char* Z8, cudaStream_t s) {
   const int threads = std::min(256, (int)cdiv(c.sh.H / 4, 32) * 32);
-  k_build_z_bf16<<<(unsigned)c.ntiles, threads, 0, s>>>(c, pA, pL, Z);
+  if (Z && Z8)
+    k_build_z_bf16<3><<<(unsigned)c.ntiles, threads, 0, s>>>(c, pA, pL, Z, Z8);
+  else if (Z8)
+    k_build_z_bf16<2><<<(unsigned)c.ntiles, threads, 0, s>>>(c, pA, pL, Z, Z8);
+  else
+    k_build_z_bf16<1><<<(unsigned)c.ntiles, threads, 0, s>>>(c, pA, pL, Z, Z8);
+  return cudaGetLastError();
+}
+
+// W^O quantized for the e4m3 score GEMMs, one block of 256 rows (the score
+// GEMMs' N tile) per CTA: S = 2^k, the smallest power of two with
+// max|W^O[block]| / S <= 448 (1 for an all-zero block); q = e4m3(W^O / S)
+// (nearest even; W^O / S is exact); the dequantized matrix W^O_q = q S, exact
+// in bf16 (4 significant bits), which the backward's dz GEMM uses so that the
+// forward and the backward differentiate the same output layer; and
+// nscale[block] = S / 2^8, the factor that turns an accumulator of
+// e4m3(2^8 z) . q back into W^O_q z.
+constexpr int kWBlock = 256;
+__global__ void __launch_bounds__(1024)
+k_quantize_wo(const __nv_bfloat16* __restrict__ WO, unsigned char* __restrict__ Q,
+              __nv_bfloat16* __restrict__ Wdq, float* __restrict__ nscale, int V, int H) {
+  __shared__ float red[32];
+  const int v0 = blockIdx.x * kWBlock, v1 = min(V, v0 + kWBlock);
+  const long long e0 = (long long)v0 * H, e1 = (long long)v1 * H;  // elements of the block
+  float amax = 0.f;
+  for (long long i = e0 + 2 * (long long)threadIdx.x; i < e1; i += 2 * blockDim.x) {
+    const uint32_t w = *(const uint32_t*)(WO + i);  // H even: pairs never straddle rows
+    amax = fmaxf(amax, fmaxf(fabsf(ptx::bf16lo(w)), fabsf(ptx::bf16hi(w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) red[0] = m;
+  }
+  __syncthreads();
+  amax = red[0];
+  // amax = f 2^e with f in [0.5, 1); 448 = 0.875 2^9
+  int e = 0;
+  const float f = frexpf(amax, &e);
+  const int k = amax > 0.f ? e - 9 + (f > 0.875f ? 1 : 0) : 0;
+  const float S = ldexpf(1.f, k), invS = ldexpf(1.f, -k);
+  if (threadIdx.x == 0) nscale[blockIdx.x] = S * (1.f / kZ8Scale);
+  for (long long i = e0 + 2 * (long long)threadIdx.x; i < e1; i += 2 * blockDim.x) {
+    const uint32_t w = *(const uint32_t*)(WO + i);
+    const uint16_t q = ptx::pack_e4m3x2(ptx::bf16lo(w) * invS, ptx::bf16hi(w) * invS);
+    *(uint16_t*)(Q + i) = q;
+    const float2 d = ptx::unpack_e4m3x2(q);
+    *(uint32_t*)(Wdq + i) = ptx::pack_bf16x2(d.x * S, d.y * S);
+  }
+}
+
+cudaError_t launch_quantize_wo(const void* WO, void* Q, void* Wdq, float* nscale, int V, int H,
+                               cudaStream_t s) {
+  if (V <= 0 || H <= 0) return cudaSuccess;
+  k_quantize_wo<<<(unsigned)cdiv(V, kWBlock), 1024, 0, s>>>(
+      (const __nv_bfloat16*)WO, (unsigned char*)Q, (__nv_bfloat16*)Wdq, nscale, V, H);
   return cudaGetLastError();
 }
 
@@ -1415,16 +1508,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows][cols] (cols contiguous), box 64 x box_rows,
-// 128-byte swizzle, zero fill outside the matrix.
-bool make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, int box_rows) {
+// Row-major matrix [rows][cols] (cols contiguous) of bf16 (e8 = false; box
+// 64 x box_rows) or of one-byte e4m3 values (e8 = true; box 128 x box_rows):
+// 128 bytes of a row per box line, 128-byte swizzle, zero fill outside the
+// matrix.
+bool make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, int box_rows,
+               bool e8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * (e8 ? 1 : 2)};
+  cuuint32_t box[2] = {e8 ? 128u : 64u, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  CUresult r = fn(m, e8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -1453,15 +1550,18 @@ struct GemmDesc {
   const void* B;
   int b_mn;
   int M, N, K;
+  int e8;  // A and B are e4m3 (one byte per element, K-major), else bf16
 };
 
-template <int BN, int AMN, int BMN, int EPI>
+template <int BN, int AMN, int BMN, int EPI, int F8 = 0>
 cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   using C = Cfg<BN, EPI>;
-  auto kern = k_tc_gemm<BN, AMN, BMN, EPI>;
+  auto kern = k_tc_gemm<BN, AMN, BMN, EPI, F8>;
   CUtensorMap ta, tb;
-  const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64) : make_tmap(&ta, g.A, g.M, g.K, BM);
-  const bool ok_b = BMN ? make_tmap(&tb, g.B, g.K, g.N, 64) : make_tmap(&tb, g.B, g.N, g.K, BN);
+  const bool ok_a = AMN ? make_tmap(&ta, g.A, g.K, g.M, 64)
+                        : make_tmap(&ta, g.A, g.M, g.K, BM, F8 != 0);
+  const bool ok_b = BMN ? make_tmap(&tb, g.B, g.K, g.N, 64)
+                        : make_tmap(&tb, g.B, g.N, g.K, BN, F8 != 0);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   // dh / kept-score epilogues: the store map of the [M][N] tile buffer; the
   // other epilogues never read the third map
@@ -1478,7 +1578,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.m_tiles = (int)cdiv(g.M, BM);
   p.n_tiles = (int)cdiv(g.N, BN);
-  p.kb_total = (int)cdiv(g.K, BK);
+  p.kb_total = (int)cdiv(g.K, F8 ? 128 : BK);
   if (p.k_splits < 1) p.k_splits = 1;
   p.kb_per_split = (int)cdiv(p.kb_total, p.k_splits);
   p.k_splits = (int)cdiv(p.kb_total, p.kb_per_split);
@@ -1510,6 +1610,10 @@ cudaError_t launch_gemm(const GemmDesc& g, const TcParams& p, int bn, cudaStream
   // dz); the store and atomic epilogues take every layout.
   if constexpr (lse_like(EPI) || EPI == EPI_DH) {
     if (g.a_mn || g.b_mn) return cudaErrorInvalidValue;
+    if (g.e8) {  // e4m3 scores: 256-wide N tiles (one W^O scale block each)
+      if (bn != 256) return cudaErrorInvalidValue;
+      return launch_gemm_t<256, 0, 0, EPI, 1>(g, p, s);
+    }
     if (bn == 256) return launch_gemm_t<256, 0, 0, EPI>(g, p, s);
     return launch_gemm_t<128, 0, 0, EPI>(g, p, s);
   } else if constexpr (EPI == EPI_DA) {
@@ -1571,6 +1675,8 @@ bool tc_path_enabled() { return true; }
 
 rnnt_status tc_check_shape(const Plan& p) {
   if (p.H % 8 || p.V % 8 || p.HA % 8 || p.HL % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
+  // e4m3 rows of H bytes: TMA strides are multiples of 16 bytes
+  if (p.f8 && p.H % 16) return RNNT_ERR_UNSUPPORTED_SHAPE;
   if (!encode_fn()) return RNNT_ERR_CUDA;
   return RNNT_OK;
 }
@@ -1619,10 +1725,15 @@ ChunkArgs make_chunk(const Plan& p, const SavedView& sv, long long k, const int3
 
 }  // namespace
 
+cudaError_t tc_quantize_wo(const Plan& p, const void* WO, void* wo8, void* wodq, float* nscale,
+                           cudaStream_t s) {
+  return launch_quantize_wo(WO, wo8, wodq, nscale, p.V, p.H, s);
+}
+
 rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_params* pr,
                              const int32_t* labels, const int32_t* T_len, const int32_t* U_len,
                              const float* pA, const float* pL, void* Zv, void* Hkeep,
-                             cudaStream_t s) {
+                             const TcF8* f8, cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   if (!Z) return RNNT_ERR_INVALID_ARG;
   long long nch = 0;
@@ -1631,12 +1742,22 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
   for (long long k = 0; k < nch; ++k) {
     ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
     {
+      // e4m3 scores: their operand only (and the bf16 z that untiled mode
+      // keeps for the backward)
       ProfScope ps("tc_build_z", s);
-      if (launch_build_z_bf16(c, pA, pL, Z, s) != cudaSuccess) return RNNT_ERR_CUDA;
+      if (launch_build_z_bf16(c, pA, pL, (f8 && !Hkeep) ? nullptr : Z, f8 ? f8->z8 : nullptr,
+                              s) != cudaSuccess)
+        return RNNT_ERR_CUDA;
     }
     ProfScope ps("tc_fwd_tiles", s);
     GemmDesc g{Z, 0, pr->WO, 0, (int)p.chunk_rows, p.V, p.H};
     TcParams tp{};
+    if (f8) {
+      g.A = f8->z8;
+      g.B = f8->wo8;
+      g.e8 = 1;
+      tp.nscale = f8->nscale;
+    }
     tp.row_complete = 1;
     tp.bias = (const __nv_bfloat16*)pr->bO;
     tp.ch = c;
@@ -1655,7 +1776,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
                               const float* grad_loss, const float* pA, const float* pL, void* Zv,
                               void* Hv, bool untiled, bool z_resident, float* dA, float* dLr,
                               float* dWO,
-                              float* dbO, float4* post, const PreLaunch* pre,
+                              float* dbO, float4* post, const TcF8* f8, const PreLaunch* pre,
                               const PreLaunch* after, cudaStream_t s) {
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
@@ -1684,9 +1805,11 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
           k_posteriors<<<(unsigned)c.ntiles, TILE, 0, fork.side(0)>>>(c, grad_loss, post);
           if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
         }
-        if (!(z_resident && nch == 1)) {
+        // (e4m3 scores: the forward kept only the e4m3 rows; both are built)
+        if (!(z_resident && nch == 1) || f8) {
           ProfScope ps("tc_build_z", s);
-          if (launch_build_z_bf16(c, pA, pL, Z, s) != cudaSuccess) return RNNT_ERR_CUDA;
+          if (launch_build_z_bf16(c, pA, pL, Z, f8 ? f8->z8 : nullptr, s) != cudaSuccess)
+            return RNNT_ERR_CUDA;
         }
         if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
       }
@@ -1694,6 +1817,12 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       ProfScope ps("tc_bwd_dh", s);
       GemmDesc g{Z, 0, pr->WO, 0, rows, p.V, p.H};
       TcParams tp{};
+      if (f8) {  // the scores recomputed exactly as the forward formed them
+        g.A = f8->z8;
+        g.B = f8->wo8;
+        g.e8 = 1;
+        tp.nscale = f8->nscale;
+      }
       tp.row_complete = 1;
       tp.bias = (const __nv_bfloat16*)pr->bO;
       tp.ch = c;
@@ -1730,7 +1859,8 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
     }
     {  // dz = dh W^O, da = dz (1 - z^2) reduced into dA and dLr
       ProfScope ps("tc_bwd_dz", s);
-      GemmDesc g{Hs, 0, pr->WO, 1, rows, p.H, p.V};
+      // (e4m3 scores: the dequantized W^O_q the scores were formed with)
+      GemmDesc g{Hs, 0, f8 ? f8->wodq : pr->WO, 1, rows, p.H, p.V};
       TcParams tp{};
       tp.ch = c;
       tp.Zin = Z;
@@ -1888,4 +2018,15 @@ extern "C" rnnt_status rnnt_testing_gemm_bf16(int M, int N, int K, const void* A
   cudaError_t e = accumulate ? launch_gemm<EPI_ATOMIC>(g, tp, bn, s)
                              : launch_gemm<EPI_STORE>(g, tp, bn, s);
   return e == cudaSuccess ? RNNT_OK : RNNT_ERR_CUDA;
+}
+
+// ===========================================================================
+// Test hook (include/rnnt_testing.h): the W^O quantization of the e4m3 scores.
+extern "C" rnnt_status rnnt_testing_quantize_wo(int V, int H, const void* WO, void* Q, void* Wdq,
+                                                float* nscale, void* stream) {
+  using namespace rnnt;
+  if (V <= 0 || H <= 0 || (H & 1) || !WO || !Q || !Wdq || !nscale) return RNNT_ERR_INVALID_ARG;
+  return launch_quantize_wo(WO, Q, Wdq, nscale, V, H, (cudaStream_t)stream) == cudaSuccess
+             ? RNNT_OK
+             : RNNT_ERR_CUDA;
 }

@@ -218,6 +218,8 @@ KERNEL_BYTES_PER_CELL = {"tc_dh_kept": lambda V: 4 * V + 16}
 # accounted per encoder row instead).
 KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 2.0,
                             "tc_bwd_dwo": 2.0}
+# The kernels whose products run on e4m3 operands with --scores e4m3.
+E4M3_KERNELS = ("tc_fwd_tiles", "tc_bwd_dh")
 
 
 def kernel_source_hash() -> str:
@@ -312,7 +314,9 @@ def run_gpu_bench(args):
     inp = synthetic.make(wl, seed=wl.seed + 1000 * rank)
     valid = inp.valid_cells()
     nominal = wl.nominal_cells
-    r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=args.tile_cells, device=dev)
+    e4m3 = args.scores == "e4m3"
+    r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=args.tile_cells, device=dev,
+                           e4m3_scores=e4m3)
     d = {k: getattr(inp, k).to(dev) for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO", "labels",
                                                "T_len", "U_len")}
     params = rn.make_params(d["WA"], d["WL"], d["bZ"], d["WO"], d["bO"])
@@ -451,7 +455,8 @@ def run_gpu_bench(args):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         torch.cuda.reset_peak_memory_stats(dev)
-        r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=peak_tc, device=dev)
+        r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=peak_tc, device=dev,
+                               e4m3_scores=e4m3)
         step()
         torch.cuda.synchronize()
         code, word = r.status()
@@ -469,6 +474,8 @@ def run_gpu_bench(args):
     launches = sum(c for _, c in prof.values())
     # the ncu summaries key their traffic figures by workload (and mode)
     traffic_key = wl.name if args.mode == "tiled" else f"{wl.name}-untiled"
+    if e4m3:
+        traffic_key += "-e4m3"
     top = max(prof.items(), key=lambda kv: kv[1][0]) if prof else ("none", (0.0, 1))
     top_name, (top_ms, top_n) = top
     H, V = wl.H, wl.V
@@ -477,11 +484,15 @@ def run_gpu_bench(args):
         flops_per_launch = KERNEL_FLOPS_PER_CELL_HV[top_name] * H * V * valid \
             / max(1, top_n // args.steps)
         ach = flops_per_launch / (top_ms / top_n / 1e3) / 1e12
-        peak = peak_tf
+        peak, src = peak_tf, f"{peak_src} bf16 {peak_kind}"
+        if e4m3 and top_name in E4M3_KERNELS:
+            # a contraction takes the peak of its own dtype: the measured bf16
+            # figure times the nominal dense e4m3 / bf16 ratio (4.5 / 2.25)
+            peak, src = 2.0 * peak_tf, f"{src} x 2 (nominal dense e4m3/bf16 ratio)"
         roof = {"kernel": top_name, "bound": "tensor", "achieved": round(ach, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "traffic": recorded_traffic(top_name, traffic_key),
-                "peak_source": f"{peak_src} bf16 {peak_kind}",
+                "peak_source": src,
                 "flops_per_launch": flops_per_launch, "launches": top_n,
                 "avg_launch_ms": top_ms / top_n}
     elif top_name in KERNEL_BYTES_PER_CELL:
@@ -504,7 +515,8 @@ def run_gpu_bench(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "dtype": ("bf16+e4m3" if e4m3 else "bf16") if wl.dtype == "bf16" else "f32",
+        "data": "synthetic",
         "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "
                                f"V={wl.V} {wl.dtype}", "B": wl.B, "T": wl.T, "U": wl.U,
                    "H": wl.H, "V": wl.V, "tile_cells": int(r.dims.tile_cells),
@@ -512,6 +524,8 @@ def run_gpu_bench(args):
                    "l2": "flushed (256 MiB write) before each timed step",
                    "execution": "CUDA graph of the step" if graph is not None else "eager",
                    "mode": args.mode,
+                   "scores": ("e4m3 (W^O per 256-row block, power-of-two scales; z as "
+                              "e4m3(2^8 z)); dz, dW^O and the rest bf16" if e4m3 else "bf16"),
                    "api": "rnnt_fwd_bwd" if args.api == "step" else "rnnt_fwd + rnnt_bwd",
                    "parallelism": f"dp{world}",
                    "collective": ("one all-reduce (sum, NCCL) of the parameter gradients per "
@@ -654,6 +668,8 @@ def main():
                     help="launch every step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--api", default="step", choices=["step", "separate"],
                     help="step: one rnnt_fwd_bwd call per step; separate: rnnt_fwd + rnnt_bwd")
+    ap.add_argument("--scores", default="bf16", choices=["bf16", "e4m3"],
+                    help="e4m3: the two score products on e4m3 tensor cores (RNNT_BF16_E4M3)")
     ap.add_argument("--mode", default="tiled", choices=["tiled", "untiled"],
                     help="untiled keeps z and the scores from the forward (no recompute)")
     args = ap.parse_args()

@@ -63,7 +63,7 @@ typedef enum {
   RNNT_ERR_CUDA = 7                /* a CUDA runtime call failed (launch, copy, ...) */
 } rnnt_status;
 
-typedef enum { RNNT_F32 = 0, RNNT_BF16 = 1 } rnnt_dtype;
+typedef enum { RNNT_F32 = 0, RNNT_BF16 = 1, RNNT_BF16_E4M3 = 2 } rnnt_dtype;
 typedef enum { RNNT_TILED = 0, RNNT_UNTILED = 1 } rnnt_mode;
 
 /* Problem description (host struct).
@@ -72,6 +72,19 @@ typedef enum { RNNT_TILED = 0, RNNT_UNTILED = 1 } rnnt_mode;
  *   dtype: element type of hA, hL and every parameter (RNNT_F32 or RNNT_BF16).
  *     RNNT_F32 runs fp32 FFMA kernels end to end; RNNT_BF16 runs the bf16
  *     tensor-core path (tcgen05, fp32 accumulation).
+ *     RNNT_BF16_E4M3: bf16 inputs and parameters as RNNT_BF16, with the
+ *     output layer's score products (the forward scores and the backward's
+ *     recompute, 2 of the 3 H x V products per position) on e4m3 tensor
+ *     cores (tcgen05.mma kind::f8f6f4, fp32 accumulation) - the reduced-
+ *     precision output layer the sample-wise paper names as complementary
+ *     work (§1 Introduction, ref. [11]; §5 Conclusion).  W^O is quantized per
+ *     block of 256 rows: S = the smallest power of two with
+ *     max|W^O[block]| / S <= 448, q = e4m3(W^O / S) rounded to nearest even,
+ *     and the layer computed is W^O_q = q S (exact in bf16) in the forward
+ *     and in every backward product; dWO and dbO are the gradients with
+ *     respect to W^O_q and b^O (the caller applies them to W^O: the
+ *     straight-through reading).  z enters the score products as
+ *     e4m3(2^8 z).  Requires H % 16 == 0.
  *   mode: RNNT_TILED (recompute per tile in the backward; workspace set by
  *     tile_cells) or RNNT_UNTILED (z and the scores are kept in `saved` for
  *     every lattice position; no recompute).

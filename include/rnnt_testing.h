@@ -36,6 +36,14 @@ rnnt_status rnnt_testing_gemm_timeout(int M, int N, int K, const void* A, const 
                                       float* C, int32_t* status, unsigned long long wait_ns,
                                       void* stream);
 
+/* The W^O quantization of the RNNT_BF16_E4M3 dtype on its own: WO bf16
+ * [V,H] (device) -> Q e4m3 bytes [V,H], Wdq = the dequantized W^O_q bf16
+ * [V,H], nscale fp32 [ceil(V/256)] = S / 2^8 per block of 256 rows (S: the
+ * block's power-of-two scale, see rnnt_dims.dtype).  H must be even.
+ * Asynchronous on `stream`. */
+rnnt_status rnnt_testing_quantize_wo(int V, int H, const void* WO, void* Q, void* Wdq,
+                                     float* nscale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

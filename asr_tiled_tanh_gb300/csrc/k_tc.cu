@@ -78,7 +78,7 @@ struct TcParams {
   float* dA;
   float* dLr;
   float* dbO;            // DH: column sums of dh accumulated here (may be NULL)
-  const float4* post;    // DH: per-row records (g pb, g pl, lnPD log2 e, label bits)
+  const float4* post;    // DH: per-row records (see k_posteriors)
   int32_t* status;
   // Lattice GEMMs: which axis runs over the chunk's tiles (TILES_ON_M: M
   // tiles are lattice tiles; TILES_ON_K: K runs over the tiles' rows), so
@@ -344,23 +344,30 @@ __device__ __forceinline__ void lse_finish(const LseState& st, const TcParams& p
 }
 
 // f^W_4 (Eq. 10): dh_v = g ((pb + pl) softmax_v - pb [v = blank] - pl [v = label]).
+// Every column but the blank and the label one is g (pb + pl) softmax_v; those
+// two come finished in the row's record and overwrite their column.
 struct DhState {
-  float gpb, gpl;  // g pb, g pl
   float lgn;       // log2|g (pb + pl)| - lnPD log2(e): |g (pb+pl)| softmax_v = 2^(h_v log2 e + lgn)
-  bool neg;        // g < 0 (the incoming gradient of the row's sample is negative)
-  int lab;
+  float dhb, dhl;  // dh of the blank column and of the label column
+  bool neg;        // g (pb + pl) < 0 (the incoming gradient of the row's sample is negative)
+  int lab;         // label id of the row's label transition, -1 without one
 };
 
 // The row's record, precomputed by k_posteriors (see there for the formulas).
 __device__ __forceinline__ DhState dh_state(const float4 q) {
   DhState st;
-  st.gpb = q.x;
-  st.gpl = q.y;
-  const float gg = q.x + q.y;
-  st.lgn = gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY;
-  st.neg = gg < 0.f;
-  st.lab = __float_as_int(q.w);
+  st.lgn = q.x;
+  st.dhb = q.y;
+  st.dhl = q.z;
+  const uint32_t w = __float_as_uint(q.w);
+  st.lab = (int)(w & 0x7fffffffu) - 1;
+  st.neg = (w >> 31) != 0;
   return st;
+}
+
+// Record of a row outside every lattice: dh = 0 everywhere.
+__device__ __forceinline__ float4 dh_record_none() {
+  return make_float4(-INFINITY, 0.f, 0.f, __uint_as_float(0u));
 }
 
 // A warp's 32 x 32 block d (lane = row) as bf16 into rows wrow0 .. +31,
@@ -370,9 +377,13 @@ __device__ __forceinline__ DhState dh_state(const float4 q) {
 // over all 32 banks).  The store engine clips rows and columns past the
 // matrix.  All lanes take part; the staging area is reused only after the
 // previous store from it has been read out.
+// fb / fl: this lane's row replaces column jb / jl of the block with vb / vl
+// (at most two columns per row; same column: same value).
 __device__ __forceinline__ void store_box_bf16(const float (&d)[32], unsigned char* stg,
                                                const CUtensorMap* tmC, int col0,
-                                               long long wrow0) {
+                                               long long wrow0, bool fb = false, int jb = 0,
+                                               float vb = 0.f, bool fl = false, int jl = 0,
+                                               float vl = 0.f) {
   const int lane = threadIdx.x & 31;
   uint4 q[4];
 #pragma unroll
@@ -382,6 +393,12 @@ __device__ __forceinline__ void store_box_bf16(const float (&d)[32], unsigned ch
   const int sw = (lane >> 1) & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) *(uint4*)(stg + lane * 64 + ((i ^ sw) << 4)) = q[i];
+  if (fb)
+    *(__nv_bfloat16*)(stg + lane * 64 + (((jb >> 3) ^ sw) << 4) + (jb & 7) * 2) =
+        __float2bfloat16_rn(vb);
+  if (fl)
+    *(__nv_bfloat16*)(stg + lane * 64 + (((jl >> 3) ^ sw) << 4) + (jl & 7) * 2) =
+        __float2bfloat16_rn(vl);
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -429,16 +446,6 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
 #pragma unroll
       for (int j = 0; j < 32; ++j) d[j] = -d[j];
     }
-    const int jb = p.ch.sh.blank - col0;   // uniform over the warp
-    if (jb >= 0 && jb < 32) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) d[j] = (j == jb) ? d[j] - st.gpb : d[j];
-    }
-    const int jl = st.lab - col0;
-    if (jl >= 0 && jl < 32) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) d[j] = (j == jl) ? d[j] - st.gpl : d[j];
-    }
     if (nv < 32) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) d[j] = (j < nv) ? d[j] : 0.f;
@@ -449,7 +456,10 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
   }
   const int lane = threadIdx.x & 31;
   if (write && col0 < p.N) {  // (no store box starts past the last column)
-    store_box_bf16(d, stg, tmC, col0, wrow0);
+    // the blank and the label column of the row take their finished values
+    const int jb = p.ch.sh.blank - col0, jl = st.lab - col0;
+    store_box_bf16(d, stg, tmC, col0, wrow0, rc.valid && (unsigned)jb < 32u, jb, st.dhb,
+                   rc.valid && st.lab >= 0 && (unsigned)jl < 32u, jl, st.dhl);
     if (p.dbO) {
       // row 16h + 2q + (e ^ h): its 16-byte piece k/4 sits at (k/4 ^ (q & 3))
       const int k = lane & 15, h = lane >> 4;
@@ -697,7 +707,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     int acc = 0;
     uint32_t acc_phase = 0;
     // dh epilogue: the row's record of the next unit is loaded one unit ahead
-    float4 post_next = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+    float4 post_next = dh_record_none();
     if (EPI == EPI_DH && cta < units) {
       const Unit w0 = unit_of(p, cta, kb_lim, kbps, ns);
       if (w0.m < p.ch.ntiles) post_next = __ldg(p.post + (long long)w0.m * BM + row);
@@ -708,7 +718,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
       if (EPI == EPI_DH && gi + n_ctas < units) {
         const Unit wn = unit_of(p, gi + n_ctas, kb_lim, kbps, ns);
         post_next = (wn.m < p.ch.ntiles) ? __ldg(p.post + (long long)wn.m * BM + row)
-                                         : make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+                                         : dh_record_none();
       }
       if (w.kb1 <= w.kb0) continue;
       const int uidx = gi / n_ctas;   // this CTA's unit counter
@@ -1076,18 +1086,23 @@ cudaError_t launch_quantize_wo(const void* WO, void* Q, void* Wdq, float* nscale
   return cudaGetLastError();
 }
 
-// Per-row records for the dh epilogue (f^W_4, Eq. 10): with the posteriors
+// Per-row records for the dh passes (f^W_4, Eq. 10).  With the posteriors
 // pb = exp(alpha + lpb + beta(t+1,u) - lnP) and pl = exp(alpha + lpl +
 // beta(t,u+1) - lnP) (beta(T_b,U_b) := 0, beta(T_b,u<U_b) := -inf, pl = 0 on
-// row U_b) and g = grad_loss[b], the record of a lattice position is
-// (g pb, g pl, lnPD log2(e), label id as bits); rows outside the lattice get
-// (0, 0, +inf, -1).  One thread per row of the chunk.
+// row U_b), g = grad_loss[b] and G = g (pb + pl), dh_v = G softmax_v on every
+// column but two: the blank column, G exp(lpb) - g pb, and the label column,
+// G exp(lpl) - g pl (both terms when the label is the blank id); softmax at
+// those columns is exp(lpb), exp(lpl) from the forward.  The record of a
+// lattice position is
+//   (log2|G| - lnPD log2(e), dh of the blank column, dh of the label column,
+//    bits: label id + 1 in bits 0-30 (0: no label transition), G < 0 in bit 31);
+// rows outside the lattice get dh_record_none().  One thread per row of the chunk.
 __global__ void __launch_bounds__(128)
 k_posteriors(ChunkArgs c, const float* __restrict__ grad_loss, float4* __restrict__ post) {
   if (!tile_in_use(c, blockIdx.x)) return;
   const TileRef tr = tile_ref(c, blockIdx.x);
   const RowCell rc = row_of(tr, threadIdx.x);
-  float4 rec = make_float4(0.f, 0.f, INFINITY, __int_as_float(-1));
+  float4 rec = dh_record_none();
   if (rc.valid) {
     const SavedView& sv = c.sv;
     const int U1 = c.sh.U1;
@@ -1097,11 +1112,21 @@ k_posteriors(ChunkArgs c, const float* __restrict__ grad_loss, float4* __restric
     float bn;
     if (rc.t + 1 < rc.Tb) bn = sv.beta[cell + U1];
     else bn = (rc.u == rc.Ub) ? 0.f : -INFINITY;
-    const float pb = __expf(a + sv.lpb[cell] + bn - lnP);
-    const float pl = (rc.u < rc.Ub) ? __expf(a + sv.lpl[cell] + sv.beta[cell + 1] - lnP) : 0.f;
+    const float lpb = sv.lpb[cell];
+    const bool has_lab = rc.u < rc.Ub;
+    const float lpl = has_lab ? sv.lpl[cell] : -INFINITY;
+    const float pb = __expf(a + lpb + bn - lnP);
+    const float pl = has_lab ? __expf(a + lpl + sv.beta[cell + 1] - lnP) : 0.f;
     const float g = grad_loss ? grad_loss[rc.b] : 1.f;
-    const int lab = (rc.u < rc.Ub) ? c.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
-    rec = make_float4(g * pb, g * pl, sv.lnPD[cell] * kLog2e, __int_as_float(lab));
+    const int lab = has_lab ? c.labels[(size_t)rc.b * U1 + rc.u + 1] : -1;
+    const float G = g * (pb + pl);
+    const float lgn = G != 0.f ? log2f(fabsf(G)) - sv.lnPD[cell] * kLog2e : -INFINITY;
+    float dhb = G * __expf(lpb) - g * pb;
+    const float dhl = has_lab ? G * __expf(lpl) - g * pl - (lab == c.sh.blank ? g * pb : 0.f)
+                              : 0.f;
+    if (has_lab && lab == c.sh.blank) dhb = dhl;
+    const uint32_t bits = (uint32_t)(lab + 1) | (G < 0.f ? 0x80000000u : 0u);
+    rec = make_float4(lgn, dhb, dhl, __uint_as_float(bits));
   }
   post[(long long)blockIdx.x * TILE + threadIdx.x] = rec;
 }
@@ -1132,12 +1157,10 @@ k_dh_kept_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float4* __rest
                      make_float2(0.f, 0.f)};
 #pragma unroll 4
     for (int r = s0; r < TILE; r += S) {
-      const float4 q = __ldg(rec + r);  // (g pb, g pl, lnPD log2(e), label)
+      const DhState st = dh_state(__ldg(rec + r));
       uint4* hp = (uint4*)(tile + (long long)r * V + v0);
       const uint4 x = *hp;
-      const float gg = q.x + q.y;
-      const float lgn = gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY;
-      const float2 g2 = make_float2(lgn, lgn);
+      const float2 g2 = make_float2(st.lgn, st.lgn);
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
       float d[8];
 #pragma unroll
@@ -1146,19 +1169,20 @@ k_dh_kept_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs, const float4* __rest
         d[2 * k] = ptx::ex2(y.x);
         d[2 * k + 1] = ptx::ex2(y.y);
       }
-      if (gg < 0.f) {
+      if (st.neg) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) d[j] = -d[j];
       }
-      // the blank and label terms touch at most two pieces of a row
-      const int jb = blank - v0, jl = __float_as_int(q.w) - v0;
+      // the blank and label columns take their finished values (at most two
+      // pieces of a row hold them)
+      const int jb = blank - v0, jl = st.lab - v0;
       if ((unsigned)jb < 8u) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? d[j] - q.x : d[j];
+        for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? st.dhb : d[j];
       }
-      if ((unsigned)jl < 8u) {
+      if (st.lab >= 0 && (unsigned)jl < 8u) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? d[j] - q.y : d[j];
+        for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? st.dhl : d[j];
       }
       const uint4 o = pack8_bf16(d);
       *hp = o;
@@ -1197,7 +1221,7 @@ k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
                       int R, int stage_bytes) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ uint64_t full[DHK_STAGES];
-  __shared__ float4 rinfo[TILE];  // (g pb, g pl, log2|g (pb+pl)| - lnPD log2(e), label)
+  __shared__ float4 rinfo[TILE];  // the rows' records (see k_posteriors)
   const long long have = (long long)*c.sv.total_tiles - c.first_tile;
   if ((long long)blockIdx.x >= have) return;
   const int V = c.sh.V, V8 = V / 8, blank = c.sh.blank;
@@ -1218,12 +1242,8 @@ k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
                      &full[issued]);
     }
   }
-  if (threadIdx.x < TILE) {
-    const float4 q = __ldg(post + (long long)blockIdx.x * TILE + threadIdx.x);
-    const float gg = q.x + q.y;
-    rinfo[threadIdx.x] =
-        make_float4(q.x, q.y, gg != 0.f ? ptx::lg2(fabsf(gg)) - q.z : -INFINITY, q.w);
-  }
+  if (threadIdx.x < TILE)
+    rinfo[threadIdx.x] = __ldg(post + (long long)blockIdx.x * TILE + threadIdx.x);
   __syncthreads();
   const int S = blockDim.x / groups, s0 = threadIdx.x / groups, k0 = threadIdx.x % groups;
   const float2 l2 = make_float2(kLog2e, kLog2e);
@@ -1240,10 +1260,10 @@ k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
     if (got) {
       unsigned char* buf = dsm + st * stage_bytes;
       for (int r = s0; r < R; r += S) {
-        const float4 ri = rinfo[i * R + r];
-        const float2 g2 = make_float2(ri.z, ri.z);
-        const bool neg = ri.x + ri.y < 0.f;
-        const int lab = __float_as_int(ri.w);
+        const DhState st = dh_state(rinfo[i * R + r]);
+        const float2 g2 = make_float2(st.lgn, st.lgn);
+        const bool neg = st.neg;
+        const int lab = st.lab;
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
           const int k8 = k0 + gi * groups;
@@ -1263,15 +1283,16 @@ k_dh_kept_stream_bf16(ChunkArgs c, __nv_bfloat16* __restrict__ Hs,
 #pragma unroll
               for (int j = 0; j < 8; ++j) d[j] = -d[j];
             }
-            // the blank and label terms touch at most two pieces of a row
+            // the blank and label columns take their finished values (at
+            // most two pieces of a row hold them)
             const int jb = blank - 8 * k8, jl = lab - 8 * k8;
             if ((unsigned)jb < 8u) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? d[j] - ri.x : d[j];
+              for (int j = 0; j < 8; ++j) d[j] = (j == jb) ? st.dhb : d[j];
             }
-            if ((unsigned)jl < 8u) {
+            if (lab >= 0 && (unsigned)jl < 8u) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? d[j] - ri.y : d[j];
+              for (int j = 0; j < 8; ++j) d[j] = (j == jl) ? st.dhl : d[j];
             }
             const uint4 o = pack8_bf16(d);
             *pp = o;

@@ -294,7 +294,8 @@ __device__ __forceinline__ void lse_init(LseState& st, const TcParams& p, const 
 // past V: -inf) of a lattice row.
 __device__ __forceinline__ void lse_chunk(LseState& st, const TcParams& p, const RowCell& rc,
                                           float* v, const float* bb, int col0, float sc) {
-  if (!rc.valid) return;
+  // (rows outside every lattice run through too, on their zero z rows: no
+  // divergent branch; lse_finish writes nothing for them)
   const int nv = min(32, p.N - col0);
   const float2 s2 = make_float2(sc, sc);
 #pragma unroll
@@ -419,9 +420,11 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
                                          float (&d)[32], const uint4 (&bq)[4], int col0,
                                          long long wrow0, unsigned char* stg,
                                          const CUtensorMap* tmC, bool write, float sc) {
-  // d holds the chunk's scores on entry and dh on exit
+  // d holds the chunk's scores on entry and dh on exit.  Rows outside every
+  // lattice need no branch: their z rows are 0 and their record's lgn is
+  // -inf, so every column comes out 0 (and their blank/label values are 0).
   const int nv = min(32, p.N - col0);
-  if (rc.valid) {
+  {
     // g (pb + pl) softmax_v for every column; the blank and label terms are
     // applied only to the (at most two) columns they belong to
     // (pairs of columns through the packed fp32 add / fma)
@@ -442,7 +445,9 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
         d1 = ptx::ex2(y.y);
       }
     }
-    if (st.neg) {  // (uniform over the warp: a tile is one sample)
+    // a tile is one sample: the sign is the same on every row of the warp
+    // that has one (rows outside the lattice are 0 either way)
+    if (__any_sync(0xffffffffu, st.neg)) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) d[j] = -d[j];
     }
@@ -450,16 +455,13 @@ __device__ __forceinline__ void dh_chunk(const DhState& st, const TcParams& p, c
 #pragma unroll
       for (int j = 0; j < 32; ++j) d[j] = (j < nv) ? d[j] : 0.f;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = 0.f;
   }
   const int lane = threadIdx.x & 31;
   if (write && col0 < p.N) {  // (no store box starts past the last column)
     // the blank and the label column of the row take their finished values
     const int jb = p.ch.sh.blank - col0, jl = st.lab - col0;
-    store_box_bf16(d, stg, tmC, col0, wrow0, rc.valid && (unsigned)jb < 32u, jb, st.dhb,
-                   rc.valid && st.lab >= 0 && (unsigned)jl < 32u, jl, st.dhl);
+    store_box_bf16(d, stg, tmC, col0, wrow0, (unsigned)jb < 32u, jb, st.dhb,
+                   st.lab >= 0 && (unsigned)jl < 32u, jl, st.dhl);
     if (p.dbO) {
       // row 16h + 2q + (e ^ h): its 16-byte piece k/4 sits at (k/4 ^ (q & 3))
       const int k = lane & 15, h = lane >> 4;

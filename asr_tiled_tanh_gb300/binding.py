@@ -27,7 +27,9 @@ RNNT_TILED, RNNT_UNTILED = 0, 1
 
 # Every symbol include/rnnt.h declares.
 EXPORTS = ("rnnt_saved_bytes", "rnnt_saved_layout", "rnnt_workspace_bytes",
-           "rnnt_graph_capturable", "rnnt_fwd", "rnnt_bwd", "rnnt_fwd_bwd", "rnnt_device_status",
+           "rnnt_graph_capturable", "rnnt_tile_cells_for_budget", "rnnt_fwd", "rnnt_bwd",
+           "rnnt_bwd_ex", "rnnt_fwd_bwd",
+           "rnnt_device_status",
            "rnnt_status_string", "rnnt_profile_start", "rnnt_profile_stop", "rnnt_profile_entry")
 
 
@@ -46,6 +48,11 @@ class RnntDims(ctypes.Structure):
 
 class RnntParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("WA", "WL", "bZ", "WO", "bO")]
+
+
+class RnntBwdOpts(ctypes.Structure):
+    _fields_ = [("enc_grad_dtype", ctypes.c_int), ("dA", ctypes.c_void_p),
+                ("dL", ctypes.c_void_p)]
 
 
 class RnntSavedOffsets(ctypes.Structure):
@@ -78,6 +85,8 @@ def load(build_if_missing: bool = False):
     lib.rnnt_saved_bytes.argtypes = [D]
     lib.rnnt_workspace_bytes.restype = S
     lib.rnnt_workspace_bytes.argtypes = [D]
+    lib.rnnt_tile_cells_for_budget.restype = ctypes.c_longlong
+    lib.rnnt_tile_cells_for_budget.argtypes = [D, S]
     lib.rnnt_graph_capturable.restype = ctypes.c_int
     lib.rnnt_graph_capturable.argtypes = [D]
     lib.rnnt_saved_layout.restype = ctypes.c_int
@@ -87,6 +96,9 @@ def load(build_if_missing: bool = False):
     lib.rnnt_bwd.restype = ctypes.c_int
     lib.rnnt_bwd.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P,
                              P, P, P, P, P, P, P, P, S, P]
+    lib.rnnt_bwd_ex.restype = ctypes.c_int
+    lib.rnnt_bwd_ex.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P,
+                                P, P, P, P, P, P, P, P, S, ctypes.POINTER(RnntBwdOpts), P]
     lib.rnnt_fwd_bwd.restype = ctypes.c_int
     lib.rnnt_fwd_bwd.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P, P,
                                  P, P, P, P, P, P, P, P, S, P]
@@ -155,6 +167,11 @@ def rnnt_workspace_bytes(dims: RnntDims) -> int:
     return int(load().rnnt_workspace_bytes(ctypes.byref(dims)))
 
 
+def rnnt_tile_cells_for_budget(dims, budget_bytes: int) -> int:
+    """tile_cells whose saved + workspace footprint fits budget_bytes (0: none)."""
+    return int(load().rnnt_tile_cells_for_budget(ctypes.byref(dims), int(budget_bytes)))
+
+
 def rnnt_graph_capturable(dims: RnntDims) -> int:
     """1 if rnnt_fwd / rnnt_bwd for dims make no host synchronization (they
     can be captured into a CUDA graph), 0 if not, -1 for invalid dims."""
@@ -191,6 +208,20 @@ def rnnt_bwd(dims, hA, hL, params: RnntParams, labels, T_len, U_len, grad_loss, 
                            _stream(stream))
     if check:
         _check(code, "rnnt_bwd")
+    return code
+
+
+def rnnt_bwd_ex(dims, hA, hL, params: RnntParams, labels, T_len, U_len, grad_loss, saved, dhA,
+                dhL, dWA, dWL, dbZ, dWO, dbO, ws, opts: RnntBwdOpts, stream=None,
+                check=True) -> int:
+    code = load().rnnt_bwd_ex(ctypes.byref(dims), _p(hA), _p(hL), ctypes.byref(params),
+                              _p(labels), _p(T_len), _p(U_len), _p(grad_loss), _p(saved),
+                              _p(dhA), _p(dhL), _p(dWA), _p(dWL), _p(dbZ), _p(dWO), _p(dbO),
+                              _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+                              ctypes.byref(opts) if opts is not None else None,
+                              _stream(stream))
+    if check:
+        _check(code, "rnnt_bwd_ex")
     return code
 
 
@@ -314,6 +345,27 @@ class Rnnt:
         rnnt_bwd(self.dims, hA, hL, params, labels, T_len, U_len, grad_loss, self.saved,
                  g["dhA"], g["dhL"], g["dWA"], g["dWL"], g["dbZ"], g["dWO"], g["dbO"], self.ws,
                  stream)
+        return g
+
+    def bwd_ex(self, hA, hL, params, labels, T_len, U_len, grad_loss=None, enc_dtype="f32",
+               handoff=False, skip_enc=False, stream=None):
+        """rnnt_bwd_ex: dhA/dhL (and, with handoff, the projections' gradients
+        dA [B,T,H], dL [B,U1,H]) in enc_dtype ("f32" or "bf16"); skip_enc
+        leaves dhA/dhL out (NULL)."""
+        d = self.dims
+        et = torch.bfloat16 if enc_dtype == "bf16" else torch.float32
+        g = self.alloc_grads()
+        g["dhA"] = None if skip_enc else torch.empty(d.B, d.T, d.HA, dtype=et, device=self.device)
+        g["dhL"] = None if skip_enc else torch.empty(d.B, d.U1, d.HL, dtype=et, device=self.device)
+        opts = RnntBwdOpts(RNNT_BF16 if enc_dtype == "bf16" else RNNT_F32, None, None)
+        if handoff:
+            g["dA"] = torch.empty(d.B, d.T, d.H, dtype=et, device=self.device)
+            g["dL"] = torch.empty(d.B, d.U1, d.H, dtype=et, device=self.device)
+            opts.dA, opts.dL = g["dA"].data_ptr(), g["dL"].data_ptr()
+        gl = None if grad_loss is None else torch.as_tensor(grad_loss, dtype=torch.float32,
+                                                             device=self.device)
+        rnnt_bwd_ex(d, hA, hL, params, labels, T_len, U_len, gl, self.saved, g["dhA"], g["dhL"],
+                    g["dWA"], g["dWL"], g["dbZ"], g["dWO"], g["dbO"], self.ws, opts, stream)
         return g
 
     def fwd_bwd(self, hA, hL, params, labels, T_len, U_len, loss=None, grad_loss=None,

@@ -264,6 +264,40 @@ size_t rnnt_workspace_bytes(const rnnt_dims* dims) {
   return make_plan(dims, &p) ? p.w_total : 0;
 }
 
+long long rnnt_tile_cells_for_budget(const rnnt_dims* dims, size_t budget_bytes) {
+  if (!dims || dims->mode != RNNT_TILED) return 0;
+  rnnt_dims d = *dims;
+  Plan p;
+  auto footprint = [&](long long tiles) -> size_t {  // 0: invalid
+    d.tile_cells = tiles * TILE;
+    return make_plan(&d, &p) ? p.s_total + p.w_total : 0;
+  };
+  d.tile_cells = TILE;
+  if (!make_plan(&d, &p)) return 0;
+  const long long max_tiles = p.max_tiles;
+  if (max_tiles < 1) return 0;
+  const size_t one = footprint(1);
+  if (one == 0 || one > budget_bytes) return 0;
+  if (footprint(max_tiles) <= budget_bytes) return max_tiles * TILE;
+  // the footprint grows with the tiles per chunk: largest that fits
+  long long lo = 1, hi = max_tiles;  // fits(lo), !fits(hi)
+  while (hi - lo > 1) {
+    const long long mid = lo + (hi - lo) / 2;
+    const size_t f = footprint(mid);
+    if (f != 0 && f <= budget_bytes) lo = mid;
+    else hi = mid;
+  }
+  // whole waves of SMs when at least one fits
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      sms > 0 && lo >= sms)
+    lo = lo / sms * sms;
+  else
+    cudaGetLastError();  // (no device: no rounding; clear the error state)
+  return lo * TILE;
+}
+
 int rnnt_graph_capturable(const rnnt_dims* dims) {
   Plan p;
   if (!make_plan(dims, &p)) return -1;
@@ -387,6 +421,16 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                         dWL, dbZ, dWO, dbO, ws, ws_bytes, stream, false);
 }
 
+rnnt_status rnnt_bwd_ex(const rnnt_dims* dims, const void* hA, const void* hL,
+                        const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
+                        const int32_t* U_len, const float* grad_loss, void* saved, void* dhA,
+                        void* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
+                        void* ws, size_t ws_bytes, const rnnt_bwd_opts* opts,
+                        rnnt_stream stream) {
+  return rnnt::bwd_impl(dims, hA, hL, pr, labels, T_len, U_len, grad_loss, saved, dhA, dhL, dWA,
+                        dWL, dbZ, dWO, dbO, ws, ws_bytes, stream, false, opts);
+}
+
 rnnt_status rnnt_fwd_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                          const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
                          const int32_t* U_len, float* loss, const float* grad_loss, void* saved,
@@ -407,12 +451,19 @@ rnnt_status rnnt_fwd_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
 rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
                            const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
                            const int32_t* U_len, const float* grad_loss, void* saved,
-                           float* dhA, float* dhL, float* dWA, float* dWL, float* dbZ,
+                           void* dhA, void* dhL, float* dWA, float* dWL, float* dbZ,
                            float* dWO, float* dbO, void* ws, size_t ws_bytes,
-                           rnnt_stream stream, bool z_resident) {
+                           rnnt_stream stream, bool z_resident, const rnnt_bwd_opts* opts) {
   Plan p;
   rnnt_status st0 = check_common(dims, hA, hL, pr, labels, T_len, U_len, saved, ws, ws_bytes, &p);
   if (st0 != RNNT_OK) return st0;
+  EncOut eout{false, nullptr, nullptr};
+  if (opts) {
+    if (opts->enc_grad_dtype != RNNT_F32 && opts->enc_grad_dtype != RNNT_BF16)
+      return RNNT_ERR_INVALID_ARG;
+    eout = EncOut{opts->enc_grad_dtype == RNNT_BF16, opts->dA, opts->dL};
+    if (eout.bf16 && !p.tc) return RNNT_ERR_INVALID_ARG;  // bf16 hand-off: bf16 problems
+  }
   cudaStream_t st = (cudaStream_t)stream;
   SavedView sv = saved_view(p, saved);
   char* w = (char*)ws;
@@ -466,7 +517,7 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
     const PreLaunch pre = prepare;
     const PreLaunch enc = [&](cudaStream_t es) {
       return tc_encoder_grads(p, w, hA, hL, pr, Teff, Ueff, dA, dLr, dhA, dhL, dWA, dWL, dbZ,
-                              es);
+                              eout, es);
     };
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
                           z_resident, dA, dLr, dWO, dbO, (float4*)(w + p.w_post),
@@ -514,7 +565,7 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
     g.M = p.B * p.T; g.N = p.HA; g.K = p.H;
     g.A = dA; g.sam = p.H; g.sak = 1;
     g.Bm = pr->WA; g.sbk = p.HA; g.sbn = 1; g.b_bf16 = bf;
-    g.C = dhA; g.ldc = p.HA; g.alpha = 1.f;
+    g.C = (float*)dhA; g.ldc = p.HA; g.alpha = 1.f;
     LAUNCH("simt_gemm", launch_simt_gemm(g, st));
   }
   if (dWA) {  // dW^A = dA^T hA over the frames of accepted samples
@@ -531,7 +582,7 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
     g.M = p.B * p.U1; g.N = p.HL; g.K = p.H;
     g.A = dLr; g.sam = p.H; g.sak = 1;
     g.Bm = pr->WL; g.sbk = p.HL; g.sbn = 1; g.b_bf16 = bf;
-    g.C = dhL; g.ldc = p.HL; g.alpha = 1.f;
+    g.C = (float*)dhL; g.ldc = p.HL; g.alpha = 1.f;
     LAUNCH("simt_gemm", launch_simt_gemm(g, st));
   }
   if (dWL) {
@@ -544,6 +595,13 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
     LAUNCH("simt_gemm", launch_simt_gemm(g, st));
   }
   if (dbZ) LAUNCH("colsum", launch_colsum(dA, (long long)p.B * p.T, p.H, p.H, dbZ, st));
+  // the projections' gradients handed over (fp32 on this path)
+  if (eout.dA)
+    RNNT_CHECK(cudaMemcpyAsync(eout.dA, dA, sizeof(float) * (size_t)p.B * p.T * p.H,
+                               cudaMemcpyDeviceToDevice, st));
+  if (eout.dL)
+    RNNT_CHECK(cudaMemcpyAsync(eout.dL, dLr, sizeof(float) * (size_t)p.B * p.U1 * p.H,
+                               cudaMemcpyDeviceToDevice, st));
   return RNNT_OK;
 }
 

@@ -68,6 +68,7 @@ struct TcParams {
   int n_split_auto;      // n_split is a maximum: the kernel picks the split from the
                          // batch's tile count (whole waves of row units)
   float* C;              // STORE / ATOMIC output, row-major with ldc
+  __nv_bfloat16* Cb;     // STORE: bf16 output instead of C (row-major with ldc)
   long long ldc;
   const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
   ChunkArgs ch;          // lattice epilogues: chunk, lengths, labels, saved arrays
@@ -775,7 +776,19 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const long long grow = (long long)w.m * BM + row;
             if (grow < p.M && col0 < p.N) {
               float* dst = p.C + grow * p.ldc + col0;
-              if constexpr (EPI == EPI_STORE) {
+              if (EPI == EPI_STORE && p.Cb) {  // bf16 output (nearest even)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += bb[j];
+                __nv_bfloat16* db = p.Cb + grow * p.ldc + col0;
+                if (col0 + 32 <= p.N && (p.ldc & 7) == 0) {
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) *(uint4*)(db + 8 * i) = pack8_bf16(v + 8 * i);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) db[j] = __float2bfloat16_rn(v[j]);
+                }
+              } else if constexpr (EPI == EPI_STORE) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] += bb[j];
                 if (col0 + 32 <= p.N && (p.ldc & 3) == 0) {
@@ -1923,10 +1936,14 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
 
 rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
                              const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,
-                             float* dA, float* dLr, float* dhA, float* dhL, float* dWA,
-                             float* dWL, float* dbZ, cudaStream_t s) {
-  __nv_bfloat16* dA16 = (__nv_bfloat16*)(ws + p.w_dA16);
-  __nv_bfloat16* dLr16 = (__nv_bfloat16*)(ws + p.w_dLr16);
+                             float* dA, float* dLr, void* dhA, void* dhL, float* dWA,
+                             float* dWL, float* dbZ, const EncOut& out, cudaStream_t s) {
+  // the bf16 operands of the encoder GEMMs go straight into the caller's
+  // hand-off buffers when those are bf16
+  __nv_bfloat16* dA16 = (out.bf16 && out.dA) ? (__nv_bfloat16*)out.dA
+                                             : (__nv_bfloat16*)(ws + p.w_dA16);
+  __nv_bfloat16* dLr16 = (out.bf16 && out.dL) ? (__nv_bfloat16*)out.dL
+                                              : (__nv_bfloat16*)(ws + p.w_dLr16);
   __nv_bfloat16* hAm = (__nv_bfloat16*)(ws + p.w_hAm);
   __nv_bfloat16* hLm = (__nv_bfloat16*)(ws + p.w_hLm);
   const size_t nA = (size_t)p.B * p.T * p.H, nL = (size_t)p.B * p.U1 * p.H;
@@ -1949,6 +1966,14 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
           (const __nv_bfloat16*)hL, hLm, p.B, p.U1, p.HL, Ueff);
     }
     if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    // fp32 hand-off: the accumulators themselves
+    if (!out.bf16 && out.dA &&
+        cudaMemcpyAsync(out.dA, dA, nA * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+    if (!out.bf16 && out.dL &&
+        cudaMemcpyAsync(out.dL, dLr, nL * sizeof(float), cudaMemcpyDeviceToDevice,
+                        fork.side(0)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
     if (fork.join() != cudaSuccess) return RNNT_ERR_CUDA;
   }
   ProfScope ps("tc_enc_grads", s);
@@ -1967,7 +1992,8 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
   if (dhA) {  // dh^A = dA W^A: A = dA16 [MA][H], B = W^A [H][HA] (K rows, N contiguous)
     GemmDesc g{dA16, 0, pr->WA, 1, MA, p.HA, p.H};
     TcParams tp{};
-    tp.C = dhA;
+    if (out.bf16) tp.Cb = (__nv_bfloat16*)dhA;
+    else tp.C = (float*)dhA;
     tp.ldc = p.HA;
     if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HA, MA), fork.side(0)) != cudaSuccess)
       return RNNT_ERR_CUDA;
@@ -1975,7 +2001,8 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
   if (dhL) {
     GemmDesc g{dLr16, 0, pr->WL, 1, ML, p.HL, p.H};
     TcParams tp{};
-    tp.C = dhL;
+    if (out.bf16) tp.Cb = (__nv_bfloat16*)dhL;
+    else tp.C = (float*)dhL;
     tp.ldc = p.HL;
     if (launch_gemm<EPI_STORE>(g, tp, pick_bn(p.HL, ML), fork.side(1)) != cudaSuccess)
       return RNNT_ERR_CUDA;

@@ -80,10 +80,12 @@ rnnt_status fwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
 // ---- the backward pass behind rnnt_bwd and rnnt_fwd_bwd (api.cu) -----------
 // z_resident: the workspace still holds the z tiles the forward of the same
 // call built, so that a single-chunk plan does not rebuild them.
+// opts: the encoder-side hand-off of rnnt_bwd_ex (NULL: fp32 dhA, dhL).
 rnnt_status bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL,
                      const rnnt_params* pr, const int32_t* labels, const int32_t* T_len,
-                     const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
-                     float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
-                     void* ws, size_t ws_bytes, rnnt_stream stream, bool z_resident);
+                     const int32_t* U_len, const float* grad_loss, void* saved, void* dhA,
+                     void* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
+                     void* ws, size_t ws_bytes, rnnt_stream stream, bool z_resident,
+                     const rnnt_bwd_opts* opts = nullptr);
 
 }  // namespace rnnt

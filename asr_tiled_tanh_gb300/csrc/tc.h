@@ -48,10 +48,17 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
                               float* dWO,
                               float* dbO, float4* post, const TcF8* f8, const PreLaunch* pre,
                               const PreLaunch* after, cudaStream_t s);
+// How the encoder-side gradients leave (rnnt_bwd_ex): bf16: dhA, dhL (and
+// dA, dL) are bf16, else fp32; dA, dL: the projections' gradients, or NULL.
+struct EncOut {
+  bool bf16;
+  void* dA;
+  void* dL;
+};
 // dh^A, dW^A, dh^L, dW^L, db^Z from dA and dLr.
 rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void* hL,
                              const rnnt_params* pr, const int32_t* Teff, const int32_t* Ueff,
-                             float* dA, float* dLr, float* dhA, float* dhL, float* dWA,
-                             float* dWL, float* dbZ, cudaStream_t s);
+                             float* dA, float* dLr, void* dhA, void* dhL, float* dWA,
+                             float* dWL, float* dbZ, const EncOut& out, cudaStream_t s);
 
 }  // namespace rnnt

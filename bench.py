@@ -315,6 +315,13 @@ def run_gpu_bench(args):
     valid = inp.valid_cells()
     nominal = wl.nominal_cells
     e4m3 = args.scores == "e4m3"
+    if args.budget_gb > 0:  # tile size from a memory budget for the library's buffers
+        bdims = rn.make_dims(wl.B, wl.T, wl.U1, wl.HA, wl.HL, wl.H, wl.V, 0,
+                             rn.RNNT_BF16_E4M3 if e4m3 else rn.binding.DTYPES[wl.dtype],
+                             rn.RNNT_TILED, 0)
+        args.tile_cells = rn.rnnt_tile_cells_for_budget(bdims, int(args.budget_gb * 1e9))
+        if args.tile_cells <= 0:
+            raise SystemExit(f"no tile size fits {args.budget_gb} GB")
     r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=args.tile_cells, device=dev,
                            e4m3_scores=e4m3)
     d = {k: getattr(inp, k).to(dev) for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO", "labels",
@@ -652,6 +659,9 @@ def main():
                     help="synthetic workload (asr_tiled_tanh_gb300/synthetic.py); the default "
                          "is the 40 s, batch-1024 configuration")
     ap.add_argument("--tile-cells", type=int, default=0)
+    ap.add_argument("--budget-gb", type=float, default=0.0,
+                    help="choose tile_cells so that the library's saved + workspace buffers "
+                         "fit this many GB (rnnt_tile_cells_for_budget)")
     ap.add_argument("--peak-tile-cells", type=int, default=-1,
                     help="after the timed steps, peak HBM of one step at this second tile "
                          "size (-1: a quarter of the first plan's tile buffers; 0: skip)")

@@ -144,6 +144,22 @@ rnnt_status rnnt_saved_layout(const rnnt_dims* dims, rnnt_saved_offsets* out);
  * rnnt_fwd to rnnt_bwd) and 256-byte alignment. */
 size_t rnnt_workspace_bytes(const rnnt_dims* dims);
 
+/* Memory-bounded scheduling: the tile_cells for which the library's whole
+ * device footprint, rnnt_saved_bytes + rnnt_workspace_bytes, fits in
+ * budget_bytes (tiled mode; dims->tile_cells is ignored).  The lattice is
+ * walked sample by sample in chunks of tiles (consecutive samples' tiles,
+ * padding-free), so the budget bounds how much of the batch is in flight at
+ * once while the per-position saved state (20 bytes) and the per-frame
+ * vectors stay whole: the Flash RNN-T blog's "Compute it, use it, make room"
+ * tile, and the sample-wise paper's conclusion that memory need barely grow
+ * with the batch, turned into a size the caller asks for.  Returns the
+ * largest multiple of 128 lattice positions that fits, rounded down to whole
+ * waves of the current device's SMs when at least one wave fits, capped at
+ * the whole lattice (one chunk: no host synchronization, see
+ * rnnt_graph_capturable); 0 if not even one tile fits or dims are invalid or
+ * untiled. */
+long long rnnt_tile_cells_for_budget(const rnnt_dims* dims, size_t budget_bytes);
+
 /* Whether rnnt_fwd and rnnt_bwd for dims run entirely as stream work, with
  * no host-side synchronization, so that a caller can capture them into a
  * CUDA graph: true when every possible lattice tile fits one chunk of the
@@ -180,6 +196,40 @@ rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
                      float* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
                      void* ws, size_t ws_bytes, rnnt_stream stream);
+
+/* Options of rnnt_bwd_ex: how the encoder-side gradients are handed over.
+ * All zero / NULL gives exactly rnnt_bwd.
+ *   enc_grad_dtype: element type of the dhA and dhL outputs, RNNT_F32 (as
+ *     rnnt_bwd) or RNNT_BF16 (bf16 [B,T,HA] / [B,U1,HL], round to nearest
+ *     even from the fp32 accumulators; half the bytes for an encoder whose
+ *     backward runs in bf16).  RNNT_BF16 needs a bf16 problem (dims.dtype
+ *     RNNT_BF16 or RNNT_BF16_E4M3).
+ *   dA, dL: optional outputs [B,T,H] and [B,U1,H] of element type
+ *     enc_grad_dtype: the gradients with respect to the joint network's
+ *     projections, dA[b,t] = dL/d(W^A hA[b,t] + b^Z) and
+ *     dL[b,u] = dL/d(W^L hL[b,u]) (the pre-activation gradients summed over
+ *     the other lattice axis; 0 outside a sample's lengths), so that
+ *     dh^A = dA W^A and dh^L = dL W^L.  An encoder can fold these products into
+ *     its own first backward GEMM (function merging across the boundary, as
+ *     the sample-wise paper's §1 Introduction describes for the loss and
+ *     output layer) and pass dhA = dhL = NULL, which skips them here.
+ * Not a step of the pages' method: an interface for the caller's backward. */
+typedef struct {
+  int enc_grad_dtype;
+  void* dA;
+  void* dL;
+} rnnt_bwd_opts;
+
+/* rnnt_bwd with options (opts NULL: rnnt_bwd).  dhA and dhL point to
+ * opts->enc_grad_dtype elements (cast through void*).  Extra errors:
+ * RNNT_ERR_INVALID_ARG for an unknown enc_grad_dtype or RNNT_BF16 on an fp32
+ * problem. */
+rnnt_status rnnt_bwd_ex(const rnnt_dims* dims, const void* hA, const void* hL,
+                        const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
+                        const int32_t* U_len, const float* grad_loss, void* saved, void* dhA,
+                        void* dhL, float* dWA, float* dWL, float* dbZ, float* dWO, float* dbO,
+                        void* ws, size_t ws_bytes, const rnnt_bwd_opts* opts,
+                        rnnt_stream stream);
 
 /* One training step: rnnt_fwd followed by rnnt_bwd on the same buffers, with
  * the arguments of both (loss is written as by rnnt_fwd; grad_loss and the

@@ -165,3 +165,30 @@ def test_untiled_mode_refuses_the_40s_batch():
     code = rn.rnnt_fwd(tiled, None, None, params, None, None, None, None, None, None,
                        check=False)
     assert code == 1  # RNNT_ERR_INVALID_ARG
+
+
+def test_audio40_under_a_memory_budget():
+    # the tile size chosen for a 13 GB budget: the library's whole footprint
+    # (saved + workspace) fits it, the chunks are whole waves of SMs, and the
+    # losses are those of the default plan (the forward is the same per tile)
+    inp = _workload("audio40")
+    budget = 13 * 10 ** 9
+    dims = rn.make_dims(inp.wl.B, inp.wl.T, inp.wl.U1, inp.wl.HA, inp.wl.HL, inp.wl.H, inp.wl.V,
+                        0, rn.RNNT_BF16, rn.RNNT_TILED, 0)
+    tc = rn.rnnt_tile_cells_for_budget(dims, budget)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tc > 0 and (tc // 128) % sms == 0
+    dev = {k: getattr(inp, k).cuda() for k in ("hA", "hL", "WA", "WL", "bZ", "WO", "bO",
+                                                "labels", "T_len", "U_len")}
+    params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
+    args = (dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
+    losses = []
+    for tile_cells in (tc, 0):
+        r = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)
+        if tile_cells == tc:
+            assert r.saved.numel() + r.ws.numel() <= budget
+        losses.append(r.fwd(*args).cpu())
+        torch.cuda.synchronize()
+        assert r.status() == (0, 0)
+        del r
+    assert torch.equal(losses[0], losses[1])

@@ -3,9 +3,12 @@
 //
 // Lattice tiles.  The Flash RNN-T blog ("Compute it, use it, make room")
 // groups lattice positions into tiles and keeps the large intermediates only
-// for the tiles in flight.  Here a tile is a 16 (t) x 8 (u) block of one
+// for the tiles in flight.  Here a tile is a 32 (t) x 4 (u) block of one
 // sample's lattice: 128 positions, one per TMEM lane / epilogue thread in the
-// tensor-core kernels.  Only tiles that intersect a sample's lattice exist
+// tensor-core kernels.  (A sample's lattice is padded to whole tiles; with
+// label lengths of tens of symbols and hundreds of frames, rounding U_b + 1
+// up to 4 and T_b up to 32 wastes fewer positions than 8 and 16: 4.5%
+// against 6.2% of the rows at the 40 s workload's lengths.)  Only tiles that intersect a sample's lattice exist
 // (per-sample padding removal, as in the sample-wise paper's conclusion);
 // positions of an edge tile that fall outside the lattice are masked.
 // Tiles are numbered sample-major, then t-block, then u-block; the exclusive
@@ -20,8 +23,8 @@
 
 namespace rnnt {
 
-constexpr int TT = 16;            // t extent of a tile
-constexpr int TU = 8;             // u extent of a tile
+constexpr int TT = 32;            // t extent of a tile
+constexpr int TU = 4;             // u extent of a tile
 constexpr int TILE = TT * TU;     // lattice positions per tile (= 128 MMA rows)
 constexpr size_t ALIGN = 256;
 

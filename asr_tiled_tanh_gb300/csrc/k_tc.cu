@@ -16,7 +16,7 @@
 //   EPI_DA     dz -> da = dz (1 - z^2), reduced over u into dA[b,t] and over
 //              t into dLr[b,u] (joint-network backward, sample-wise paper §4)
 // Rows of the lattice GEMMs are lattice positions: M tile m of a chunk is the
-// 16 x 8 lattice tile (chunk's first tile + m), one position per TMEM lane.
+// TT x TU lattice tile (chunk's first tile + m), one position per TMEM lane.
 //
 // Roles: warp 0 issues TMA loads into a ring of shared-memory stages, warp 1
 // allocates TMEM and one thread issues tcgen05.mma into one of two TMEM
@@ -71,6 +71,7 @@ struct TcParams {
   __nv_bfloat16* Cb;     // STORE: bf16 output instead of C (row-major with ldc)
   long long ldc;
   const __nv_bfloat16* bias;  // STORE / LSE / DH: bias along N (may be NULL)
+  int sbias;             // LSE / DH: the bias is copied to shared memory (N % 8 == 0)
   ChunkArgs ch;          // lattice epilogues: chunk, lengths, labels, saved arrays
   const float* grad_loss;
   const float* nscale;   // e4m3 score GEMMs: dequantization scale per N tile (NULL: 1)
@@ -198,9 +199,15 @@ __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) {
 }
 
 // 32 bias values of columns col0.. as packed bf16 (0 beyond N or without a
-// bias); widened with unpack32 where they are used.
+// bias); widened with unpack32 where they are used.  sb: the CTA's copy of the
+// bias in shared memory (all lanes read the same 16 bytes: broadcasts), or NULL.
 __device__ __forceinline__ void load_bias_q(const __nv_bfloat16* bias, int N, int col0,
-                                            uint4 (&q)[4]) {
+                                            uint4 (&q)[4], const uint4* sb = nullptr) {
+  if (sb && col0 + 32 <= N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = sb[col0 / 8 + i];
+    return;
+  }
   if (bias && col0 + 32 <= N && (N & 7) == 0) {
     const uint4* src = (const uint4*)(bias + col0);
 #pragma unroll
@@ -524,6 +531,9 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   uint64_t* comb_bar = done_bar + 1;  // [2]: the other parts' LSE partials are in `comb`
   uint32_t* tmem_holder = (uint32_t*)(comb_bar + 2);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+  // score epilogues: the output bias, copied once per CTA behind the barrier
+  // area when the launch provided the room (p.sbias); read as broadcasts
+  uint4* sbias = (uint4*)(smem + C::SMEM - 1024);
 
   const int warp = ptx::warp_id(), lane = ptx::lane_id();
   if (threadIdx.x == 0) {
@@ -543,6 +553,12 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+  }
+  if ((lse_like(EPI) || EPI == EPI_DH) && p.sbias) {
+    // (the bias is a caller input that no kernel of the stream writes: it
+    // may be read before the programmatic-dependency wait)
+    const uint4* src = (const uint4*)p.bias;
+    for (int i = threadIdx.x; i < p.N / 8; i += blockDim.x) sbias[i] = __ldg(src + i);
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -751,7 +767,8 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         // bias values of the current chunk; the next chunk's are loaded early
         constexpr bool USE_BIAS = (EPI == EPI_STORE || lse_like(EPI) || EPI == EPI_DH);
         uint4 bq[4];
-        if (USE_BIAS) load_bias_q(p.bias, p.N, n * BN + hf * 32, bq);
+        const uint4* sb = (EPI != EPI_STORE && p.sbias) ? sbias : nullptr;
+        if (USE_BIAS) load_bias_q(p.bias, p.N, n * BN + hf * 32, bq, sb);
         // dz epilogue: z rows of the current chunk, loaded one chunk ahead
         const bool z_vec = (EPI == EPI_DA) && tr.exists && (p.N & 7) == 0;
         const __nv_bfloat16* zrow = p.Zin + ((long long)w.m * BM + sub * 32) * p.N;
@@ -768,7 +785,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
           }
           const int col0 = n * BN + c * 32;
           uint4 bqn[4];
-          if (DB && USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn);
+          if (DB && USE_BIAS && more) load_bias_q(p.bias, p.N, col0 + 64, bqn, sb);
 
           float bb[32];
           if (USE_BIAS && EPI != EPI_DH) unpack32(bq, bb);
@@ -856,17 +873,21 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               }
             }
             const int cc = lane & 15, h = lane >> 4;
-            const int tw = tr.t0 + sub * 4;   // rows r of this warp: t = tw + r/8, u = u0 + r%8
+            // rows r of this warp: t = tw + r / TU, u = u0 + r % TU; a 16-row
+            // half holds FQ frames of TU label positions
+            constexpr int FQ = 16 / TU;
+            static_assert(16 % TU == 0 && TU % 2 == 0, "tile shape");
+            const int tw = tr.t0 + sub * (32 / TU);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) wscr[lane * 17 + j] = v[half * 16 + j];
               __syncwarp();
               // this lane: column col0 + half*16 + cc, rows h*16 .. h*16+15
-              // (t = tw + 2h and tw + 2h + 1, u = u0 .. u0+7)
-              float sum_u[TU], st[2];
+              // (t = tw + FQ h .. tw + FQ h + FQ-1, u = u0 .. u0+TU-1)
+              float sum_u[TU], st[FQ];
 #pragma unroll
-              for (int q = 0; q < 2; ++q) {
+              for (int q = 0; q < FQ; ++q) {
                 st[q] = 0.f;
 #pragma unroll
                 for (int k = 0; k < TU; ++k) {
@@ -880,12 +901,12 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               const int col = col0 + half * 16 + cc;
               if (col < p.N && tr.exists && tw < tr.Tb) {
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const int t = tw + 2 * h + q;
+                for (int q = 0; q < FQ; ++q) {
+                  const int t = tw + FQ * h + q;
                   if (t < tr.Tb)
                     ptx::red_add_f32(p.dA + ((size_t)tr.b * p.ch.sh.T + t) * p.N + col, st[q]);
                 }
-                // the two row halves split the 8 label positions: h=0 -> u0..u0+3
+                // the two row halves split the TU label positions: h=0 takes the first half
 #pragma unroll
                 for (int k = 0; k < TU / 2; ++k) {
                   const int kk = h * (TU / 2) + k;
@@ -910,7 +931,7 @@ k_tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
               }
             } else {
               ptx::tmem_ld32(tbase + (c + PARTS) * 32, v);
-              if (USE_BIAS) load_bias_q(p.bias, p.N, col0 + 32 * PARTS, bq);
+              if (USE_BIAS) load_bias_q(p.bias, p.N, col0 + 32 * PARTS, bq, sb);
               ptx::tmem_ld_wait();
               ptx::reg_fence32(v);
             }
@@ -977,8 +998,8 @@ namespace {
 // z rows of a chunk in bf16: tanh(pA[b,t] + pL[b,u]) (joint network, Eq. 3-4),
 // 0 on rows outside the lattice.  One block per tile; a thread owns 4
 // consecutive h (a column group, strided by the block size) and writes them
-// for all 128 positions of the tile: the tile's 8 pL rows are loaded once into
-// registers, each of its 16 pA rows once per frame, and the stores of a warp
+// for all 128 positions of the tile: the tile's TU pL rows are loaded once into
+// registers, each of its TT pA rows once per frame, and the stores of a warp
 // cover 256 contiguous bytes of a z row.
 //
 // OUT selects the outputs: bit 0 the bf16 z rows (Z, [rows][H]), bit 1 the
@@ -1606,10 +1627,19 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   static bool opted_in[kDeviceSlots] = {};  // per instantiation and device
   bool& opted = opted_in[device_slot()];
   if (!opted) {
+    // up to the per-block maximum: the score epilogues' bias copy goes behind
+    // the kernel's own layout when it fits
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+                                         SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     opted = true;
+  }
+  int smem_bytes = C::SMEM;
+  p.sbias = 0;
+  if ((lse_like(EPI) || EPI == EPI_DH) && p.bias && g.N % 8 == 0 &&
+      C::SMEM + 2 * g.N <= SMEM_LIMIT) {
+    p.sbias = 1;
+    smem_bytes = C::SMEM + 2 * g.N;
   }
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.m_tiles = (int)cdiv(g.M, BM);
@@ -1632,7 +1662,7 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

@@ -44,7 +44,7 @@ def test_budget_edges():
     # enough for the whole lattice: one chunk, capped at every possible tile
     small = _dims(B=4, T=50, U1=11, HA=64, HL=64, H=64, V=128)
     tc = rn.rnnt_tile_cells_for_budget(small, 1 << 40)
-    assert tc == 4 * 4 * 2 * 128        # B * ceil(T/16) * ceil(U1/8) tiles
+    assert tc == 4 * 2 * 3 * 128        # B * ceil(T/32) * ceil(U1/4) tiles of 32 x 4 tiles
     assert rn.rnnt_graph_capturable(rn.make_dims(4, 50, 11, 64, 64, 64, 128, 0, rn.RNNT_BF16,
                                                  rn.RNNT_TILED, tc)) == 1
     # untiled plans and invalid dims have no tile size

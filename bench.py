@@ -406,6 +406,10 @@ def run_gpu_bench(args):
     peak_bytes = torch.cuda.max_memory_allocated(dev)
     ms_max = reduce_max(ms, dist, dev)
     value = job_value(nominal, world, ms_max)
+    # what the timed steps ran (the peak measurement below builds another plan)
+    timed_tile_cells = int(r.dims.tile_cells)
+    timed_tiles_per_chunk = _tiles_per_chunk(rn, r.dims)
+    execution = "CUDA graph of the step" if graph is not None else "eager"
     # --- the same steps again, eager, with every kernel bracketed by CUDA
     # events on its own stream: per-kernel times, shares and launch counts
     prof_ms, _, _, prof = timed_region(step, profile=True)
@@ -450,7 +454,7 @@ def run_gpu_bench(args):
     # first plan's buffers are freed, a plan with a quarter of its tiles per
     # chunk (whole waves of SMs) runs one step, and both peaks are reported
     # with their tiles per chunk.
-    tiles_first = _tiles_per_chunk(rn, r.dims)
+    tiles_first = timed_tiles_per_chunk
     peak_by_tiles = {str(tiles_first): round(peak_bytes / 1e9, 4)}
     peak_tc = args.peak_tile_cells
     if peak_tc < 0 and args.mode == "tiled":
@@ -526,10 +530,11 @@ def run_gpu_bench(args):
         "data": "synthetic",
         "config": {"workload": f"{wl.name}: B={wl.B} T={wl.T} U={wl.U} HA=HL=H={wl.H} "
                                f"V={wl.V} {wl.dtype}", "B": wl.B, "T": wl.T, "U": wl.U,
-                   "H": wl.H, "V": wl.V, "tile_cells": int(r.dims.tile_cells),
+                   "H": wl.H, "V": wl.V, "tile_cells": timed_tile_cells,
+                   "tiles_per_chunk": timed_tiles_per_chunk,
                    "nominal_cells": nominal, "valid_cells": valid,
                    "l2": "flushed (256 MiB write) before each timed step",
-                   "execution": "CUDA graph of the step" if graph is not None else "eager",
+                   "execution": execution,
                    "mode": args.mode,
                    "scores": ("e4m3 (W^O per 256-row block, power-of-two scales; z as "
                               "e4m3(2^8 z)); dz, dW^O and the rest bf16" if e4m3 else "bf16"),

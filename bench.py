@@ -263,11 +263,13 @@ def recorded_traffic(kernel: str, workload: str):
 def _tiles_per_chunk(rn, dims) -> int:
     """Lattice tiles whose intermediates a plan holds at once, read back from
     the workspace size: each tile of a chunk adds 128 rows of bf16 z and
-    scores and a 16-byte posterior record per row."""
+    scores and a 16-byte posterior record per row (and, with e4m3 scores,
+    the rows' e4m3 z)."""
     import copy
     one = copy.copy(dims)
     one.tile_cells = 128
-    per_tile = 128 * (2 * dims.H + 2 * dims.V + 16)
+    per_tile = 128 * (2 * dims.H + 2 * dims.V + 16 + (dims.H if dims.dtype == rn.RNNT_BF16_E4M3
+                                                        else 0))
     extra = rn.rnnt_workspace_bytes(dims) - rn.rnnt_workspace_bytes(one)
     return 1 + int(round(extra / per_tile))
 

@@ -179,3 +179,19 @@ def test_e4m3_scores_large_vocabulary_shapes():
     print("bigvocab e4m3 loss", lrel, "grads", gerr)
     assert lrel <= E4M3_TOL["loss"], lrel
     assert max(gerr.values()) <= E4M3_TOL["grad"], gerr
+
+
+def test_e4m3_ragged_vocabulary_and_partial_k_block():
+    # V = 1000: the last W^O block holds 232 rows and the last N tile is
+    # ragged; H = HA = HL = 48: one e4m3 K block of 128 bytes of which 48 hold
+    # data (the MMA issues two of its four 32-wide steps)
+    inp = synthetic.custom(B=3, T=29, U=7, HA=48, HL=48, H=48, V=1000, dtype="bf16", seed=56,
+                           t_frac=0.3, u_frac=0.0, bias_std=0.3)
+    g = np.array([0.7, 1.3, -0.4])
+    for mode, tc in (("tiled", 128), ("untiled", 0)):
+        gpu = _run(inp, mode, tc, grad_loss=g)
+        orc = run_oracle(e4m3ref.with_quantized_wo(inp), grad_loss=g)
+        lrel, gerr = _errors(gpu, orc)
+        print("ragged", mode, "loss", lrel, "grads", gerr)
+        assert lrel <= E4M3_TOL["loss"], (mode, lrel)
+        assert max(gerr.values()) <= E4M3_TOL["grad"], (mode, gerr)

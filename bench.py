@@ -28,7 +28,9 @@ whole lattice fits one chunk, so the calls make no host synchronization), the
 timed steps replay a CUDA graph of the step (`config.execution`); `--eager`
 launches them one by one instead.  A second, eager run of the same number of
 steps with every kernel bracketed by CUDA events on its own stream gives the
-per-kernel times (`kernel_shares`, `roofline`) and `gpu_launches`.
+per-kernel times (`kernel_shares`, `roofline`) and `gpu_launches`.  A third
+eager run times rnnt_fwd and rnnt_bwd apart (`ms_by_phase`: medians of the
+forward, the backward and their sum, and the median of the timed steps).
 """
 from __future__ import annotations
 
@@ -400,11 +402,11 @@ def run_gpu_bench(args):
         if dist:
             dist.barrier()
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        return sum(step_ms) / len(step_ms), clk, wall, prof
+        return sum(step_ms) / len(step_ms), clk, wall, prof, step_ms
 
     # --- timed region: device-resident inputs ---------------------------------
     torch.cuda.reset_peak_memory_stats(dev)
-    ms, clk, wall, _ = timed_region(run, profile=False)
+    ms, clk, wall, _, step_ms = timed_region(run, profile=False)
     peak_bytes = torch.cuda.max_memory_allocated(dev)
     ms_max = reduce_max(ms, dist, dev)
     value = job_value(nominal, world, ms_max)
@@ -414,7 +416,29 @@ def run_gpu_bench(args):
     execution = "CUDA graph of the step" if graph is not None else "eager"
     # --- the same steps again, eager, with every kernel bracketed by CUDA
     # events on its own stream: per-kernel times, shares and launch counts
-    prof_ms, _, _, prof = timed_region(step, profile=True)
+    prof_ms, _, _, prof, _ = timed_region(step, profile=True)
+
+    # --- the forward and the backward timed apart (eager, separate calls) ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if args.flush_mb > 0:
+            flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        r.fwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], loss=loss)
+        ev[i][1].record(stream)
+        r.bwd(d["hA"], d["hL"], params, d["labels"], d["T_len"], d["U_len"], grads=grads)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    phases = {"api": "rnnt_fwd then rnnt_bwd, eager, L2 flushed before each step",
+              "fwd_median": round(statistics.median(fwd_ms), 4),
+              "bwd_median": round(statistics.median(bwd_ms), 4),
+              "fwd_bwd_median": round(statistics.median(f + b for f, b in zip(fwd_ms, bwd_ms)), 4),
+              "timed_step_median": round(statistics.median(step_ms), 4)}
 
     # --- e2e: host buffers through the C ABI ----------------------------------
     e2e_ms, h2d, d2h = None, 0, 0
@@ -548,6 +572,11 @@ def run_gpu_bench(args):
         "peak_hbm_gb": round(peak_bytes / 1e9, 4),
         "peak_hbm_gb_by_tiles_per_chunk": peak_by_tiles,
         "bf16_peak_frac_6HV": round(6 * H * V * valid / (ms_max / 1e3) / 1e12 / peak_tf, 4),
+        # executed products: the tiled backward recomputes the scores (8HV per
+        # valid position); the untiled one keeps them (6HV)
+        "bf16_peak_frac_executed": round((8 if args.mode == "tiled" else 6) * H * V * valid
+                                         / (ms_max / 1e3) / 1e12 / peak_tf, 4),
+        "ms_by_phase": phases,
         "e2e": None if e2e_ms is None else {
             "value": round(job_value(nominal, world, e2e_ms), 1), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,

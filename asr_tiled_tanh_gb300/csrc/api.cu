@@ -159,9 +159,10 @@ bool aligned(const void* x) { return ((uintptr_t)x & (ALIGN - 1)) == 0; }
     RNNT_CHECK(expr);                   \
   } while (0)
 
-// Number of chunks to walk.  When every possible tile fits in one chunk no
-// synchronization is needed; otherwise read the actual tile count.
-rnnt_status chunk_count(const Plan& p, const SavedView& sv, cudaStream_t st, long long* n) {
+}  // namespace
+
+rnnt_status rnnt::chunk_count(const Plan& p, const SavedView& sv, cudaStream_t st,
+                              long long* n) {
   const long long bound = cdiv(p.max_tiles, p.chunk_tiles);
   if (bound <= 1) {
     *n = bound;
@@ -174,8 +175,8 @@ rnnt_status chunk_count(const Plan& p, const SavedView& sv, cudaStream_t st, lon
   return RNNT_OK;
 }
 
-ChunkArgs chunk_args(const Plan& p, const SavedView& sv, long long k, const int32_t* labels,
-                     const int32_t* T_len, const int32_t* U_len) {
+ChunkArgs rnnt::chunk_args(const Plan& p, const SavedView& sv, long long k,
+                           const int32_t* labels, const int32_t* T_len, const int32_t* U_len) {
   ChunkArgs c;
   c.sh = shape_of(p);
   c.first_tile = k * p.chunk_tiles;
@@ -186,6 +187,8 @@ ChunkArgs chunk_args(const Plan& p, const SavedView& sv, long long k, const int3
   c.sv = sv;
   return c;
 }
+
+namespace {
 
 // Projections pA = hA W^A^T + b^Z [B*T,H] and pL = hL W^L^T [B*U1,H], fp32.
 rnnt_status projections(const Plan& p, const void* hA, const void* hL, const rnnt_params* pr,

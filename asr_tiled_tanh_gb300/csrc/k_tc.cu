@@ -1759,38 +1759,6 @@ cudaError_t tc_projection(const Plan& p, const void* X, const void* W, const voi
   return launch_gemm<EPI_STORE>(g, tp, pick_bn(p.H, M), s);
 }
 
-namespace {
-
-rnnt_status chunk_total(const Plan& p, const SavedView& sv, cudaStream_t st, long long* n) {
-  const long long bound = cdiv(p.max_tiles, p.chunk_tiles);
-  if (bound <= 1) {
-    *n = bound;
-    return RNNT_OK;
-  }
-  int32_t total = 0;
-  if (cudaMemcpyAsync(&total, sv.total_tiles, sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(st) != cudaSuccess)
-    return RNNT_ERR_CUDA;
-  *n = cdiv(total, p.chunk_tiles);
-  return RNNT_OK;
-}
-
-ChunkArgs make_chunk(const Plan& p, const SavedView& sv, long long k, const int32_t* labels,
-                     const int32_t* T_len, const int32_t* U_len) {
-  ChunkArgs c;
-  c.sh = Shape{p.B, p.T, p.U1, p.H, p.V, p.blank};
-  c.first_tile = k * p.chunk_tiles;
-  c.ntiles = p.chunk_tiles;
-  c.T_len = T_len;
-  c.U_len = U_len;
-  c.labels = labels;
-  c.sv = sv;
-  return c;
-}
-
-}  // namespace
-
 cudaError_t tc_quantize_wo(const Plan& p, const void* WO, void* wo8, void* wodq, float* nscale,
                            cudaStream_t s) {
   return launch_quantize_wo(WO, wo8, wodq, nscale, p.V, p.H, s);
@@ -1803,10 +1771,10 @@ rnnt_status tc_forward_tiles(const Plan& p, const SavedView& sv, const rnnt_para
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   if (!Z) return RNNT_ERR_INVALID_ARG;
   long long nch = 0;
-  rnnt_status st = chunk_total(p, sv, s, &nch);
+  rnnt_status st = chunk_count(p, sv, s, &nch);
   if (st != RNNT_OK) return st;
   for (long long k = 0; k < nch; ++k) {
-    ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
+    ChunkArgs c = chunk_args(p, sv, k, labels, T_len, U_len);
     {
       // e4m3 scores: their operand only (and the bf16 z that untiled mode
       // keeps for the backward)
@@ -1847,7 +1815,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
   __nv_bfloat16* Z = (__nv_bfloat16*)Zv;
   __nv_bfloat16* Hs = (__nv_bfloat16*)Hv;
   long long nch = 0;
-  rnnt_status st = chunk_total(p, sv, s, &nch);
+  rnnt_status st = chunk_count(p, sv, s, &nch);
   if (st != RNNT_OK) return st;
   const int rows = (int)p.chunk_rows;
   if (pre && (untiled || nch == 0)) {
@@ -1856,7 +1824,7 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
   }
   if (nch == 0 && after) return (*after)(s);
   for (long long k = 0; k < nch; ++k) {
-    ChunkArgs c = make_chunk(p, sv, k, labels, T_len, U_len);
+    ChunkArgs c = chunk_args(p, sv, k, labels, T_len, U_len);
     if (!untiled) {
       {
         // the z rebuild, the posterior records and (first chunk) the caller's

@@ -69,6 +69,15 @@ cudaError_t launch_da_reduce(const ChunkArgs& c, const float* dZ, const void* Z,
 cudaError_t launch_colsum(const float* X, long long R, int N, long long ld, float* out,
                           cudaStream_t s);
 
+// ---- chunk walk (api.cu) ----------------------------------------------------
+// Number of chunks of tiles a pass walks: the upper bound when every possible
+// tile fits one chunk (no synchronization); otherwise the actual tile count is
+// read back from the device (one synchronization of st).
+rnnt_status chunk_count(const Plan& p, const SavedView& sv, cudaStream_t st, long long* n);
+// Arguments of chunk k (its first tile and the chunk buffer's tile count).
+ChunkArgs chunk_args(const Plan& p, const SavedView& sv, long long k, const int32_t* labels,
+                     const int32_t* T_len, const int32_t* U_len);
+
 // ---- the forward pass behind rnnt_fwd (api.cu) ----------------------------
 // side_streams: run the independent launches on side streams (false: every
 // launch on `stream`, and no stream is ever created).

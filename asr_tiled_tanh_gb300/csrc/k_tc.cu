@@ -1030,7 +1030,10 @@ k_build_z_bf16(ChunkArgs c, const float* __restrict__ pA, const float* __restric
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     __nv_bfloat16* z = Z + (long long)blockIdx.x * TILE * H + 4 * k4;
     unsigned char* z8 = Z8 + (long long)blockIdx.x * TILE * H + 4 * k4;
-#pragma unroll 2
+    // four frames per pass: their pA loads are in flight together (the kernel
+    // waits on these loads; two per pass left it 30% slower at B=1024, 40 s,
+    // eight gained nothing)
+#pragma unroll 4
     for (int ti = 0; ti < TT; ++ti) {
       const bool t_ok = ti < nt;
       const float4 a = t_ok ? __ldg((const float4*)(gA + (size_t)ti * H) + k4)

@@ -39,9 +39,22 @@ static int grid_for(size_t n, int threads) {
   return g < 1 ? 1 : (int)g;
 }
 
+__global__ void k_fill_f32x4(float4* __restrict__ p, float v, size_t n4) {
+  const float4 q = make_float4(v, v, v, v);
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n4; i += stride) p[i] = q;
+}
+
 cudaError_t launch_fill_f32(float* p, float v, size_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  k_fill_f32<<<grid_for(n, 256), 256, 0, s>>>(p, v, n);
+  if (((uintptr_t)p & 15) != 0) {  // unaligned: one float per store
+    k_fill_f32<<<grid_for(n, 256), 256, 0, s>>>(p, v, n);
+    return cudaGetLastError();
+  }
+  const size_t n4 = n / 4, tail = n % 4;
+  if (n4) k_fill_f32x4<<<grid_for(n4, 256), 256, 0, s>>>((float4*)p, v, n4);
+  if (tail) k_fill_f32<<<1, 32, 0, s>>>(p + 4 * n4, v, tail);
   return cudaGetLastError();
 }
 

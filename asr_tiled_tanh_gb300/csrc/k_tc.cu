@@ -1553,6 +1553,64 @@ int elementwise_grid(size_t n) {
   return (int)std::max<size_t>(1, std::min(g, cap));
 }
 
+// Eight elements per thread step (two 16-byte loads, one 16-byte store).
+__global__ void k_f32_to_bf16_x8(const float4* __restrict__ x, uint4* __restrict__ y,
+                                 size_t n8) {
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n8; i += stride) {
+    const float4 a = __ldg(x + 2 * i), b = __ldg(x + 2 * i + 1);
+    y[i] = make_uint4(ptx::pack_bf16x2(a.x, a.y), ptx::pack_bf16x2(a.z, a.w),
+                      ptx::pack_bf16x2(b.x, b.y), ptx::pack_bf16x2(b.z, b.w));
+  }
+}
+
+// y = bf16(x), n elements (16-byte aligned pointers: eight per step).
+cudaError_t launch_f32_to_bf16(const float* x, __nv_bfloat16* y, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if ((((uintptr_t)x | (uintptr_t)y) & 15) != 0) {
+    k_f32_to_bf16<<<elementwise_grid(n), 256, 0, s>>>(x, y, n);
+    return cudaGetLastError();
+  }
+  const size_t n8 = n / 8, tail = n % 8;
+  if (n8)
+    k_f32_to_bf16_x8<<<elementwise_grid(n8), 256, 0, s>>>((const float4*)x, (uint4*)y, n8);
+  if (tail) k_f32_to_bf16<<<1, 32, 0, s>>>(x + 8 * n8, y + 8 * n8, tail);
+  return cudaGetLastError();
+}
+
+// k_mask_rows_bf16 with rows of N8 16-byte words: a warp per row (one
+// division per row, not per element).
+__global__ void k_mask_rows_bf16_x8(const uint4* __restrict__ x, uint4* __restrict__ y,
+                                    long long rows, int P, int N8,
+                                    const int32_t* __restrict__ len) {
+  const int lane = threadIdx.x & 31;
+  const long long w0 = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = w0; r < rows; r += nw) {
+    const int b = (int)(r / P), q = (int)(r - (long long)b * P);
+    const bool keep = q < __ldg(len + b);
+    const uint4* xs = x + r * N8;
+    uint4* ys = y + r * N8;
+    for (int k = lane; k < N8; k += 32) ys[k] = keep ? __ldg(xs + k) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// y[b,q,:] = x[b,q,:] for q < len[b], else 0 (B x P rows of N bf16).
+cudaError_t launch_mask_rows_bf16(const __nv_bfloat16* x, __nv_bfloat16* y, int B, int P, int N,
+                                  const int32_t* len, cudaStream_t s) {
+  const long long rows = (long long)B * P;
+  if (rows == 0 || N == 0) return cudaSuccess;
+  if ((N & 7) != 0 || (((uintptr_t)x | (uintptr_t)y) & 15) != 0) {
+    k_mask_rows_bf16<<<elementwise_grid((size_t)rows * N), 256, 0, s>>>(x, y, B, P, N, len);
+    return cudaGetLastError();
+  }
+  const int grid = (int)std::max<long long>(
+      1, std::min<long long>((rows + 7) / 8, (long long)num_sms() * 16));
+  k_mask_rows_bf16_x8<<<grid, 256, 0, s>>>((const uint4*)x, (uint4*)y, rows, P, N / 8, len);
+  return cudaGetLastError();
+}
+
 // ---- tensor maps ----------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1954,19 +2012,15 @@ rnnt_status tc_encoder_grads(const Plan& p, char* ws, const void* hA, const void
     ProfScope ps("tc_enc_prep", s);
     ps.set_kernels(2 + (dWA ? 1 : 0) + (dWL ? 1 : 0));
     Fork fork(s, 3);
-    k_f32_to_bf16<<<elementwise_grid(nA), 256, 0, s>>>(dA, dA16, nA);
-    k_f32_to_bf16<<<elementwise_grid(nL), 256, 0, fork.side(0)>>>(dLr, dLr16, nL);
-    if (dWA) {
-      const size_t n = (size_t)p.B * p.T * p.HA;
-      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, fork.side(1)>>>(
-          (const __nv_bfloat16*)hA, hAm, p.B, p.T, p.HA, Teff);
-    }
-    if (dWL) {
-      const size_t n = (size_t)p.B * p.U1 * p.HL;
-      k_mask_rows_bf16<<<elementwise_grid(n), 256, 0, fork.side(2)>>>(
-          (const __nv_bfloat16*)hL, hLm, p.B, p.U1, p.HL, Ueff);
-    }
-    if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
+    if (launch_f32_to_bf16(dA, dA16, nA, s) != cudaSuccess ||
+        launch_f32_to_bf16(dLr, dLr16, nL, fork.side(0)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+    if (dWA && launch_mask_rows_bf16((const __nv_bfloat16*)hA, hAm, p.B, p.T, p.HA, Teff,
+                                     fork.side(1)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
+    if (dWL && launch_mask_rows_bf16((const __nv_bfloat16*)hL, hLm, p.B, p.U1, p.HL, Ueff,
+                                     fork.side(2)) != cudaSuccess)
+      return RNNT_ERR_CUDA;
     // fp32 hand-off: the accumulators themselves
     if (!out.bf16 && out.dA &&
         cudaMemcpyAsync(out.dA, dA, nA * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

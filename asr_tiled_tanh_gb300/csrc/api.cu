@@ -140,6 +140,8 @@ SavedView saved_view(const Plan& p, void* saved) {
 Shape shape_of(const Plan& p) { return Shape{p.B, p.T, p.U1, p.H, p.V, p.blank}; }
 
 bool aligned(const void* x) { return ((uintptr_t)x & (ALIGN - 1)) == 0; }
+// (NULL counts as aligned: optional arrays)
+bool aligned16(const void* x) { return ((uintptr_t)x & 15) == 0; }
 
 #define RNNT_CHECK(expr)                               \
   do {                                                 \
@@ -246,6 +248,11 @@ rnnt_status check_common(const rnnt_dims* dims, const void* hA, const void* hL,
   if (p->U1 > 1024) return RNNT_ERR_UNSUPPORTED_SHAPE;  // one thread per label position
   if (p->T > 65535) return RNNT_ERR_UNSUPPORTED_SHAPE;  // tile table packs T_b in 16 bits
   if (p->tc) {
+    // operands of TMA loads and 16-byte vector loads: an unaligned one would
+    // fault the kernel, so it is refused here, before any launch
+    if (!aligned16(hA) || !aligned16(hL) || !aligned16(pr->WA) || !aligned16(pr->WL) ||
+        !aligned16(pr->WO) || !aligned16(pr->bZ) || !aligned16(pr->bO))
+      return RNNT_ERR_INVALID_ARG;
     rnnt_status s = tc_check_shape(*p);
     if (s != RNNT_OK) return s;
   }
@@ -466,6 +473,13 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
       return RNNT_ERR_INVALID_ARG;
     eout = EncOut{opts->enc_grad_dtype == RNNT_BF16, opts->dA, opts->dL};
     if (eout.bf16 && !p.tc) return RNNT_ERR_INVALID_ARG;  // bf16 hand-off: bf16 problems
+  }
+  // the tensor-core path writes these by 16-byte stores and vector reductions
+  // (and reads a bf16 dA / dL back by TMA)
+  if (p.tc) {
+    const void* outs[7] = {dhA, dhL, dWA, dWL, dWO, eout.dA, eout.dL};
+    for (const void* o : outs)
+      if (!aligned16(o)) return RNNT_ERR_INVALID_ARG;
   }
   cudaStream_t st = (cudaStream_t)stream;
   SavedView sv = saved_view(p, saved);

@@ -175,7 +175,12 @@ int rnnt_graph_capturable(const rnnt_dims* dims);
  * int32, T_len [B], U_len [B] int32.  Outputs: loss [B] fp32 = -ln P(y_b|x_b)
  * (the batch loss of Eq. 9 is their sum), and `saved` (rnnt_saved_bytes,
  * 256-byte aligned) for rnnt_bwd.  ws: rnnt_workspace_bytes bytes.
- * stream: a cudaStream_t (NULL = legacy default stream). */
+ * stream: a cudaStream_t (NULL = legacy default stream).
+ * bf16 problems (RNNT_BF16, RNNT_BF16_E4M3: the tensor-core path, which reads
+ * its operands by TMA and 16-byte vector loads) need hA, hL and every params
+ * array 16-byte aligned; an unaligned one is refused with
+ * RNNT_ERR_INVALID_ARG before anything is launched.  The fp32 path has no
+ * alignment rule beyond the element size. */
 rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
                      const int32_t* U_len, float* loss, void* saved, void* ws, size_t ws_bytes,
@@ -190,7 +195,10 @@ rnnt_status rnnt_fwd(const rnnt_dims* dims, const void* hA, const void* hL,
  * beyond a sample's lengths are written as 0.  Any output pointer may be NULL
  * to skip writing it (the work that feeds other outputs still runs).
  * When the largest lattice the dims allow does not fit in one tile buffer,
- * this call synchronizes `stream` once to read the number of tiles. */
+ * this call synchronizes `stream` once to read the number of tiles.
+ * bf16 problems: as for rnnt_fwd, and dhA, dhL, dWA, dWL, dWO 16-byte aligned
+ * (written by 16-byte stores and vector reductions; dbZ and dbO have no
+ * alignment rule), else RNNT_ERR_INVALID_ARG before anything is launched. */
 rnnt_status rnnt_bwd(const rnnt_dims* dims, const void* hA, const void* hL,
                      const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
                      const int32_t* U_len, const float* grad_loss, void* saved, float* dhA,
@@ -222,8 +230,9 @@ typedef struct {
 
 /* rnnt_bwd with options (opts NULL: rnnt_bwd).  dhA and dhL point to
  * opts->enc_grad_dtype elements (cast through void*).  Extra errors:
- * RNNT_ERR_INVALID_ARG for an unknown enc_grad_dtype or RNNT_BF16 on an fp32
- * problem. */
+ * RNNT_ERR_INVALID_ARG for an unknown enc_grad_dtype, RNNT_BF16 on an fp32
+ * problem, or (bf16 problems) an opts->dA / opts->dL that is not 16-byte
+ * aligned. */
 rnnt_status rnnt_bwd_ex(const rnnt_dims* dims, const void* hA, const void* hL,
                         const rnnt_params* params, const int32_t* labels, const int32_t* T_len,
                         const int32_t* U_len, const float* grad_loss, void* saved, void* dhA,

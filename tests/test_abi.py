@@ -130,3 +130,22 @@ def test_binding_argument_counts_match_the_headers(lib):
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
         checked += 1
     assert checked >= len(rn.EXPORTS) - 3
+
+
+def test_bf16_operands_must_be_16_byte_aligned(lib):
+    # The tensor-core path reads hA, hL and the parameters by TMA and 16-byte
+    # vector loads: a pointer that is bf16- but not 16-byte aligned is refused
+    # on the host, before the driver is touched.  The addresses are fake and
+    # never dereferenced.
+    d = rn.make_dims(2, 32, 9, 64, 64, 64, 64, 0, rn.RNNT_BF16, rn.RNNT_TILED, 0)
+    nws = rn.rnnt_workspace_bytes(d)
+    assert nws > 0
+    base = {"hA": 0x10000, "hL": 0x20000, "WA": 0x30000, "WL": 0x40000, "bZ": 0x50000,
+            "WO": 0x60000, "bO": 0x70000}
+    for name in base:
+        a = dict(base)
+        a[name] += 2
+        params = rn.RnntParams(a["WA"], a["WL"], a["bZ"], a["WO"], a["bO"])
+        code = lib.rnnt_fwd(ctypes.byref(d), a["hA"], a["hL"], ctypes.byref(params), 0x80000,
+                            0x90000, 0xA0000, 0xB0000, 0x100000, 0x200000, nws, None)
+        assert code == 1, name  # RNNT_ERR_INVALID_ARG

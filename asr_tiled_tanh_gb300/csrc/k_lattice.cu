@@ -12,6 +12,8 @@
 // u = lane + 32 j.  The value handed from position u-1 (alpha) or u+1 (beta)
 // moves by warp shuffles.  The log-probabilities of the diagonals ahead are
 // prefetched into a register ring so the front never waits on a global load.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace rnnt {
@@ -636,12 +638,17 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
                               SavedView sv, float* loss, bool fast, cudaStream_t s) {
   if (sh.B == 0) return cudaSuccess;
   if (sh.U1 > 1024) return cudaErrorInvalidValue;
-  // shared-memory ring when it fits in 220 KiB, else the register-prefetch kernel
+  // shared-memory ring when it fits in 220 KiB and the 2B walks it leaves
+  // resident finish in at most two waves; else the register-prefetch kernel
+  // (two warps per sample, every sample resident at once: at B=1024, U=100
+  // the ring allows one walk per SM, 13.5 waves, 4.4 ms against 2.8 ms)
   int R = AB_W;
   while (R < ((int)cdiv(sh.U1, AB_W) + 2) * AB_W) R *= 2;
   const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float) + 2 * 4 * sizeof(float);
   const int nj = (int)cdiv(sh.U1, 32);
-  if (smem <= 220 * 1024 && nj <= 4) {
+  const long long per_sm = std::max<long long>(1, (228LL * 1024) / (long long)(smem + 1024));
+  const bool few_waves = 2LL * sh.B <= 2LL * per_sm * sm_count();
+  if (smem <= 220 * 1024 && nj <= 4 && few_waves) {
     // warps per sample and direction: one label position per lane when the
     // 2B recursions leave most SMs idle, else one warp (several positions each)
     int w = 1;

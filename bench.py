@@ -224,20 +224,30 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
 E4M3_KERNELS = ("tc_fwd_tiles", "tc_bwd_dh")
 
 
-def kernel_source_hash() -> str:
-    """sha1 of every library source (kernels, headers, the host plan and
-    launch code in csrc/) with comments and whitespace removed: the ncu
-    traffic figures are only valid for the code they were captured from, and
-    tile geometry, plan layout and launch parameters change a kernel's DRAM
-    bytes as much as its body does."""
-    import glob
+def kernel_source_hash(root: str = ROOT) -> str:
+    """sha1 of the sources that decide the lattice GEMMs' DRAM traffic, with
+    comments and whitespace removed: k_tc.cu (the tensor-core kernels and their
+    launches), every header it includes, transitively (tile geometry, the
+    workspace layout, the PTX wrappers), and api.cu (the plan: chunk sizes and
+    buffer placement).  The ncu traffic figures are only valid for the code
+    they were captured from; the other translation units (the alpha/beta
+    recursion, the fp32 path, the no-allocation entry point) do not touch the
+    GEMMs."""
     import hashlib
     import re
+    csrc = os.path.join(root, "asr_tiled_tanh_gb300", "csrc")
+    todo = [os.path.join(csrc, "k_tc.cu"), os.path.join(csrc, "api.cu")]
+    seen = []
+    while todo:
+        path = os.path.normpath(todo.pop(0))
+        if path in seen or not os.path.exists(path):
+            continue
+        seen.append(path)
+        with open(path) as fh:
+            for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', fh.read(), flags=re.M):
+                todo.append(os.path.join(os.path.dirname(path), inc))
     h = hashlib.sha1()
-    csrc = os.path.join(ROOT, "asr_tiled_tanh_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
-                   + glob.glob(os.path.join(csrc, "*.h")))
-    for path in files:
+    for path in sorted(seen, key=os.path.basename):
         h.update(os.path.basename(path).encode())
         with open(path) as fh:
             src = fh.read()

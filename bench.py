@@ -224,7 +224,7 @@ KERNEL_FLOPS_PER_CELL_HV = {"tc_fwd_tiles": 2.0, "tc_bwd_dh": 2.0, "tc_bwd_dz": 
 E4M3_KERNELS = ("tc_fwd_tiles", "tc_bwd_dh")
 
 
-def kernel_source_hash(root: str = ROOT) -> str:
+def kernel_source_hash(root: str | None = None) -> str:
     """sha1 of the sources that decide the lattice GEMMs' DRAM traffic, with
     comments and whitespace removed: k_tc.cu (the tensor-core kernels and their
     launches), every header it includes, transitively (tile geometry, the
@@ -235,7 +235,7 @@ def kernel_source_hash(root: str = ROOT) -> str:
     GEMMs."""
     import hashlib
     import re
-    csrc = os.path.join(root, "asr_tiled_tanh_gb300", "csrc")
+    csrc = os.path.join(root or ROOT, "asr_tiled_tanh_gb300", "csrc")
     todo = [os.path.join(csrc, "k_tc.cu"), os.path.join(csrc, "api.cu")]
     seen = []
     while todo:

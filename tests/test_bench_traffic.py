@@ -1,6 +1,7 @@
 """bench.py's DRAM-traffic bookkeeping on the host: a traffic line from an ncu
 summary is reported only for its kernel and workload key and only while the
-kernel sources still hash to the value it was captured from."""
+sources that decide the GEMMs' traffic still hash to the value it was
+captured from."""
 import bench
 
 
@@ -37,4 +38,25 @@ def test_source_hash_ignores_comments_and_whitespace(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     (src / "k_tc.cu").write_text("int f() { return 2; }\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_source_hash_covers_the_gemm_sources_only(tmp_path, monkeypatch):
+    # k_tc.cu, the headers it includes (transitively) and api.cu decide the
+    # GEMMs' traffic; another translation unit does not
+    src = tmp_path / "asr_tiled_tanh_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k_tc.cu").write_text('#include "tc.h"\nint f() { return 1; }\n')
+    (src / "tc.h").write_text('#include "common.cuh"\n')
+    (src / "common.cuh").write_text("constexpr int TT = 32;\n")
+    (src / "api.cu").write_text("int plan() { return 0; }\n")
+    (src / "k_lattice.cu").write_text("int walk() { return 0; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (src / "k_lattice.cu").write_text("int walk() { return 1; }\n")
+    assert bench.kernel_source_hash() == h0
+    (src / "common.cuh").write_text("constexpr int TT = 16;\n")
+    h1 = bench.kernel_source_hash()
+    assert h1 != h0
+    (src / "api.cu").write_text("int plan() { return 1; }\n")
+    assert bench.kernel_source_hash() != h1
 

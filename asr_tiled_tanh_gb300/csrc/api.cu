@@ -45,7 +45,7 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
   std::memset(p, 0, sizeof(*p));
   p->B = d->B; p->T = d->T; p->U1 = d->U1; p->HA = d->HA; p->HL = d->HL; p->H = d->H;
   p->V = d->V; p->blank = d->blank; p->dtype = d->dtype; p->mode = d->mode;
-  p->tc = (d->dtype == RNNT_BF16 || d->dtype == RNNT_BF16_E4M3) && tc_path_enabled();
+  p->tc = d->dtype == RNNT_BF16 || d->dtype == RNNT_BF16_E4M3;  // bf16 inputs: tensor cores
   p->f8 = p->tc && d->dtype == RNNT_BF16_E4M3;
   p->max_tiles = (long long)d->B * cdiv(d->T, TT) * cdiv(d->U1, TU);
   if (p->max_tiles > kMaxI32 / TILE) return false;
@@ -195,7 +195,7 @@ namespace {
 // Projections pA = hA W^A^T + b^Z [B*T,H] and pL = hL W^L^T [B*U1,H], fp32.
 rnnt_status projections(const Plan& p, const void* hA, const void* hL, const rnnt_params* pr,
                         float* pA, float* pL, cudaStream_t st, cudaStream_t st_l) {
-  const int bf = p.dtype == RNNT_BF16;
+  const int bf = p.dtype != RNNT_F32;
   if (p.tc) {
     RNNT_CHECK(tc_projection(p, hA, pr->WA, pr->bZ, p.B * p.T, p.HA, pA, st));
     RNNT_CHECK(tc_projection(p, hL, pr->WL, nullptr, p.B * p.U1, p.HL, pL, st_l));
@@ -218,7 +218,7 @@ rnnt_status projections(const Plan& p, const void* hA, const void* hL, const rnn
 // Scores of a chunk on the fp32 path: Hs = Z W^O^T + b^O.
 rnnt_status simt_scores(const Plan& p, const rnnt_params* pr, const float* Z, float* Hs,
                         long long rows, cudaStream_t st) {
-  const int bf = p.dtype == RNNT_BF16;
+  const int bf = p.dtype != RNNT_F32;
   SimtGemm g{};
   g.M = (int)rows; g.N = p.V; g.K = p.H;
   g.A = Z; g.sam = p.H; g.sak = 1; g.a_bf16 = 0;
@@ -490,7 +490,7 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
   float* dLr = (float*)(w + p.w_dLr);
   int32_t* Teff = (int32_t*)(w + p.w_len);
   int32_t* Ueff = Teff + (p.B ? p.B : 1);
-  const int bf = p.dtype == RNNT_BF16;
+  const int bf = p.dtype != RNNT_F32;
   const bool untiled = p.mode == RNNT_UNTILED;
 
   // Outputs are overwritten; accumulated ones start from zero (one launch).

@@ -1798,8 +1798,6 @@ int pick_splits(int units_mn, int K) {
 // ===========================================================================
 // Entry points used by the C ABI (tc.h).
 
-bool tc_path_enabled() { return true; }
-
 rnnt_status tc_check_shape(const Plan& p) {
   if (p.H % 8 || p.V % 8 || p.HA % 8 || p.HL % 8) return RNNT_ERR_UNSUPPORTED_SHAPE;
   // e4m3 rows of H bytes: TMA strides are multiples of 16 bytes

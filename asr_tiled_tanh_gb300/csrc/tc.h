@@ -5,8 +5,6 @@
 
 namespace rnnt {
 
-// True when this build runs RNNT_BF16 problems on the tensor-core kernels.
-bool tc_path_enabled();
 // RNNT_OK or RNNT_ERR_UNSUPPORTED_SHAPE for shapes the tensor-core kernels cannot take.
 rnnt_status tc_check_shape(const Plan& p);
 // out[M,H] = X[M,K] W[H,K]^T (+ bias[H]), bf16 operands, fp32 result.

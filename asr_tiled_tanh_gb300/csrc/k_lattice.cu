@@ -13,6 +13,7 @@
 // moves by warp shuffles.  The log-probabilities of the diagonals ahead are
 // prefetched into a register ring so the front never waits on a global load.
 #include <algorithm>
+#include <atomic>
 
 #include "kernels.h"
 
@@ -594,27 +595,31 @@ template <int NJ, bool FAST, int W>
 static cudaError_t launch_ab_smem(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
                                   SavedView sv, float* loss, int R, size_t smem,
                                   cudaStream_t s) {
-  static bool attr[kDeviceSlots] = {};  // per instantiation and device
-  bool& done = attr[device_slot()];
-  if (!done) {
+  static std::atomic<bool> attr[kDeviceSlots];  // per instantiation and device
+  std::atomic<bool>& done = attr[device_slot()];
+  if (!done.load()) {
     cudaError_t e = cudaFuncSetAttribute(k_alpha_beta_smem<NJ, FAST, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
-    done = true;
+    done.store(true);
   }
   k_alpha_beta_smem<NJ, FAST, W><<<dim3(sh.B, 2), 32 * W, smem, s>>>(sh, T_len, U_len, sv, loss,
                                                                        R);
   return cudaGetLastError();
 }
 
-static int sm_count() {
-  static int count[kDeviceSlots] = {};
-  int& n = count[device_slot()];
+int num_sms() {
+  static std::atomic<int> count[kDeviceSlots];
+  std::atomic<int>& cached = count[device_slot()];
+  int n = cached.load();
   if (n == 0) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();  // (no device: clear the error state)
+      n = 152;
+    }
+    cached.store(n);
   }
   return n;
 }
@@ -647,12 +652,12 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
   const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float) + 2 * 4 * sizeof(float);
   const int nj = (int)cdiv(sh.U1, 32);
   const long long per_sm = std::max<long long>(1, (228LL * 1024) / (long long)(smem + 1024));
-  const bool few_waves = 2LL * sh.B <= 2LL * per_sm * sm_count();
+  const bool few_waves = 2LL * sh.B <= 2LL * per_sm * num_sms();
   if (smem <= 220 * 1024 && nj <= 4 && few_waves) {
     // warps per sample and direction: one label position per lane when the
     // 2B recursions leave most SMs idle, else one warp (several positions each)
     int w = 1;
-    if (nj > 1 && 2LL * sh.B * nj <= 2LL * sm_count()) w = nj <= 2 ? 2 : 4;
+    if (nj > 1 && 2LL * sh.B * nj <= 2LL * num_sms()) w = nj <= 2 ? 2 : 4;
     return fast ? launch_ab_smem_nj<true>(sh, T_len, U_len, sv, loss, R, smem, w, s)
                 : launch_ab_smem_nj<false>(sh, T_len, U_len, sv, loss, R, smem, w, s);
   }

@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -1406,13 +1407,13 @@ cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const flo
                                    : k_dh_kept_stream_bf16<DHK_GROUPS_MAX>);
     // dynamic plus static shared memory pass the 48 KiB default: opt in once
     // per instantiation to the largest ring
-    static bool opted[3][kDeviceSlots] = {};
-    bool& done = opted[ng <= 1 ? 0 : (ng <= 2 ? 1 : 2)][device_slot()];
-    if (!done) {
+    static std::atomic<bool> opted[3][kDeviceSlots];
+    std::atomic<bool>& done = opted[ng <= 1 ? 0 : (ng <= 2 ? 1 : 2)][device_slot()];
+    if (!done.load()) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                DHK_STAGES * DHK_CHUNK_MAX) != cudaSuccess)
         return cudaErrorInvalidValue;
-      done = true;
+      done.store(true);
     }
     kern<<<(unsigned)c.ntiles, groups * S, smem, s>>>(c, Hs, post, dbO, groups, R, stage_bytes);
     return cudaGetLastError();
@@ -1421,17 +1422,6 @@ cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const flo
   return cudaGetLastError();
 }
 
-int num_sms() {
-  static int count[kDeviceSlots] = {};
-  int& n = count[device_slot()];
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 // out[n] += sum over rows of a bf16 [R][N] matrix (N % 8 == 0).  A block is
 // 8 row groups x 32 threads; each thread sums 8 consecutive columns (one
@@ -1685,15 +1675,15 @@ cudaError_t launch_gemm_t(const GemmDesc& g, TcParams p, cudaStream_t s) {
   // other epilogues never read the third map
   CUtensorMap tc = ta;
   if (box_store(EPI) && !make_tmap_store32(&tc, p.Hout, g.M, g.N)) return cudaErrorInvalidValue;
-  static bool opted_in[kDeviceSlots] = {};  // per instantiation and device
-  bool& opted = opted_in[device_slot()];
-  if (!opted) {
+  static std::atomic<bool> opted_in[kDeviceSlots];  // per instantiation and device
+  std::atomic<bool>& opted = opted_in[device_slot()];
+  if (!opted.load()) {
     // up to the per-block maximum: the score epilogues' bias copy goes behind
     // the kernel's own layout when it fits
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_LIMIT);
     if (e != cudaSuccess) return e;
-    opted = true;
+    opted.store(true);
   }
   int smem_bytes = C::SMEM;
   p.sbias = 0;

@@ -5,6 +5,9 @@
 namespace rnnt {
 
 // ---- lattice bookkeeping and the loss recursion (k_lattice.cu) -----------
+// Multiprocessor count of the current device (cached per device; 152 when
+// the query fails).
+int num_sms();
 cudaError_t launch_fill_f32(float* p, float v, size_t n, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 // Zero up to 8 buffers (16-byte aligned pointers) in one launch; NULL entries are skipped.

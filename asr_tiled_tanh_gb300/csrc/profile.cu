@@ -1,4 +1,6 @@
 // profile.cu -- per-kernel CUDA-event timing sessions (include/rnnt_profile.h).
+#include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -8,9 +10,9 @@
 namespace rnnt {
 namespace {
 struct Session {
-  bool open = false;
+  std::atomic<bool> open{false};
   int capacity = 0;
-  int used = 0;
+  std::atomic<int> used{0};  // brackets handed out (may pass capacity)
   std::vector<cudaEvent_t> ev;       // 2 per launch
   std::vector<const char*> name;     // per bracket
   std::vector<int> kernels;          // kernel launches inside each bracket
@@ -24,11 +26,14 @@ struct Entry {
 std::vector<Entry> g_last;
 }  // namespace
 
-bool prof_enabled() { return g_sess.open; }
+bool prof_enabled() { return g_sess.open.load(); }
 
+// Calls from several threads take distinct slots.
 ProfScope::ProfScope(const char* name, cudaStream_t s) : slot_(-1), s_(s) {
-  if (!g_sess.open || g_sess.used >= g_sess.capacity) return;
-  slot_ = g_sess.used++;
+  if (!g_sess.open.load()) return;
+  const int slot = g_sess.used.fetch_add(1);
+  if (slot >= g_sess.capacity) return;
+  slot_ = slot;
   g_sess.name[slot_] = name;
   g_sess.kernels[slot_] = 1;
   cudaEventRecord(g_sess.ev[2 * slot_], s);
@@ -49,7 +54,7 @@ using namespace rnnt;
 extern "C" {
 
 rnnt_status rnnt_profile_start(int capacity) {
-  if (capacity < 1 || g_sess.open) return RNNT_ERR_INVALID_ARG;
+  if (capacity < 1 || g_sess.open.load()) return RNNT_ERR_INVALID_ARG;
   g_sess.ev.assign(2 * (size_t)capacity, nullptr);
   g_sess.name.assign(capacity, nullptr);
   g_sess.kernels.assign(capacity, 1);
@@ -62,17 +67,18 @@ rnnt_status rnnt_profile_start(int capacity) {
     }
   }
   g_sess.capacity = capacity;
-  g_sess.used = 0;
-  g_sess.open = true;
+  g_sess.used.store(0);
+  g_sess.open.store(true);
   return RNNT_OK;
 }
 
 int rnnt_profile_stop(void) {
-  if (!g_sess.open) return -1;
-  g_sess.open = false;
+  if (!g_sess.open.load()) return -1;
+  g_sess.open.store(false);
   g_last.clear();
   int rc = 0;
-  for (int i = 0; i < g_sess.used && rc == 0; ++i) {
+  const int used = std::min(g_sess.used.load(), g_sess.capacity);
+  for (int i = 0; i < used && rc == 0; ++i) {
     float ms = 0.f;
     if (cudaEventSynchronize(g_sess.ev[2 * i + 1]) != cudaSuccess ||
         cudaEventElapsedTime(&ms, g_sess.ev[2 * i], g_sess.ev[2 * i + 1]) != cudaSuccess) {

@@ -7,8 +7,10 @@
  * stream, so the device time of each step can be summed by name after the
  * fact.  A bracket holds one kernel launch, except the encoder-gradient
  * steps (tc_enc_prep, tc_enc_grads), which hold up to four and five.  Recording an event is asynchronous; nothing is
- * synchronized until rnnt_profile_stop.  Sessions are process-wide and not
- * thread-safe.  Events are created by rnnt_profile_start (no device memory
+ * synchronized until rnnt_profile_stop.  Sessions are process-wide: library
+ * calls from several host threads may record into an open session (each
+ * bracket takes its own slot), but rnnt_profile_start and rnnt_profile_stop
+ * must not run while a library call is in progress.  Events are created by rnnt_profile_start (no device memory
  * is allocated for them) and destroyed by rnnt_profile_stop.
  */
 #ifndef RNNT_GB300_PROFILE_H

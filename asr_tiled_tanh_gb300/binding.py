@@ -25,10 +25,11 @@ RNNT_F32, RNNT_BF16, RNNT_BF16_E4M3 = 0, 1, 2
 DTYPES = {"f32": RNNT_F32, "bf16": RNNT_BF16, "bf16-e4m3": RNNT_BF16_E4M3}
 RNNT_TILED, RNNT_UNTILED = 0, 1
 
-# Every symbol include/rnnt.h declares.
+# Every function include/rnnt.h and include/rnnt_profile.h declare (the test
+# hooks of include/rnnt_testing.h are called by their own tests).
 EXPORTS = ("rnnt_saved_bytes", "rnnt_saved_layout", "rnnt_workspace_bytes",
            "rnnt_graph_capturable", "rnnt_tile_cells_for_budget", "rnnt_fwd", "rnnt_bwd",
-           "rnnt_bwd_ex", "rnnt_fwd_bwd",
+           "rnnt_bwd_ex", "rnnt_fwd_bwd", "rnnt_fwd_noalloc",
            "rnnt_device_status",
            "rnnt_status_string", "rnnt_profile_start", "rnnt_profile_stop", "rnnt_profile_entry")
 
@@ -102,6 +103,8 @@ def load(build_if_missing: bool = False):
     lib.rnnt_fwd_bwd.restype = ctypes.c_int
     lib.rnnt_fwd_bwd.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P, P,
                                  P, P, P, P, P, P, P, P, S, P]
+    lib.rnnt_fwd_noalloc.restype = ctypes.c_int
+    lib.rnnt_fwd_noalloc.argtypes = [D, P, P, ctypes.POINTER(RnntParams), P, P, P, P, P, P]
     lib.rnnt_device_status.restype = ctypes.c_int
     lib.rnnt_device_status.argtypes = [D, P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.rnnt_status_string.restype = ctypes.c_char_p
@@ -235,6 +238,16 @@ def rnnt_fwd_bwd(dims, hA, hL, params: RnntParams, labels, T_len, U_len, loss, g
                                _stream(stream))
     if check:
         _check(code, "rnnt_fwd_bwd")
+    return code
+
+
+def rnnt_fwd_noalloc(dims, hA, hL, params: RnntParams, labels, T_len, U_len, loss, saved,
+                     stream=None, check=True) -> int:
+    code = load().rnnt_fwd_noalloc(ctypes.byref(dims), _p(hA), _p(hL), ctypes.byref(params),
+                                   _p(labels), _p(T_len), _p(U_len), _p(loss), _p(saved),
+                                   _stream(stream))
+    if check:
+        _check(code, "rnnt_fwd_noalloc")
     return code
 
 

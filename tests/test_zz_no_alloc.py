@@ -9,27 +9,20 @@ that every call gives what rnnt_fwd gives with a fresh caller-provided
 workspace; it runs last (file name) so that a failure here never hides the
 rest of the suite, and it needs no earlier test's state.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
 
 import asr_tiled_tanh_gb300 as rn
-from asr_tiled_tanh_gb300 import binding, synthetic
+from asr_tiled_tanh_gb300 import synthetic
 from tests.helpers import TOL, to_device
 
 pytestmark = pytest.mark.gpu
 
 
-def _noalloc_fn():
-    lib = rn.load(build_if_missing=True)
-    f = lib.rnnt_fwd_noalloc
-    P = ctypes.c_void_p
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.POINTER(binding.RnntDims), P, P, ctypes.POINTER(binding.RnntParams),
-                  P, P, P, P, P, P]
-    return f
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rn.load(build_if_missing=True)
 
 
 def _saved_state(r):
@@ -37,18 +30,16 @@ def _saved_state(r):
     return {k: getattr(sa, k).clone() for k in ("lnP", "lpb", "lpl", "lnPD", "alpha", "beta")}
 
 
-def _call_noalloc(f, r, dev, params, B):
+def _call_noalloc(r, dev, params, B):
     loss = torch.full((B,), float("nan"), device="cuda")
-    stream = torch.cuda.current_stream().cuda_stream
-    code = f(ctypes.byref(r.dims), dev["hA"].data_ptr(), dev["hL"].data_ptr(),
-             ctypes.byref(params), dev["labels"].data_ptr(), dev["T_len"].data_ptr(),
-             dev["U_len"].data_ptr(), loss.data_ptr(), r.saved.data_ptr(), stream)
+    code = rn.rnnt_fwd_noalloc(r.dims, dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"],
+                               dev["U_len"], loss, r.saved, check=False)
     assert code == 0, rn.rnnt_status_string(code)
     torch.cuda.synchronize()
     return loss
 
 
-def _check_against_rnnt_fwd(f, inp, tile_cells, tag):
+def _check_against_rnnt_fwd(inp, tile_cells, tag):
     """One rnnt_fwd_noalloc call against rnnt_fwd with a fresh caller workspace."""
     dtype = inp.wl.dtype
     dev = to_device(inp)
@@ -60,7 +51,7 @@ def _check_against_rnnt_fwd(f, inp, tile_cells, tag):
     assert ref.status() == (0, 0)
     ref_state = _saved_state(ref)
     r = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)  # fresh `saved`; scratch from the library
-    loss = _call_noalloc(f, r, dev, params, inp.wl.B)
+    loss = _call_noalloc(r, dev, params, inp.wl.B)
     assert r.status() == (0, 0)
     tl = TOL[dtype][0]
     got, want = loss.double().cpu().numpy(), ref_loss.double().cpu().numpy()
@@ -81,7 +72,6 @@ def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(dtype):
     # lattice); then a plan of several chunks (small tile buffers), so that
     # every chunk reuses tile buffers the previous one wrote.
     H, V = (128, 256) if dtype == "bf16" else (64, 96)
-    f = _noalloc_fn()
     cases = [
         (synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=23,
                           bias_std=0.1), 0, "first"),
@@ -92,15 +82,14 @@ def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(dtype):
                           bias_std=0.1), 3 * 128, "three tiles per chunk"),
     ]
     for inp, tile_cells, tag in cases:
-        _check_against_rnnt_fwd(f, inp, tile_cells, tag)
+        _check_against_rnnt_fwd(inp, tile_cells, tag)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    f = _noalloc_fn()
     # the large-batch 40 s workload needs far more than the fixed scratch
     dims = rn.make_dims(1024, 1000, 101, 512, 512, 512, 4096, 0, rn.RNNT_BF16, rn.RNNT_TILED, 0)
     assert rn.rnnt_workspace_bytes(dims) > 32 << 20
     params = rn.make_params(None, None, None, None, None)
-    code = f(ctypes.byref(dims), None, None, ctypes.byref(params), None, None, None, None, None,
-             None)
+    code = rn.rnnt_fwd_noalloc(dims, None, None, params, None, None, None, None, None,
+                               check=False)
     assert code == 3  # RNNT_ERR_WORKSPACE_TOO_SMALL

@@ -39,18 +39,19 @@ def _call_noalloc(r, dev, params, B):
     return loss
 
 
-def _check_against_rnnt_fwd(inp, tile_cells, tag):
+def _check_against_rnnt_fwd(inp, tile_cells, tag, e4m3=False):
     """One rnnt_fwd_noalloc call against rnnt_fwd with a fresh caller workspace."""
     dtype = inp.wl.dtype
     dev = to_device(inp)
     params = rn.make_params(dev["WA"], dev["WL"], dev["bZ"], dev["WO"], dev["bO"])
-    ref = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)
+    ref = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells, e4m3_scores=e4m3)
     assert rn.rnnt_workspace_bytes(ref.dims) <= 32 << 20
     ref_loss = ref.fwd(dev["hA"], dev["hL"], params, dev["labels"], dev["T_len"], dev["U_len"])
     torch.cuda.synchronize()
     assert ref.status() == (0, 0)
     ref_state = _saved_state(ref)
-    r = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells)  # fresh `saved`; scratch from the library
+    # fresh `saved`; scratch from the library
+    r = rn.Rnnt.for_inputs(inp, tile_cells=tile_cells, e4m3_scores=e4m3)
     loss = _call_noalloc(r, dev, params, inp.wl.B)
     assert r.status() == (0, 0)
     tl = TOL[dtype][0]
@@ -64,13 +65,15 @@ def _check_against_rnnt_fwd(inp, tile_cells, tag):
         assert np.allclose(a[fin], b[fin], rtol=tl, atol=tl), (tag, k)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(dtype):
+@pytest.mark.parametrize("mode", ["bf16", "bf16-e4m3", "f32"])
+def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(mode):
     # Three calls in a row share the library's scratch array, each left with
     # the previous call's contents: full-ish lengths; then other values with
     # much shorter lattices (more positions of the same tiles outside every
     # lattice); then a plan of several chunks (small tile buffers), so that
     # every chunk reuses tile buffers the previous one wrote.
+    dtype = "f32" if mode == "f32" else "bf16"
+    e4m3 = mode == "bf16-e4m3"  # (the quantized output layer lives in the scratch too)
     H, V = (128, 256) if dtype == "bf16" else (64, 96)
     cases = [
         (synthetic.custom(B=4, T=60, U=20, HA=H, HL=H, H=H, V=V, dtype=dtype, seed=23,
@@ -82,7 +85,7 @@ def test_noalloc_forward_matches_rnnt_fwd_on_calls_in_a_row(dtype):
                           bias_std=0.1), 3 * 128, "three tiles per chunk"),
     ]
     for inp, tile_cells, tag in cases:
-        _check_against_rnnt_fwd(inp, tile_cells, tag)
+        _check_against_rnnt_fwd(inp, tile_cells, tag, e4m3)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():

@@ -108,6 +108,7 @@ bool make_plan(const rnnt_dims* d, Plan* p) {
     p->w_dLr16 = put(2 * B * U1 * H);
     p->w_hAm = put(2 * B * T * HA);
     p->w_hLm = put(2 * B * U1 * HL);
+    p->w_dbO = put(4 * V);  // db^O accumulated here (16-byte aligned), then copied out
   }
   if (p->f8) {
     p->w_z8 = put(rows * H);              // e4m3(2^8 z) rows of a chunk
@@ -504,10 +505,13 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
     LAUNCH("zero", launch_zero_many(z0, st));
     return RNNT_OK;
   }
+  // tensor-core path: db^O is summed into an aligned workspace vector and
+  // copied to the caller's (any alignment) at the end
+  float* dbO_acc = (p.tc && dbO) ? (float*)(w + p.w_dbO) : dbO;
   // zero the accumulated outputs (one launch) and clamp the lengths
   auto prepare = [&](cudaStream_t st) -> rnnt_status {
     ZeroList z{};
-    void* ps[7] = {dWO, dbO, dbZ, dA, dLr, dWA, dWL};
+    void* ps[7] = {dWO, dbO_acc, dbZ, dA, dLr, dWA, dWL};
     size_t bs[7] = {sizeof(float) * (size_t)p.V * p.H, sizeof(float) * (size_t)p.V,
                     sizeof(float) * (size_t)p.H, sizeof(float) * (size_t)p.B * p.T * p.H,
                     sizeof(float) * (size_t)p.B * p.U1 * p.H, sizeof(float) * (size_t)p.H * p.HA,
@@ -537,9 +541,13 @@ rnnt_status rnnt::bwd_impl(const rnnt_dims* dims, const void* hA, const void* hL
                               eout, es);
     };
     s = tc_backward_tiles(p, sv, pr, labels, T_len, U_len, grad_loss, pA, pL, Z, Hs, untiled,
-                          z_resident, dA, dLr, dWO, dbO, (float4*)(w + p.w_post),
+                          z_resident, dA, dLr, dWO, dbO_acc, (float4*)(w + p.w_post),
                           p.f8 ? &f8 : nullptr, &pre, &enc, st);
-    return s;
+    if (s != RNNT_OK) return s;
+    if (dbO)
+      RNNT_CHECK(cudaMemcpyAsync(dbO, dbO_acc, sizeof(float) * (size_t)p.V,
+                                 cudaMemcpyDeviceToDevice, st));
+    return RNNT_OK;
   }
 
   s = prepare(st);

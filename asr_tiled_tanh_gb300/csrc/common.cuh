@@ -60,7 +60,7 @@ struct Plan {
       s_total;
   // workspace layout
   size_t w_dA, w_dLr, w_z, w_h, w_dz, w_post, w_dA16, w_dLr16, w_hAm, w_hLm, w_z8, w_wo8,
-      w_wodq, w_nscale, w_len, w_total;
+      w_wodq, w_nscale, w_dbO, w_len, w_total;
 };
 
 // Header words at saved + s_status.

@@ -1423,43 +1423,9 @@ cudaError_t launch_dh_kept_bf16(const ChunkArgs& c, __nv_bfloat16* Hs, const flo
 }
 
 
-// out[n] += sum over rows of a bf16 [R][N] matrix (N % 8 == 0).  A block is
-// 8 row groups x 32 threads; each thread sums 8 consecutive columns (one
+// out[n] += sum over rows of an fp32 [R][N] matrix (N % 4 == 0).  A block is
+// 8 row groups x 32 threads; each thread sums 4 consecutive columns (one
 // 16-byte load per row), so a warp reads 512 contiguous bytes of a row.
-__global__ void __launch_bounds__(256)
-k_colsum_bf16(const __nv_bfloat16* __restrict__ X, long long R, int N, float* __restrict__ out,
-              long long rows_per, const int32_t* __restrict__ tiles_total, long long first_tile) {
-  __shared__ float part[8][256];
-  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
-  const int c0 = (blockIdx.x * 32 + lane) * 8;
-  // rows of tiles past the batch's last one hold nothing
-  if (tiles_total) R = min(R, max(0LL, ((long long)*tiles_total - first_tile) * TILE));
-  const long long r0 = (long long)blockIdx.y * rows_per;
-  const long long r1 = min(R, r0 + rows_per);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (c0 < N) {
-    for (long long r = r0 + grp; r < r1; r += 8) {
-      const uint4 q = __ldg((const uint4*)(X + r * N + c0));
-      acc[0] += ptx::bf16lo(q.x); acc[1] += ptx::bf16hi(q.x);
-      acc[2] += ptx::bf16lo(q.y); acc[3] += ptx::bf16hi(q.y);
-      acc[4] += ptx::bf16lo(q.z); acc[5] += ptx::bf16hi(q.z);
-      acc[6] += ptx::bf16lo(q.w); acc[7] += ptx::bf16hi(q.w);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) part[grp][lane * 8 + k] = acc[k];
-  __syncthreads();
-  const int c = blockIdx.x * 256 + threadIdx.x;
-  if (c < N) {
-    float sum = 0.f;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) sum += part[g][threadIdx.x];
-    if (sum != 0.f) atomicAdd(out + c, sum);
-  }
-}
-
-// out[n] += sum over rows of an fp32 [R][N] matrix (N % 4 == 0); same layout
-// as k_colsum_bf16 with 4 columns (one 16-byte load) per thread.
 __global__ void __launch_bounds__(256)
 k_colsum_f32v(const float* __restrict__ X, long long R, int N, float* __restrict__ out,
               long long rows_per) {
@@ -1499,19 +1465,6 @@ cudaError_t launch_colsum_f32v(const float* X, long long R, int N, float* out, c
   long long rows_per = cdiv(R, slabs);
   if (cdiv(R, rows_per) > 65535) rows_per = cdiv(R, 65535);
   k_colsum_f32v<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_colsum_bf16(const __nv_bfloat16* X, long long R, int N, float* out,
-                               cudaStream_t s, const int32_t* tiles_total = nullptr,
-                               long long first_tile = 0) {
-  if (R <= 0 || N <= 0) return cudaSuccess;
-  const int strips = (int)cdiv(N, 256);
-  long long slabs = std::max<long long>(1, (long long)num_sms() * 4 / strips);
-  long long rows_per = cdiv(R, slabs);
-  if (cdiv(R, rows_per) > 65535) rows_per = cdiv(R, 65535);
-  k_colsum_bf16<<<dim3(strips, (unsigned)cdiv(R, rows_per)), 256, 0, s>>>(X, R, N, out, rows_per,
-                                                                          tiles_total, first_tile);
   return cudaGetLastError();
 }
 
@@ -1917,9 +1870,9 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
       tp.n_split = 4;
       tp.n_split_auto = 1;
       tp.status = sv.status;
-      // db^O: column sums of dh formed in the same epilogue (vector
-      // reductions need a 16-byte aligned db^O)
-      if (dbO && ((uintptr_t)dbO & 15) == 0) tp.dbO = dbO;
+      // db^O: column sums of dh formed in the same epilogue (into a 16-byte
+      // aligned workspace vector)
+      tp.dbO = dbO;
       tp.tiles_on = TILES_ON_M;
       if (launch_gemm<EPI_DH>(g, tp, 256, s) != cudaSuccess) return RNNT_ERR_CUDA;
     } else {
@@ -1928,17 +1881,9 @@ rnnt_status tc_backward_tiles(const Plan& p, const SavedView& sv, const rnnt_par
         k_posteriors<<<(unsigned)c.ntiles, TILE, 0, s>>>(c, grad_loss, post);
         if (cudaGetLastError() != cudaSuccess) return RNNT_ERR_CUDA;
       }
-      // dh over the kept scores, db^O in the same pass (16-byte aligned db^O)
+      // dh over the kept scores, db^O in the same pass
       ProfScope ps("tc_dh_kept", s);
-      if (launch_dh_kept_bf16(c, Hs, post, dbO && ((uintptr_t)dbO & 15) == 0 ? dbO : nullptr,
-                              s) != cudaSuccess)
-        return RNNT_ERR_CUDA;
-    }
-    if (dbO && ((uintptr_t)dbO & 15) != 0) {
-      // db^O += sum over the chunk's positions of dh (rows outside are 0)
-      ProfScope ps("tc_colsum_dh", s);
-      if (launch_colsum_bf16(Hs, rows, p.V, dbO, s, sv.total_tiles, c.first_tile) != cudaSuccess)
-        return RNNT_ERR_CUDA;
+      if (launch_dh_kept_bf16(c, Hs, post, dbO, s) != cudaSuccess) return RNNT_ERR_CUDA;
     }
     {  // dz = dh W^O, da = dz (1 - z^2) reduced into dA and dLr
       ProfScope ps("tc_bwd_dz", s);

@@ -39,7 +39,8 @@ def _lib():
     rn.load(build_if_missing=True)
 
 
-def test_quantizer_matches_the_host_reference_bit_for_bit():
+@pytest.mark.parametrize("case", ["spread", "zero block"])
+def test_quantizer_matches_the_host_reference_bit_for_bit(case):
     g = torch.Generator().manual_seed(7)
     V, H = 1000, 512   # four blocks, the last one ragged
     WO = (torch.randn(V, H, generator=g) / H ** 0.5)
@@ -47,6 +48,8 @@ def test_quantizer_matches_the_host_reference_bit_for_bit():
     WO[512:768] *= 1e-3
     WO[768:] = 0.0
     WO[999, 3] = 5e-3   # a lone value in an otherwise empty block
+    if case == "zero block":
+        WO[512:768] = 0.0   # an all-zero block: scale 1, every byte 0
     WO = WO.to(torch.bfloat16)
     q_ref, Wq_ref, s_ref = e4m3ref.quantize_wo(WO)
     dev = WO.cuda()

@@ -559,6 +559,159 @@ __device__ __forceinline__ void ab_walk(float* ring, float* xch, int R, int Tb, 
 // w owns u = NJ (32 w + l) ..); with W > 1 the warps meet at a barrier once
 // per diagonal.  Several warps pay off when there are few samples (the
 // recursion is latency-bound, and the GPU otherwise runs 2B warps).
+// ---------------------------------------------------------------------------
+// The recursion for batches whose walks outnumber the SMs: instead of whole
+// rows (the ring above needs room for U1 + 64 rows of the lattice, one walk
+// per SM at U1 = 101), a walk keeps only the next KD diagonals of its
+// sample's log-probabilities in shared memory, double-buffered: two bands of
+// KD x 32 NJ entries per array.  A band is filled by cp.async from row
+// segments: for row t the diagonals d0 .. d0+KD-1 of the band hold KD
+// consecutive label positions u = d - t, so the lanes of a warp copy 32/KD
+// contiguous row pieces per instruction (the register-prefetch walk reads 32
+// rows per instruction).  Entry (d, u) sits at [d - d0][u % NJ][u / NJ], so
+// that the lanes, which own u = NJ lane + j, read consecutive words.
+constexpr int AB_KD = 8;  // diagonals per band
+
+template <int NJ, bool FAST, bool BETA>
+__device__ __forceinline__ void ab_walk_band(float* band, int Tb, int Ub, int U1,
+                                             const float* __restrict__ LPB,
+                                             const float* __restrict__ LPL,
+                                             float* __restrict__ OUT, float* lnP, float* loss) {
+  constexpr int KD = AB_KD, UP = 32 * NJ, BAND = KD * UP;
+  const int lane = threadIdx.x & 31;
+  const int ndiag = Tb + Ub;
+  const int nband = (ndiag + KD - 1) / KD;
+  constexpr float kIn = FAST ? 1.4426950408889634f : 1.f;
+  constexpr float kOut = FAST ? 0.6931471805599453f : 1.f;
+  // band b holds walk steps s in [b KD, b KD + KD): diagonals from its lowest
+  // one, dlo(b) (alpha: d = s; beta: d = ndiag - 1 - s), possibly below 0
+  auto band_lo = [&](int b) { return BETA ? ndiag - (b + 1) * KD : b * KD; };
+  auto load_band = [&](int b) {
+    float* dst = band + (b & 1) * 2 * BAND;  // the band's lpb entries, then its lpl ones
+    const int d0 = band_lo(b);
+    const int t0 = max(0, d0 - Ub), t1 = min(Tb - 1, d0 + KD - 1);
+    const int n = (t1 - t0 + 1) * KD;
+    for (int i = lane; i < n; i += 32) {
+      const int t = t0 + i / KD, c = i % KD, d = d0 + c, u = d - t;
+      if (d >= 0 && d < ndiag && u >= 0 && u <= Ub) {
+        const int k = c * UP + (u % NJ) * 32 + u / NJ;
+        cp_async4(dst + k, LPB + (size_t)t * U1 + u);
+        cp_async4(dst + BAND + k, LPL + (size_t)t * U1 + u);
+      }
+    }
+    cp_async_commit();
+  };
+  load_band(0);
+  if (nband > 1) load_band(1); else cp_async_commit();
+  cp_async_wait<1>();
+  __syncwarp();
+
+  const int u0 = NJ * lane;
+  const int d0 = BETA ? ndiag - 1 : 0;
+  int t[NJ], oo[NJ];
+  bool uok[NJ], ulast[NJ];
+  float own[NJ], send[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const int u = u0 + j;
+    uok[j] = u <= Ub;
+    ulast[j] = u == Ub;
+    t[j] = d0 - u;
+    oo[j] = t[j] * U1 + u;
+    own[j] = send[j] = -INFINITY;
+  }
+
+  for (int s = 0; s < ndiag; ++s) {
+    const int b = s / KD, c = s - b * KD;
+    if (c == 0 && b > 0) {
+      // entering band b: every lane is done with band b-1, whose buffer takes
+      // band b+1; band b (issued one band ago) is complete after the wait
+      __syncwarp();
+      if (b + 1 < nband) load_band(b + 1); else cp_async_commit();
+      cp_async_wait<1>();
+      __syncwarp();
+    }
+    const float* cur = band + (b & 1) * 2 * BAND + (BETA ? KD - 1 - c : c) * UP + lane;
+    float nb[NJ];
+    if (!BETA) {
+      const float x = __shfl_up_sync(0xffffffffu, send[NJ - 1], 1);
+      nb[0] = lane > 0 ? x : -INFINITY;
+#pragma unroll
+      for (int j = 1; j < NJ; ++j) nb[j] = send[j - 1];
+    } else {
+      const float x = __shfl_down_sync(0xffffffffu, send[0], 1);
+      nb[NJ - 1] = lane < 31 ? x : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NJ - 1; ++j) nb[j] = send[j + 1];
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const bool in = uok[j] && (unsigned)t[j] < (unsigned)Tb;
+      const float lb = in ? cur[j * 32] * kIn : -INFINITY;
+      const float ll = in ? cur[BAND + j * 32] * kIn : -INFINITY;
+      float val;
+      if (!BETA) {
+        val = (s == 0) ? 0.f : lae_k<FAST>(own[j], nb[j]);
+      } else {
+        const float from_t = (t[j] + 1 < Tb) ? own[j] : (ulast[j] ? 0.f : -INFINITY);
+        val = lae_k<FAST>(from_t + lb, nb[j] + ll);
+      }
+      val = in ? val : -INFINITY;
+      if (in) OUT[oo[j]] = val * kOut;
+      if (!BETA) {
+        own[j] = val + lb;   // alpha + lpb: the blank move to (t+1, u)
+        send[j] = val + ll;  // alpha + lpl: the label move to (t, u+1)
+        ++t[j];
+        oo[j] += U1;
+      } else {
+        own[j] = val;
+        send[j] = val;
+        --t[j];
+        oo[j] -= U1;
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (!BETA) {
+    // ln P = alpha(T_b-1, U_b) + lpb(T_b-1, U_b): the own value at u = U_b
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (ulast[j]) {
+        *lnP = own[j] * kOut;
+        *loss = -own[j] * kOut;
+      }
+    }
+  }
+}
+
+template <int NJ, bool FAST>
+__global__ void __launch_bounds__(32)
+k_alpha_beta_band(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
+                  SavedView sv, float* __restrict__ loss) {
+  __shared__ float band[2 * 2 * AB_KD * 32 * NJ];
+  const int b = blockIdx.x;
+  if (sv.prefix[b + 1] == sv.prefix[b]) return;  // rejected sample
+  const int Tb = T_len[b], Ub = U_len[b];
+  const size_t base = (size_t)b * sh.T * sh.U1;
+  if (blockIdx.y == 0)
+    ab_walk_band<NJ, FAST, false>(band, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                                  sv.alpha + base, sv.lnP + b, loss + b);
+  else
+    ab_walk_band<NJ, FAST, true>(band, Tb, Ub, sh.U1, sv.lpb + base, sv.lpl + base,
+                                 sv.beta + base, nullptr, nullptr);
+}
+
+template <bool FAST>
+static cudaError_t launch_ab_band(const Shape& sh, const int32_t* T_len, const int32_t* U_len,
+                                  SavedView sv, float* loss, cudaStream_t s) {
+  const int nj = (int)cdiv(sh.U1, 32);
+  const dim3 g(sh.B, 2);
+  if (nj <= 1) k_alpha_beta_band<1, FAST><<<g, 32, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else if (nj <= 2) k_alpha_beta_band<2, FAST><<<g, 32, 0, s>>>(sh, T_len, U_len, sv, loss);
+  else k_alpha_beta_band<4, FAST><<<g, 32, 0, s>>>(sh, T_len, U_len, sv, loss);
+  return cudaGetLastError();
+}
+
 template <int NJ, bool FAST, int W>
 __global__ void __launch_bounds__(32 * W)
 k_alpha_beta_smem(Shape sh, const int32_t* __restrict__ T_len, const int32_t* __restrict__ U_len,
@@ -644,9 +797,10 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
   if (sh.B == 0) return cudaSuccess;
   if (sh.U1 > 1024) return cudaErrorInvalidValue;
   // shared-memory ring when it fits in 220 KiB and the 2B walks it leaves
-  // resident finish in at most two waves; else the register-prefetch kernel
-  // (two warps per sample, every sample resident at once: at B=1024, U=100
-  // the ring allows one walk per SM, 13.5 waves, 4.4 ms against 2.8 ms)
+  // resident finish in at most two waves; more walks take the band kernel
+  // (16 KiB per walk, every walk resident at once: at B=1024, U=100 the ring
+  // allows one walk per SM, 13.5 waves), or the register-prefetch kernel when
+  // U1 > 128
   int R = AB_W;
   while (R < ((int)cdiv(sh.U1, AB_W) + 2) * AB_W) R *= 2;
   const size_t smem = (size_t)2 * R * sh.U1 * sizeof(float) + 2 * 4 * sizeof(float);
@@ -661,6 +815,9 @@ cudaError_t launch_alpha_beta(const Shape& sh, const int32_t* T_len, const int32
     return fast ? launch_ab_smem_nj<true>(sh, T_len, U_len, sv, loss, R, smem, w, s)
                 : launch_ab_smem_nj<false>(sh, T_len, U_len, sv, loss, R, smem, w, s);
   }
+  if (nj <= 4)
+    return fast ? launch_ab_band<true>(sh, T_len, U_len, sv, loss, s)
+                : launch_ab_band<false>(sh, T_len, U_len, sv, loss, s);
   return fast ? launch_ab<true>(sh, T_len, U_len, sv, loss, s)
               : launch_ab<false>(sh, T_len, U_len, sv, loss, s);
 }

@@ -77,6 +77,24 @@ def test_fp32_long_label_sequences_split_over_warps():
         np.testing.assert_allclose(gpu["lpl"][ml], orc.lpl[ml], rtol=2e-5, atol=2e-5)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_alpha_beta_of_many_samples(dtype):
+    # more walks (2B = 320) than the shared-memory ring at U+1 = 101 keeps
+    # resident: the band-buffered walk, alpha and beta against the oracle
+    # (bf16: 64-wide scores; at H = 16 a score sums too few rounded products
+    # for the bf16 value tolerance of the saved log-probabilities)
+    H = 16 if dtype == "f32" else 64
+    inp = synthetic.custom(B=160, T=21, U=100, HA=H, HL=H, H=H, V=H, dtype=dtype, seed=77,
+                           t_frac=0.2, u_frac=0.05, bias_std=0.2)
+    gpu = run_gpu(inp, want_grad=False)
+    orc = run_oracle(inp, want_grad=False)
+    assert_parity(gpu, orc, inp, grads=False)
+    if dtype == "f32":
+        m = valid_mask(inp)
+        for k in ("alpha", "beta"):
+            np.testing.assert_allclose(gpu[k][m], getattr(orc, k)[m], rtol=2e-5, atol=2e-5)
+
+
 def test_small_bf16_workload():
     inp = synthetic.make("small")
     gpu = run_gpu(inp)

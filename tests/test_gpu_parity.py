@@ -77,14 +77,16 @@ def test_fp32_long_label_sequences_split_over_warps():
         np.testing.assert_allclose(gpu["lpl"][ml], orc.lpl[ml], rtol=2e-5, atol=2e-5)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_alpha_beta_of_many_samples(dtype):
-    # more walks (2B = 320) than the shared-memory ring at U+1 = 101 keeps
-    # resident: the band-buffered walk, alpha and beta against the oracle
+@pytest.mark.parametrize("dtype,B,T,U", [("f32", 160, 21, 100), ("bf16", 160, 21, 100),
+                                         ("f32", 460, 10, 63), ("f32", 2000, 8, 20)])
+def test_alpha_beta_of_many_samples(dtype, B, T, U):
+    # more walks than the shared-memory ring keeps resident (U+1 = 101: one
+    # per SM; 64: three; 21: thirteen): the band-buffered walk with 4, 2 and 1
+    # label positions per lane, alpha and beta against the oracle
     # (bf16: 64-wide scores; at H = 16 a score sums too few rounded products
     # for the bf16 value tolerance of the saved log-probabilities)
     H = 16 if dtype == "f32" else 64
-    inp = synthetic.custom(B=160, T=21, U=100, HA=H, HL=H, H=H, V=H, dtype=dtype, seed=77,
+    inp = synthetic.custom(B=B, T=T, U=U, HA=H, HL=H, H=H, V=H, dtype=dtype, seed=77 + U,
                            t_frac=0.2, u_frac=0.05, bias_std=0.2)
     gpu = run_gpu(inp, want_grad=False)
     orc = run_oracle(inp, want_grad=False)

@@ -30,7 +30,9 @@ launches them one by one instead.  A second, eager run of the same number of
 steps with every kernel bracketed by CUDA events on its own stream gives the
 per-kernel times (`kernel_shares`, `roofline`) and `gpu_launches`.  A third
 eager run times rnnt_fwd and rnnt_bwd apart (`ms_by_phase`: medians of the
-forward, the backward and their sum, and the median of the timed steps).
+forward, the backward and their sum, and the median of the timed steps).  A bf16
+workload is then timed once more with the score products on e4m3 tensor cores
+(`e4m3_scores`, a secondary line on its own plan; `--no-e4m3-leg` skips it).
 """
 from __future__ import annotations
 
@@ -555,6 +557,35 @@ def run_gpu_bench(args):
         peak_by_tiles[str(_tiles_per_chunk(rn, r.dims))] = \
             round(torch.cuda.max_memory_allocated(dev) / 1e9, 4)
 
+    # --- the same workload with the score products on e4m3 tensor cores --------
+    # A secondary line (`value` is the bf16 path's): RNNT_BF16_E4M3, timed like
+    # the main steps on a plan of its own, so that every default run also
+    # records the reduced-precision option on the same box.
+    e4m3_leg = None
+    if args.e4m3_leg and not e4m3 and wl.dtype == "bf16" and dist is None:
+        graph = run = None
+        r.saved = r.ws = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        r = rn.Rnnt.for_inputs(inp, mode=args.mode, tile_cells=args.tile_cells, device=dev,
+                               e4m3_scores=True)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        code, word = r.status()
+        if code != 0:
+            raise SystemExit(f"device status {code} word {word} (e4m3 scores)")
+        g8 = captured(step) if (not args.eager and rn.rnnt_graph_capturable(r.dims) == 1) \
+            else None
+        ms8, clk8, _, _, _ = timed_region(g8.replay if g8 is not None else step, profile=False)
+        g8 = None
+        ms8 = reduce_max(ms8, dist, dev)
+        e4m3_leg = {"dtype": "bf16+e4m3", "ms_per_step": round(ms8, 4),
+                    "value": round(job_value(nominal, world, ms8), 1), "unit": UNIT,
+                    "scores": "W^O per 256-row block with power-of-two scales, z as e4m3(2^8 z); "
+                              "dz, dW^O and the rest bf16",
+                    "clocks": clk8.summary()}
+
     # --- roofline of the dominant kernel ----------------------------------------
     hbm_peak, tf_burst, tf_sust, peak_src = _peaks()
     # the burst figure for a short timed region, the power-capped sustained
@@ -643,6 +674,7 @@ def run_gpu_bench(args):
         "kernel_ms_per_step": {k: round(v[0] / args.steps, 5) for k, v in
                                sorted(prof.items(), key=lambda kv: -kv[1][0])},
         "profiled_ms_per_step": round(prof_ms, 4),
+        "e4m3_scores": e4m3_leg,
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
     }
@@ -772,6 +804,9 @@ def main():
                     help="step: one rnnt_fwd_bwd call per step; separate: rnnt_fwd + rnnt_bwd")
     ap.add_argument("--scores", default="bf16", choices=["bf16", "e4m3"],
                     help="e4m3: the two score products on e4m3 tensor cores (RNNT_BF16_E4M3)")
+    ap.add_argument("--no-e4m3-leg", dest="e4m3_leg", action="store_false",
+                    help="skip the secondary timing of a bf16 workload with e4m3 scores "
+                         "(`e4m3_scores` in the JSON line)")
     ap.add_argument("--mode", default="tiled", choices=["tiled", "untiled"],
                     help="untiled keeps z and the scores from the forward (no recompute)")
     args = ap.parse_args()

@@ -1,6 +1,7 @@
 """bench.py's GPU arm prints the one JSON line its readers parse (GPU): every
 key, with the roofline object of the dominant kernel, the end-to-end leg, the
-oracle's CPU baseline and the clock record of the timed region."""
+oracle's CPU baseline, the clock record of the timed region and the secondary
+e4m3-scores line."""
 import json
 import os
 import subprocess
@@ -39,3 +40,5 @@ def test_small_workload_line():
     k = d["clocks"]
     assert k["sm_max_mhz"] and "reasons" in k
     assert len(d["peak_hbm_gb_by_tiles_per_chunk"]) == 2  # memory at two tile sizes
+    e8 = d["e4m3_scores"]  # the secondary line with the score products on e4m3
+    assert e8["dtype"] == "bf16+e4m3" and e8["value"] > 0 and e8["unit"] == d["unit"]
